@@ -1,0 +1,286 @@
+"""CPU oracle for DeepSeek-V4 sparse MLA decode attention (fp64, numpy).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this file; only the
+tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` do.
+It shares no code with the CUDA path.
+
+What it computes is the plain definition of the operation, written out in
+float64 with no blocking, fusion or reordering:
+
+for every flattened query token t and head h, over the set V_t of slots the
+token's index row selects,
+
+    l_j   = bmm1_scale * <q[t, h, :], kv_j>                      (natural-log units)
+    O[d]  = bmm2_scale * sum_j e^{l_j} kv_j[d] / (sum_j e^{l_j} + e^{sink_h})
+    LSE2  = log2 sum_j e^{l_j}                                   (sink excluded)
+
+Sources (FlashInfer and vLLM documentation pages):
+
+* trtllm_batch_decode_sparse_mla_dsv4, description (SM100/SM103 paragraph):
+  head dim 512; BF16 or per-tensor FP8 E4M3 query and KV; BF16 output; the
+  first 128 index columns address the SWA pool, the rest the compressed pool;
+  ``sparse_topk_lens`` counts active columns including the 128 SWA ones;
+  ``seq_lens`` bounds the SWA validity window.
+* same page, Parameters: ``bmm1_scale`` (QK and softmax scale), ``bmm2_scale``
+  (VO scale), ``sinks`` (per-head sink logits), ``cum_seq_lens_q`` (varlen
+  query, top-k lengths in flattened token order).
+* cake_sparse_mla_sm120_dsv4_nvfp4_decode, Parameters: -1 masks a slot;
+  ``out_lse`` is the base-2 log-sum-exp; ``attn_sink`` joins the softmax
+  normalisation; ``mid_out`` / ``mid_lse`` are split partials.
+* msa_sparse_decode_attention, description: decode tokens are right-aligned,
+  token i of a request sits at position seq_len - q_len + i.
+* vLLM DeepseekV4FlashInferMLAAttention: FP8 scale folding
+  ``bmm1 = scale * q_scale * kv_scale``, ``bmm2 = kv_scale``.
+
+Readings where the pages are silent (each is listed in the design notes):
+
+* SWA window: SWA column j is valid iff j < min(128, pos + 1), pos being the
+  right-aligned token position.  PARITY UNPINNED by the pages (our reading).
+* A fully masked token yields O = 0 and LSE = -inf.
+* The sink is a natural-log logit, not multiplied by bmm1_scale.
+* LSE2 excludes the sink.  PARITY UNPINNED by the pages (our reading);
+  ``lse_with_sink=True`` gives the other reading.
+* ``sparse_topk_lens`` outside [0, W] is clamped to that range.
+* V = K = the whole 512-wide row.
+* Duplicate indices each count as their own slot.
+* An index < -1 or >= the pool's row count is a caller error: raised by
+  default, or treated as masked with ``invalid_index="mask"``.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+HEAD_DIM = 512
+SWA_COLS = 128
+LN2 = math.log(2.0)
+LOG2E = 1.0 / LN2
+
+
+# --------------------------------------------------------------------------
+# element decoding, from the bit-format definitions
+# --------------------------------------------------------------------------
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 is the upper 16 bits of an IEEE-754 binary32."""
+    wide = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return wide.view(np.float32).astype(np.float64)
+
+
+def _e4m3_value(code: int) -> float:
+    """OCP 8-bit floating point E4M3 ("fn" variant).
+
+    1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent field 0
+    encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; there is no infinity,
+    so the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(bits, dtype=np.uint8)]
+
+
+def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return bf16_to_f64(bits)
+    if dtype == "e4m3":
+        return e4m3_to_f64(bits)
+    raise ValueError(dtype)
+
+
+# --------------------------------------------------------------------------
+# step a1: token metadata
+# --------------------------------------------------------------------------
+
+def token_request(t: int, sum_q: int, batch: int,
+                  cum_seq_lens_q: Optional[np.ndarray]) -> tuple[int, int, int]:
+    """(request b, index i inside the request, q_len of the request).
+
+    Without ``cum_seq_lens_q`` the query is dense ``[batch, q_len, ...]`` with
+    q_len = sum_q / batch.
+    """
+    if cum_seq_lens_q is None:
+        q_len = sum_q // batch
+        return t // q_len, t % q_len, q_len
+    cum = [int(c) for c in cum_seq_lens_q]
+    for b in range(batch):
+        if cum[b] <= t < cum[b + 1]:
+            return b, t - cum[b], cum[b + 1] - cum[b]
+    raise ValueError(f"token {t} is outside cum_seq_lens_q")
+
+
+def token_position(t, sum_q, batch, cum_seq_lens_q, seq_lens) -> int:
+    """Right-aligned absolute position seq_len - q_len + i."""
+    b, i, q_len = token_request(t, sum_q, batch, cum_seq_lens_q)
+    return int(seq_lens[b]) - q_len + i
+
+
+# --------------------------------------------------------------------------
+# step a2: which slots a token reads
+# --------------------------------------------------------------------------
+
+def valid_slots(t: int, *, indices, topk_lens, seq_lens, cum_seq_lens_q,
+                batch: int, swa_rows: int, comp_rows: int,
+                invalid_index: str = "raise") -> list[tuple[int, str, int]]:
+    """List of (column j, pool name, row) that token t attends to, in column order."""
+    sum_q, width = indices.shape
+    n_lim = width if topk_lens is None else min(max(int(topk_lens[t]), 0), width)
+    pos = token_position(t, sum_q, batch, cum_seq_lens_q, seq_lens)
+    w_swa = min(SWA_COLS, max(0, pos + 1))
+    out = []
+    for j in range(n_lim):
+        idx = int(indices[t, j])
+        if idx == -1:
+            continue
+        if j < SWA_COLS:
+            if j >= w_swa:
+                continue
+            pool, rows = "swa", swa_rows
+        else:
+            pool, rows = "comp", comp_rows
+        if not 0 <= idx < rows:
+            if invalid_index == "raise":
+                raise IndexError(f"token {t} column {j}: index {idx} outside {pool} pool of {rows} rows")
+            continue
+        out.append((j, pool, idx))
+    return out
+
+
+# --------------------------------------------------------------------------
+# steps a4-a6 and a9 for one token: masked softmax attention over the slots
+# --------------------------------------------------------------------------
+
+def attend(q_t: np.ndarray, kv: np.ndarray, bmm1: float, bmm2: float,
+           sinks: Optional[np.ndarray], lse_with_sink: bool = False):
+    """q_t [H, 512], kv [n, 512] (both float64) -> (O [H, 512], LSE2 [H])."""
+    H = q_t.shape[0]
+    if kv.shape[0] == 0:
+        return np.zeros((H, HEAD_DIM)), np.full(H, -np.inf)
+    logits = bmm1 * (q_t @ kv.T)                        # [H, n]
+    m = logits.max(axis=1)                               # [H]
+    e = np.exp(logits - m[:, None])                      # [H, n]
+    z = e.sum(axis=1)                                    # [H]
+    denom = z.copy()
+    if sinks is not None:
+        denom = denom + np.exp(np.asarray(sinks, dtype=np.float64) - m)
+    o = bmm2 * (e @ kv) / denom[:, None]
+    lse2 = (m + np.log(denom if lse_with_sink else z)) * LOG2E
+    return o, lse2
+
+
+# --------------------------------------------------------------------------
+# steps a7-a9: split partials and their log-sum-exp combine
+# --------------------------------------------------------------------------
+
+def partial(q_t: np.ndarray, kv: np.ndarray, bmm1: float):
+    """Unsunk, unscaled normalised partial (O_s, LSE2_s) over one slot subset."""
+    return attend(q_t, kv, bmm1, 1.0, None)
+
+
+def combine_partials(o_s: np.ndarray, lse_s: np.ndarray, bmm2: float,
+                     sinks: Optional[np.ndarray], lse_with_sink: bool = False):
+    """o_s [S, H, 512], lse_s [S, H] -> (O [H, 512], LSE2 [H]).
+
+    LSE2 = log2 sum_s 2^{LSE2_s};  O = sum_s 2^{LSE2_s - LSE2} O_s; then the
+    sink joins the normaliser: O *= 1 / (1 + 2^{sink * log2 e - LSE2}); then
+    O *= bmm2.
+    """
+    H = o_s.shape[1]
+    mx = lse_s.max(axis=0)
+    empty = ~np.isfinite(mx)
+    mx_safe = np.where(empty, 0.0, mx)
+    w = np.where(np.isfinite(lse_s), np.exp2(lse_s - mx_safe[None, :]), 0.0)  # [S, H]
+    wsum = w.sum(axis=0)
+    out = np.zeros((H, HEAD_DIM))
+    lse = np.full(H, -np.inf)
+    ok = ~empty
+    out[ok] = (w[:, ok, None] * o_s[:, ok, :]).sum(axis=0) / wsum[ok, None]
+    lse[ok] = mx_safe[ok] + np.log2(wsum[ok])
+    if sinks is not None:
+        sink2 = np.asarray(sinks, dtype=np.float64) * LOG2E
+        factor = np.where(ok, 1.0 / (1.0 + np.exp2(sink2 - np.where(ok, lse, 0.0))), 0.0)
+        out = out * factor[:, None]
+        if lse_with_sink:
+            lse = np.where(ok, np.logaddexp2(lse, sink2), lse)
+    return bmm2 * out, lse
+
+
+# --------------------------------------------------------------------------
+# the whole operation
+# --------------------------------------------------------------------------
+
+def _gather(pool_bits: dict, slots, dtype: str) -> np.ndarray:
+    if not slots:
+        return np.zeros((0, HEAD_DIM))
+    rows = [pool_bits[p][r] for (_, p, r) in slots]
+    return decode(np.stack(rows), dtype)
+
+
+def sparse_mla_decode(*, dtype: str, batch: int, q, swa_kv, comp_kv, indices,
+                      topk_lens=None, seq_lens, cum_seq_lens_q=None, sinks=None,
+                      bmm1_scale: float, bmm2_scale: float,
+                      tokens: Optional[Sequence[int]] = None,
+                      splits: Optional[int] = None, lse_with_sink: bool = False,
+                      invalid_index: str = "raise"):
+    """Return (O [T, H, 512] float64, LSE2 [T, H] float64) for ``tokens``.
+
+    Arguments are raw element bits as the operation takes them (see the module
+    docstring).  ``splits`` (optional) evaluates every token as that many
+    contiguous column ranges of its active columns and merges them with
+    ``combine_partials``; it must agree with the unsplit result.
+    """
+    sum_q = q.shape[0]
+    tokens = range(sum_q) if tokens is None else list(tokens)
+    pools = {"swa": swa_kv, "comp": comp_kv}
+    bmm1 = float(bmm1_scale)
+    bmm2 = float(bmm2_scale)
+    O, L = [], []
+    for t in tokens:
+        slots = valid_slots(t, indices=indices, topk_lens=topk_lens, seq_lens=seq_lens,
+                            cum_seq_lens_q=cum_seq_lens_q, batch=batch,
+                            swa_rows=swa_kv.shape[0], comp_rows=comp_kv.shape[0],
+                            invalid_index=invalid_index)
+        q_t = decode(q[t], dtype)                         # [H, 512]
+        if splits is None:
+            o, lse = attend(q_t, _gather(pools, slots, dtype), bmm1, bmm2, sinks, lse_with_sink)
+        else:
+            width = indices.shape[1]
+            n_lim = width if topk_lens is None else min(max(int(topk_lens[t]), 0), width)
+            per = -(-n_lim // splits) if n_lim > 0 else 0
+            o_s, lse_s = [], []
+            for s in range(splits):
+                lo, hi = s * per, min(n_lim, (s + 1) * per)
+                part = [sl for sl in slots if lo <= sl[0] < hi]
+                o_p, l_p = partial(q_t, _gather(pools, part, dtype), bmm1)
+                o_s.append(o_p)
+                lse_s.append(l_p)
+            o, lse = combine_partials(np.stack(o_s), np.stack(lse_s), bmm2, sinks, lse_with_sink)
+        O.append(o)
+        L.append(lse)
+    H = q.shape[1]
+    if not O:
+        return np.zeros((0, H, HEAD_DIM)), np.zeros((0, H))
+    return np.stack(O), np.stack(L)
+
+
+def run_workload(w, **kw):
+    """Convenience: evaluate a ``Workload`` (duck-typed) with the oracle."""
+    return sparse_mla_decode(dtype=w.dtype, batch=w.batch, q=w.q, swa_kv=w.swa_kv,
+                             comp_kv=w.comp_kv, indices=w.indices, topk_lens=w.topk_lens,
+                             seq_lens=w.seq_lens, cum_seq_lens_q=w.cum_seq_lens_q,
+                             sinks=w.sinks, bmm1_scale=w.bmm1_scale,
+                             bmm2_scale=w.bmm2_scale, **kw)
