@@ -1,0 +1,409 @@
+"""Benchmark of the sparse MLA decode hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+One step = one whole decode (split kernel, plus the combine kernel when the
+plan splits) over one batch of the synthetic workload.  Default workload:
+FP8 E4M3, 128 tokens, H=128, 128 SWA + 2048 compressed slots per token over a
+256k-row compressed pool.  L2 is flushed (a write of twice the L2 size)
+between timed steps, outside the timed events.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import os
+
+_NCPU = os.cpu_count() or 1
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_NCPU))   # the CPU oracle's BLAS threads
+os.environ.setdefault("OMP_NUM_THREADS", str(_NCPU))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mla_decode_token_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse-MLA decode query-tokens/s; gathered-KV GB/s and % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+HEAD_DIM, SWA_COLS = 512, 128
+
+
+# ------------------------------------------------------------------ accounting
+
+def valid_slots_per_token(w) -> np.ndarray:
+    """Slots each token reads: columns below clamp(topk_lens, 0, W) that are not
+    -1 and, for SWA columns, inside the window min(128, pos + 1)."""
+    T, width = w.indices.shape
+    n_lim = np.full(T, width) if w.topk_lens is None else np.clip(w.topk_lens, 0, width)
+    q_lens = (np.full(w.batch, T // w.batch) if w.cum_seq_lens_q is None
+              else np.diff(w.cum_seq_lens_q))
+    pos = np.concatenate([np.arange(ql) + sl - ql for sl, ql in zip(w.seq_lens, q_lens)])
+    w_swa = np.clip(pos + 1, 0, SWA_COLS)
+    j = np.arange(width)[None, :]
+    active = (j < n_lim[:, None]) & (w.indices != -1) & ((j >= SWA_COLS) | (j < w_swa[:, None]))
+    return active.sum(axis=1)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    csrc = os.path.join(ROOT, "sparse_mla_decode_token_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_sources_sha") != kernel_sources_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3][1:5]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
+
+
+# -------------------------------------------------------------- oracle timing
+
+def time_oracle(w, budget_s: float, max_tokens: int | None = None):
+    """Run the CPU oracle token by token until ``budget_s`` is spent; returns
+    (tokens done, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    done = 0
+    limit = w.sum_q if max_tokens is None else min(w.sum_q, max_tokens)
+    while done < limit:
+        oracle.run_workload(w, tokens=[done])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def blas_threads() -> int:
+    try:
+        return int(os.environ.get("OPENBLAS_NUM_THREADS", _NCPU))
+    except ValueError:
+        return _NCPU
+
+
+# ----------------------------------------------------------------- the bench
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_config(w, n: int) -> dict:
+    return {"workload": W.CONFIG_NAMES[n], "dtype": w.dtype, "batch": w.batch, "sum_q": w.sum_q,
+            "num_heads": w.num_heads, "head_dim": HEAD_DIM, "index_width": w.width,
+            "swa_rows": int(w.swa_kv.shape[0]), "compressed_rows": int(w.comp_kv.shape[0]),
+            "sinks": w.sinks is not None, "varlen": w.cum_seq_lens_q is not None,
+            "l2": "flushed between timed steps (write of 2x L2 size, outside the timed events)",
+            "parallelism": "replicas"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = W.config_workload(args.config)
+    per_step = max(1, min(w.sum_q, args.ref_tokens))
+    for _ in range(args.warmup):
+        time_oracle(w, 1e9, max_tokens=1)
+    t_total = 0.0
+    tokens = 0
+    for _ in range(args.steps):
+        n, dt = time_oracle(w, 1e9, max_tokens=per_step)
+        tokens += n
+        t_total += dt
+    value = tokens / t_total
+    cores = blas_threads()
+    sample = f"first {per_step} tokens of the workload per step, {args.steps} steps"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, args.config),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_gpu(args):
+    from sparse_mla_decode_token_gb300 import binding as B
+    from sparse_mla_decode_token_gb300 import build as smla_build
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    smla_build.build()
+    B.lib()
+    dev = torch.device("cuda", local)
+    w = W.config_workload(args.config)
+    n_valid = valid_slots_per_token(w)
+    eb = w.elem_bytes
+    gathered_bytes = int(n_valid.sum()) * HEAD_DIM * eb          # per step
+    flops = int(n_valid.sum()) * 2 * 2 * HEAD_DIM * w.num_heads   # QK + PV, 2 flops per MAC
+
+    def kv(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(torch.int16).view(torch.bfloat16) if w.dtype == "bf16" else t.view(torch.float8_e4m3fn))
+
+    def i32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+    # host (pinned) per-step inputs and outputs for the end-to-end leg
+    h_q = kv(w.q).pin_memory()
+    h_idx = i32(w.indices).pin_memory()
+    h_lens = i32(w.topk_lens).pin_memory() if w.topk_lens is not None else None
+    h_seq = i32(w.seq_lens).pin_memory()
+    h_cum = i32(w.cum_seq_lens_q).pin_memory() if w.cum_seq_lens_q is not None else None
+    # device-resident state: KV pools, sinks
+    d_swa = kv(w.swa_kv).to(dev)
+    d_comp = kv(w.comp_kv).to(dev)
+    d_sinks = torch.from_numpy(w.sinks).to(dev) if w.sinks is not None else None
+    d_q, d_idx, d_seq = h_q.to(dev), h_idx.to(dev), h_seq.to(dev)
+    d_lens = h_lens.to(dev) if h_lens is not None else None
+    d_cum = h_cum.to(dev) if h_cum is not None else None
+    out = torch.empty((w.sum_q, w.num_heads, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.sum_q, w.num_heads), dtype=torch.float32, device=dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    args_c = B.make_args(q=d_q, swa_kv=d_swa, compressed_kv=d_comp, sparse_indices=d_idx,
+                         seq_lens=d_seq, out=out, sparse_topk_lens=d_lens, cum_seq_lens_q=d_cum,
+                         sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                         out_lse=lse, kernel=args.kernel)
+    plan = B.smla_plan_decode(args_c, local)
+    workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    launches_per_step = 1 + (1 if plan.num_splits > 1 else 0)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def new_event():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)          # materialise the CUDA event handle
+        return e
+
+    def step():
+        B.smla_decode(args_c, sptr)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_step = [(new_event(), new_event()) for _ in range(K)]
+    ev_main = [(new_event(), new_event()) for _ in range(K)]
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws_ > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            args_c.profile_event_begin = ev_main[k][0].cuda_event
+            args_c.profile_event_end = ev_main[k][1].cuda_event
+            ev_step[k][0].record(stream)
+            step()
+            ev_step[k][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        args_c.profile_event_begin = args_c.profile_event_end = None
+        # end-to-end leg: pinned host inputs -> device, decode, outputs -> pinned host
+        ev_e2e = [(new_event(), new_event()) for _ in range(K)]
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            ev_e2e[k][0].record(stream)
+            d_q.copy_(h_q, non_blocking=True)
+            d_idx.copy_(h_idx, non_blocking=True)
+            d_seq.copy_(h_seq, non_blocking=True)
+            if d_lens is not None:
+                d_lens.copy_(h_lens, non_blocking=True)
+            if d_cum is not None:
+                d_cum.copy_(h_cum, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            ev_e2e[k][1].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    main_ms = [a.elapsed_time(b) for a, b in ev_main]
+    e2e_ms = [a.elapsed_time(b) for a, b in ev_e2e]
+    total_s = sum(step_ms) / 1e3
+    if ws_ > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    n_tok_all = w.sum_q * K * ws_
+    value = n_tok_all / total_s
+    e2e_value = w.sum_q * K * ws_ / (sum(e2e_ms) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_seq, h_lens, h_cum) if t is not None)
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    hbm_gbs, bf16_tf, peak_src = peaks()
+    dtype_tf = bf16_tf * (2.0 if w.dtype == "e4m3" else 1.0)     # FP8 dense = 2x BF16 (nominal ratio)
+    main_s = statistics.mean(main_ms) / 1e3
+    t_hbm = gathered_bytes / (hbm_gbs * 1e9)
+    t_tc = flops / (dtype_tf * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": gathered_bytes / main_s / 1e9, "peak": hbm_gbs,
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / main_s / 1e12, "peak": dtype_tf,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["traffic"] = recorded_traffic(W.CONFIG_NAMES[args.config])
+    roof["algorithmic_bytes_per_launch"] = gathered_bytes
+    roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
+    roof["main_kernel_us"] = 1e6 * main_s
+    roof["roofline_frac_whole_step"] = max(t_hbm, t_tc) / (total_s / (K * 1.0)) if ws_ == 1 else None
+
+    if rank != 0:
+        return
+    cpu = None
+    if ws_ == 1 and not args.no_cpu_baseline:
+        n_done, dt = time_oracle(w, args.cpu_budget)
+        cpu = {"value": n_done / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"first {n_done} of {w.sum_q} tokens of the same workload, fp64 numpy, {dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3" if w.dtype == "e4m3" else "bf16", "data": "synthetic",
+        "config": workload_config(w, args.config),
+        "gathered_kv_gbs": gathered_bytes * K * ws_ / total_s / 1e9,
+        "roofline": roof,
+        "plan": plan.as_dict(),
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle timing")
+    ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * smla.h -- C ABI of the GB300 (sm_103a) DeepSeek-V4 sparse MLA decode library.
+ *
+ * The operation (FlashInfer trtllm_batch_decode_sparse_mla_dsv4, description,
+ * SM100/SM103 paragraph, and its Parameters list): every flattened query token
+ * t has H heads (64 or 128) of dimension 512 (448 NoPE + 64 RoPE dims; FlashInfer
+ * cake_sparse_mla_sm120_dsv4_nvfp4_decode, Parameters: q).  All heads share one
+ * latent KV row per selected slot.  Row t of the index table selects the slots:
+ * columns 0..127 are rows of the sliding-window (SWA) pool, the remaining
+ * columns are rows of the compressed pool, and -1 masks a slot (cake page,
+ * Parameters: indices).  Per head h:
+ *
+ *   l_j  = bmm1_scale * <q[t,h,:], kv_j>
+ *   O    = bmm2_scale * sum_j e^{l_j} kv_j / (sum_j e^{l_j} + e^{sinks[h]})
+ *   LSE2 = log2 sum_j e^{l_j}            (base 2; cake page, Parameters: out_lse)
+ *
+ * O is written as BF16; LSE2 as float32.  The slots of token t are the columns
+ * j < clamp(sparse_topk_lens[t], 0, W) whose index is not -1 and, for SWA
+ * columns, j < min(128, pos + 1) where pos = seq_lens[b] - q_len_b + i is the
+ * right-aligned position of token i of request b (msa_sparse_decode_attention
+ * page, description).  A token with no slot gets O = 0 and LSE2 = -inf.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device unless
+ *    stated otherwise.  The caller owns every buffer, including the workspace;
+ *    the library never allocates, never synchronises the device and never
+ *    copies an input.  A wrong output layout is rejected, never copied into
+ *    (msa_sparse_decode_attention page, Parameters: out).
+ *  - Host-detectable problems return a status synchronously and launch
+ *    nothing.  smla_last_error() gives a one-line reason (thread-local).
+ *  - Launches are stream-ordered on the stream given; no host synchronisation.
+ */
+#ifndef SMLA_H
+#define SMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMLA_ABI_VERSION 1
+#define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
+#define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
+#define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
+#define SMLA_DEFAULT_MAX_SPLITS 32
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size or stride */
+  SMLA_ERR_UNSUPPORTED = 2,        /* e.g. num_heads not in {64, 128} */
+  SMLA_ERR_WORKSPACE_TOO_SMALL = 3,
+  SMLA_ERR_CUDA = 4                /* a CUDA runtime call or launch failed */
+} smla_status;
+
+typedef enum smla_dtype {
+  SMLA_BF16 = 0,                   /* bfloat16 query and KV rows */
+  SMLA_E4M3 = 1                    /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */
+} smla_dtype;
+
+/* Kernel selection (smla_args.kernel).  AUTO picks the tensor-core kernel. */
+typedef enum smla_kernel {
+  SMLA_KERNEL_AUTO = 0,
+  SMLA_KERNEL_CUDA_CORE = 1,       /* plain CUDA-core kernel (fp32 FMA) */
+  SMLA_KERNEL_TCGEN05 = 2          /* tcgen05 / TMEM tensor-core kernel */
+} smla_kernel;
+
+/* Bits the kernels OR into *error_word (device-side detection, no trap). */
+#define SMLA_DEVERR_INDEX_OUT_OF_RANGE 0x1  /* index < -1 or >= pool rows: slot treated as masked */
+
+/*
+ * Arguments of one decode call.  Zero-initialise and fill what you use.
+ * Strides are in ELEMENTS; 0 selects the dense default given in brackets.
+ */
+typedef struct smla_args {
+  int32_t sum_q;        /* flattened query tokens T (0 = nothing to do) */
+  int32_t batch;        /* requests B >= 1 */
+  int32_t num_heads;    /* H: 64 or 128 (vLLM get_padded_num_q_heads) */
+  int32_t width;        /* index-table columns W >= 128 (W == 128: SWA-only layer) */
+  int32_t dtype;        /* smla_dtype of q, swa_kv and compressed_kv (one type for all three) */
+
+  /* query [T, H, 512]; heads and dims contiguous; token stride [H*512] */
+  const void* q;
+  int64_t q_stride_token;
+
+  /* SWA pool rows [swa_rows, 512]; row stride [512], a multiple of 16 bytes */
+  const void* swa_kv;
+  int64_t swa_rows;
+  int64_t swa_row_stride;
+
+  /* compressed pool rows [comp_rows, 512]; may alias swa_kv (SWA-only layers) */
+  const void* compressed_kv;
+  int64_t comp_rows;
+  int64_t comp_row_stride;
+
+  /* int32 index table [T, W], row stride [W]; physical row = page*page_size+offset */
+  const int32_t* sparse_indices;
+  int64_t indices_row_stride;
+
+  const int32_t* sparse_topk_lens;  /* [T] int32, or NULL = W for every token */
+  const int32_t* seq_lens;          /* [B] int32 original KV lengths, required */
+  const int32_t* cum_seq_lens_q;    /* [B+1] int32 varlen offsets, or NULL = uniform T/B */
+  const float* sinks;               /* [H] float32 sink logits (natural-log units), or NULL */
+
+  float bmm1_scale;                 /* QK and softmax scale (FP8: scale*q_scale*kv_scale) */
+  float bmm2_scale;                 /* VO scale (FP8: kv_scale) */
+  const float* bmm1_scale_dev;      /* optional device float32 overriding bmm1_scale */
+  const float* bmm2_scale_dev;      /* optional device float32 overriding bmm2_scale */
+
+  void* out;                        /* [T, H, 512] BF16, contiguous, 16-byte aligned */
+  float* out_lse;                   /* [T, H] float32 base-2 LSE, contiguous, or NULL */
+
+  void* workspace;                  /* caller-owned scratch, >= smla_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+
+  int32_t num_splits;               /* 0 = planner; else forced split count in [1, SMLA_MAX_SPLITS] */
+  int32_t max_splits;               /* 0 = SMLA_DEFAULT_MAX_SPLITS; planner upper bound */
+  int32_t kernel;                   /* smla_kernel */
+
+  int32_t* error_word;              /* optional device int32; kernels OR SMLA_DEVERR_* bits into it */
+
+  /* Optional cudaEvent_t handles recorded on the stream immediately before
+   * and after the main decode kernel (not the combine).  For profiling. */
+  void* profile_event_begin;
+  void* profile_event_end;
+} smla_args;
+
+/* The resolved launch plan (shape-based: it never reads device memory). */
+typedef struct smla_plan {
+  int32_t kernel;            /* smla_kernel actually used */
+  int32_t num_splits;        /* S: column ranges per token; S > 1 adds a combine launch */
+  int32_t ctas_per_split;    /* CTAs cooperating on one (token, split) */
+  int32_t grid;              /* CTAs of the main decode launch */
+  int32_t threads;           /* threads per CTA of the main decode launch */
+  int32_t smem_bytes;        /* dynamic shared memory per CTA */
+  size_t workspace_bytes;    /* workspace the call needs (0 when S == 1) */
+} smla_plan;
+
+/*
+ * Plan a call for the device ordinal `device` (SM count and limits are read
+ * from it).  Validates args like smla_decode except pointers and workspace.
+ * The plan depends only on shapes, the device and num_splits/max_splits/kernel.
+ */
+smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan);
+
+/* Workspace bytes smla_decode will need for these args on `device`. */
+smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes);
+
+/*
+ * Run the decode on `stream` (a cudaStream_t, NULL = legacy default stream) on
+ * the current device.  Asynchronous; allocation- and synchronisation-free.
+ * Writes out (and out_lse if given).  Returns SMLA_ERR_* without launching on
+ * a host-detectable problem, SMLA_ERR_CUDA if a launch fails.
+ */
+smla_status smla_decode(const smla_args* args, void* stream);
+
+/* Static text for a status code. */
+const char* smla_status_string(smla_status status);
+
+/* One-line reason for the last non-OK status returned on this thread. */
+const char* smla_last_error(void);
+
+/* SMLA_ABI_VERSION of the loaded library. */
+int smla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H */

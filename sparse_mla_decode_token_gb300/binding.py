@@ -1,0 +1,263 @@
+"""Python binding of the C ABI in ``include/smla.h`` (argument marshalling only).
+
+Every step of the decode runs in the CUDA kernels of ``libsmla.so``; this
+module only fills the ``smla_args`` struct from torch tensors and forwards the
+call.  There is no fallback: if the library is missing, the first call raises.
+
+Names follow the C ABI: ``smla_decode``, ``smla_plan_decode``,
+``smla_workspace_size``, ``smla_status_string``, ``smla_last_error``; plus
+``sparse_mla_decode(...)``, the tensor-level call whose argument list follows
+the FlashInfer ``trtllm_batch_decode_sparse_mla_dsv4`` signature.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libsmla.so")
+
+HEAD_DIM = 512
+SWA_COLS = 128
+MAX_SPLITS = 64
+
+SMLA_OK, SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE_TOO_SMALL, SMLA_ERR_CUDA = range(5)
+SMLA_BF16, SMLA_E4M3 = 0, 1
+KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05 = 0, 1, 2
+DEVERR_INDEX_OUT_OF_RANGE = 0x1
+
+_c_void_p = ctypes.c_void_p
+
+
+class SmlaArgs(ctypes.Structure):
+    _fields_ = [
+        ("sum_q", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+        ("width", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("q", _c_void_p), ("q_stride_token", ctypes.c_int64),
+        ("swa_kv", _c_void_p), ("swa_rows", ctypes.c_int64), ("swa_row_stride", ctypes.c_int64),
+        ("compressed_kv", _c_void_p), ("comp_rows", ctypes.c_int64), ("comp_row_stride", ctypes.c_int64),
+        ("sparse_indices", _c_void_p), ("indices_row_stride", ctypes.c_int64),
+        ("sparse_topk_lens", _c_void_p), ("seq_lens", _c_void_p),
+        ("cum_seq_lens_q", _c_void_p), ("sinks", _c_void_p),
+        ("bmm1_scale", ctypes.c_float), ("bmm2_scale", ctypes.c_float),
+        ("bmm1_scale_dev", _c_void_p), ("bmm2_scale_dev", _c_void_p),
+        ("out", _c_void_p), ("out_lse", _c_void_p),
+        ("workspace", _c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("num_splits", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
+        ("error_word", _c_void_p),
+        ("profile_event_begin", _c_void_p), ("profile_event_end", _c_void_p),
+    ]
+
+
+class SmlaPlan(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("ctas_per_split", ctypes.c_int32), ("grid", ctypes.c_int32),
+        ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{smla_status_string(status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+# (symbol, restype, argtypes) of every entry point the header declares
+EXPORTS = {
+    "smla_plan_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(SmlaPlan)]),
+    "smla_workspace_size": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "smla_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
+    "smla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "smla_last_error": (ctypes.c_char_p, []),
+    "smla_abi_version": (ctypes.c_int, []),
+}
+
+
+def lib():
+    """Load ``libsmla.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libsmla.so is not built ({LIB_PATH}); run "
+                              "sparse_mla_decode_token_gb300.build.build() first")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, argt) in EXPORTS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = argt
+        _lib = handle
+    return _lib
+
+
+# ------------------------------------------------------------- raw ABI calls
+
+def smla_status_string(status: int) -> str:
+    return lib().smla_status_string(status).decode()
+
+
+def smla_last_error() -> str:
+    return lib().smla_last_error().decode()
+
+
+def smla_abi_version() -> int:
+    return lib().smla_abi_version()
+
+
+def _check(status: int) -> None:
+    if status != SMLA_OK:
+        raise SmlaError(status, smla_last_error())
+
+
+def smla_plan_decode(args: SmlaArgs, device: int = 0) -> SmlaPlan:
+    plan = SmlaPlan()
+    _check(lib().smla_plan_decode(ctypes.byref(args), device, ctypes.byref(plan)))
+    return plan
+
+
+def smla_workspace_size(args: SmlaArgs, device: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().smla_workspace_size(ctypes.byref(args), device, ctypes.byref(n)))
+    return int(n.value)
+
+
+def smla_decode(args: SmlaArgs, stream: Optional[int] = None) -> None:
+    """Launch on ``stream`` (a raw cudaStream_t value; default: torch's current stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(lib().smla_decode(ctypes.byref(args), _c_void_p(stream)))
+
+
+# ---------------------------------------------------------- tensor marshalling
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SMLA_BF16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return SMLA_E4M3
+    raise TypeError(f"q/KV dtype {t.dtype} is not bfloat16 or float8_e4m3fn")
+
+
+def _rows_and_stride(kv: torch.Tensor) -> tuple[int, int]:
+    """Flatten a KV pool view ([..., 512], any page layout) to (rows, row stride)."""
+    if kv.shape[-1] != HEAD_DIM or kv.stride(-1) != 1:
+        raise ValueError(f"KV pool must end in a contiguous dim of {HEAD_DIM}; got {tuple(kv.shape)}")
+    flat = kv.reshape(-1, HEAD_DIM) if kv.dim() != 2 else kv
+    if flat.data_ptr() != kv.data_ptr():
+        raise ValueError("KV pool view cannot be flattened to rows without a copy")
+    return flat.shape[0], flat.stride(0)
+
+
+def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Tensor,
+              sparse_indices: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+              sparse_topk_lens: Optional[torch.Tensor] = None,
+              cum_seq_lens_q: Optional[torch.Tensor] = None,
+              sinks: Optional[torch.Tensor] = None,
+              bmm1_scale=1.0, bmm2_scale=1.0,
+              out_lse: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None,
+              num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
+              error_word: Optional[torch.Tensor] = None) -> SmlaArgs:
+    """Fill ``smla_args`` from tensors (no copies; wrong layouts raise)."""
+    if q.dim() == 4:                       # dense [B, q_len, H, 512]
+        q = q.reshape(-1, q.shape[2], q.shape[3])
+    if q.dim() != 3 or q.shape[-1] != HEAD_DIM or q.stride(-1) != 1 or q.stride(1) != HEAD_DIM:
+        raise ValueError(f"query must be [T, H, {HEAD_DIM}] with contiguous heads; got {tuple(q.shape)}")
+    T, H = q.shape[0], q.shape[1]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.numel() != T * H * HEAD_DIM:
+        raise ValueError("out must be a contiguous bfloat16 tensor of T*H*512 elements")
+    if out_lse is not None and (out_lse.dtype != torch.float32 or not out_lse.is_contiguous()
+                                or out_lse.numel() != T * H):
+        raise ValueError("out_lse must be a contiguous float32 tensor of T*H elements")
+    for name, t in (("sparse_indices", sparse_indices), ("seq_lens", seq_lens),
+                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q)):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if sparse_indices.dim() == 3:          # [T, 1, W]
+        sparse_indices = sparse_indices[:, 0, :]
+    if sparse_indices.stride(-1) != 1:
+        raise ValueError("sparse_indices must have a contiguous last dim")
+    swa_rows, swa_stride = _rows_and_stride(swa_kv)
+    comp_rows, comp_stride = _rows_and_stride(compressed_kv)
+    a = SmlaArgs()
+    a.sum_q, a.num_heads, a.width = T, H, sparse_indices.shape[-1]
+    a.batch = seq_lens.numel()
+    a.dtype = _dtype_code(q)
+    if _dtype_code(swa_kv) != a.dtype or _dtype_code(compressed_kv) != a.dtype:
+        raise TypeError("query, swa_kv and compressed_kv must share one dtype")
+    a.q, a.q_stride_token = q.data_ptr(), q.stride(0)
+    a.swa_kv, a.swa_rows, a.swa_row_stride = swa_kv.data_ptr(), swa_rows, swa_stride
+    a.compressed_kv, a.comp_rows, a.comp_row_stride = compressed_kv.data_ptr(), comp_rows, comp_stride
+    a.sparse_indices, a.indices_row_stride = sparse_indices.data_ptr(), sparse_indices.stride(0)
+    a.sparse_topk_lens = _ptr(sparse_topk_lens)
+    a.seq_lens = seq_lens.data_ptr()
+    a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() < H):
+        raise ValueError("sinks must be float32 with at least H entries")
+    a.sinks = _ptr(sinks)
+    for name, val in (("bmm1", bmm1_scale), ("bmm2", bmm2_scale)):
+        if isinstance(val, torch.Tensor):
+            if val.dtype != torch.float32:
+                raise TypeError(f"{name}_scale tensor must be float32")
+            setattr(a, f"{name}_scale_dev", val.data_ptr())
+            setattr(a, f"{name}_scale", 1.0)
+        else:
+            setattr(a, f"{name}_scale", float(val))
+    a.out, a.out_lse = out.data_ptr(), _ptr(out_lse)
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    a.error_word = _ptr(error_word)
+    return a
+
+
+def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace_buffer: Optional[torch.Tensor],
+                      sparse_indices: torch.Tensor, compressed_kv_cache: torch.Tensor,
+                      sparse_topk_lens: Optional[torch.Tensor], seq_lens: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, bmm1_scale=1.0, bmm2_scale=1.0,
+                      sinks: Optional[torch.Tensor] = None,
+                      cum_seq_lens_q: Optional[torch.Tensor] = None,
+                      out_lse: Optional[torch.Tensor] = None,
+                      num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
+                      error_word: Optional[torch.Tensor] = None,
+                      stream: Optional[int] = None):
+    """Decode; returns ``(out, out_lse)``.  ``out`` / ``out_lse`` are allocated when not given."""
+    T = query.shape[0] if query.dim() == 3 else query.shape[0] * query.shape[1]
+    H = query.shape[-2]
+    if out is None:
+        out = torch.empty((T, H, HEAD_DIM), dtype=torch.bfloat16, device=query.device)
+    if out_lse is None:
+        out_lse = torch.empty((T, H), dtype=torch.float32, device=query.device)
+    args = make_args(q=query, swa_kv=swa_kv_cache, compressed_kv=compressed_kv_cache,
+                     sparse_indices=sparse_indices, seq_lens=seq_lens, out=out,
+                     sparse_topk_lens=sparse_topk_lens, cum_seq_lens_q=cum_seq_lens_q,
+                     sinks=sinks, bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
+                     out_lse=out_lse, workspace=workspace_buffer, num_splits=num_splits,
+                     max_splits=max_splits, kernel=kernel, error_word=error_word)
+    smla_decode(args, stream)
+    return out, out_lse
+
+
+def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=0,
+                   kernel=KERNEL_AUTO, cum_seq_lens_q=None, device: int = 0) -> int:
+    """Workspace bytes for a call with these shapes (no device memory is read)."""
+    a = SmlaArgs()
+    q3 = query if query.dim() == 3 else query.reshape(-1, query.shape[2], query.shape[3])
+    a.sum_q, a.num_heads, a.width = q3.shape[0], q3.shape[1], sparse_indices.shape[-1]
+    a.batch, a.dtype = seq_lens.numel(), _dtype_code(q3)
+    a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
+    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    return smla_workspace_size(a, device)

@@ -1,0 +1,244 @@
+// Host side of the C ABI: validation, planner and launches.
+//
+// Argument semantics follow the FlashInfer trtllm_batch_decode_sparse_mla_dsv4
+// page (signature and Parameters).  The planner mirrors the adaptive split
+// described on the msa_sparse_decode_attention page (Parameters: force_fused:
+// many chunks per token at low batch, a single fused chunk at high batch) and
+// the split cap of the cake_sparse_mla_sm120_dsv4_nvfp4_decode page
+// (Parameters: num_splits, max_splits).  Everything here reads shapes only:
+// no device memory is read, nothing is allocated and nothing synchronises.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace smla {
+namespace {
+
+thread_local std::string g_last_error;
+
+smla_status fail(smla_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+smla_status fail(smla_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int elem_bytes(int dtype) { return dtype == SMLA_BF16 ? 2 : 1; }
+
+// Shape checks shared by planning and decoding.
+smla_status check_shapes(const smla_args* a) {
+  if (a == nullptr) return fail(SMLA_ERR_INVALID_ARG, "args is NULL");
+  if (a->dtype != SMLA_BF16 && a->dtype != SMLA_E4M3)
+    return fail(SMLA_ERR_INVALID_ARG, "dtype %d is not SMLA_BF16 or SMLA_E4M3", a->dtype);
+  if (a->num_heads != 64 && a->num_heads != 128)
+    return fail(SMLA_ERR_UNSUPPORTED, "num_heads %d: only 64 or 128 heads are supported", a->num_heads);
+  if (a->sum_q < 0) return fail(SMLA_ERR_INVALID_ARG, "sum_q %d < 0", a->sum_q);
+  if (a->batch < 1) return fail(SMLA_ERR_INVALID_ARG, "batch %d < 1", a->batch);
+  if (a->width < kSwaCols)
+    return fail(SMLA_ERR_INVALID_ARG, "width %d < %d fixed SWA columns", a->width, kSwaCols);
+  if (a->cum_seq_lens_q == nullptr && a->sum_q % a->batch != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "sum_q %d is not a multiple of batch %d (pass cum_seq_lens_q for varlen)",
+                a->sum_q, a->batch);
+  if (a->num_splits < 0 || a->num_splits > SMLA_MAX_SPLITS)
+    return fail(SMLA_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", a->num_splits, SMLA_MAX_SPLITS);
+  if (a->max_splits < 0 || a->max_splits > SMLA_MAX_SPLITS)
+    return fail(SMLA_ERR_INVALID_ARG, "max_splits %d outside [0, %d]", a->max_splits, SMLA_MAX_SPLITS);
+  if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05)
+    return fail(SMLA_ERR_INVALID_ARG, "kernel %d is not a smla_kernel", a->kernel);
+  if (a->swa_rows < 0 || a->comp_rows < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "negative pool row count");
+  const int eb = elem_bytes(a->dtype);
+  const int64_t min_qs = (int64_t)a->num_heads * kHeadDim;
+  const int64_t qs = a->q_stride_token ? a->q_stride_token : min_qs;
+  if (qs < min_qs || (qs * eb) % 16 != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "q_stride_token %lld must be >= H*512 and a multiple of 16 bytes",
+                (long long)qs);
+  const int64_t ss = a->swa_row_stride ? a->swa_row_stride : kHeadDim;
+  const int64_t cs = a->comp_row_stride ? a->comp_row_stride : kHeadDim;
+  if (ss < kHeadDim || (ss * eb) % 16 != 0 || cs < kHeadDim || (cs * eb) % 16 != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "pool row strides (%lld, %lld) must be >= 512 and multiples of 16 bytes",
+                (long long)ss, (long long)cs);
+  const int64_t is = a->indices_row_stride ? a->indices_row_stride : a->width;
+  if (is < a->width)
+    return fail(SMLA_ERR_INVALID_ARG, "indices_row_stride %lld < width %d", (long long)is, a->width);
+  return SMLA_OK;
+}
+
+int g_sm_count[64];
+
+smla_status sm_count(int device, int* out) {
+  if (device < 0 || device >= 64) return fail(SMLA_ERR_INVALID_ARG, "device %d out of range", device);
+  if (g_sm_count[device] == 0) {
+    int n = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    g_sm_count[device] = n;
+  }
+  *out = g_sm_count[device];
+  return SMLA_OK;
+}
+
+smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
+  smla_status st = check_shapes(a);
+  if (st != SMLA_OK) return st;
+  int sms = 0;
+  st = sm_count(device, &sms);
+  if (st != SMLA_OK) return st;
+  memset(plan, 0, sizeof(*plan));
+  if (a->kernel == SMLA_KERNEL_TCGEN05)
+    return fail(SMLA_ERR_UNSUPPORTED, "the tcgen05 kernel is not built into this library");
+  plan->kernel = SMLA_KERNEL_CUDA_CORE;
+  plan->ctas_per_split = cuda_core_ctas_per_split(a->num_heads);
+  plan->threads = cuda_core_threads();
+  plan->smem_bytes = cuda_core_smem_bytes();
+  const int resident = 2;                         // CTAs per SM at this smem size
+  const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
+  int S = a->num_splits;
+  if (S == 0) {
+    const int64_t units = (int64_t)a->sum_q * plan->ctas_per_split;
+    const int64_t target = (int64_t)sms * resident;
+    int64_t want = units > 0 ? (target + units - 1) / units : 1;
+    const int64_t by_width = (a->width + 255) / 256;  // keep >= 256 columns per split
+    if (want > by_width) want = by_width;
+    if (want > max_splits) want = max_splits;
+    S = (int)(want < 1 ? 1 : want);
+  }
+  plan->num_splits = S;
+  const int64_t grid = (int64_t)a->sum_q * S * plan->ctas_per_split;
+  if (grid > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "grid of %lld CTAs is too large", (long long)grid);
+  plan->grid = (int32_t)grid;
+  if (S > 1) {
+    const size_t rows = (size_t)a->sum_q * a->num_heads * S;
+    plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
+  }
+  return SMLA_OK;
+}
+
+}  // namespace
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" {
+
+smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan) {
+  if (plan == nullptr) return fail(SMLA_ERR_INVALID_ARG, "plan is NULL");
+  return make_plan(args, device, plan);
+}
+
+smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes) {
+  if (bytes == nullptr) return fail(SMLA_ERR_INVALID_ARG, "bytes is NULL");
+  smla_plan plan;
+  smla_status st = make_plan(args, device, &plan);
+  if (st != SMLA_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return SMLA_OK;
+}
+
+smla_status smla_decode(const smla_args* a, void* stream_ptr) {
+  smla_status st = check_shapes(a);   // host-only checks come before any CUDA call
+  if (st != SMLA_OK) return st;
+  if (a->sum_q == 0) return SMLA_OK;   // empty batch: nothing to launch
+  int device = 0;
+  cudaError_t ce = cudaGetDevice(&device);
+  if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  smla_plan plan;
+  st = make_plan(a, device, &plan);
+  if (st != SMLA_OK) return st;
+  if (a->sum_q == 0) return SMLA_OK;
+  if (!a->q || !a->swa_kv || !a->compressed_kv || !a->sparse_indices || !a->seq_lens || !a->out)
+    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv, sparse_indices, seq_lens and out are required");
+  if (!aligned(a->q, 16) || !aligned(a->swa_kv, 16) || !aligned(a->compressed_kv, 16) || !aligned(a->out, 16))
+    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv and out must be 16-byte aligned");
+  if (!aligned(a->sparse_indices, 4) || (a->out_lse && !aligned(a->out_lse, 4)))
+    return fail(SMLA_ERR_INVALID_ARG, "sparse_indices and out_lse must be 4-byte aligned");
+  if (plan.workspace_bytes > 0) {
+    if (a->workspace == nullptr || a->workspace_bytes < plan.workspace_bytes)
+      return fail(SMLA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes given, %zu needed",
+                  a->workspace ? a->workspace_bytes : (size_t)0, plan.workspace_bytes);
+    if (!aligned(a->workspace, 256)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+
+  DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.sum_q = a->sum_q;
+  p.batch = a->batch;
+  p.H = a->num_heads;
+  p.W = a->width;
+  p.dtype = a->dtype;
+  p.num_splits = plan.num_splits;
+  p.q = a->q;
+  p.q_stride_token = a->q_stride_token ? a->q_stride_token : (int64_t)a->num_heads * kHeadDim;
+  p.swa = a->swa_kv;
+  p.swa_rows = a->swa_rows;
+  p.swa_stride = a->swa_row_stride ? a->swa_row_stride : kHeadDim;
+  p.comp = a->compressed_kv;
+  p.comp_rows = a->comp_rows;
+  p.comp_stride = a->comp_row_stride ? a->comp_row_stride : kHeadDim;
+  p.ind = a->sparse_indices;
+  p.ind_stride = a->indices_row_stride ? a->indices_row_stride : a->width;
+  p.topk = a->sparse_topk_lens;
+  p.seq_lens = a->seq_lens;
+  p.cum = a->cum_seq_lens_q;
+  p.sinks = a->sinks;
+  p.bmm1 = a->bmm1_scale;
+  p.bmm2 = a->bmm2_scale;
+  p.bmm1_dev = a->bmm1_scale_dev;
+  p.bmm2_dev = a->bmm2_scale_dev;
+  p.out = reinterpret_cast<__nv_bfloat16*>(a->out);
+  p.out_lse = a->out_lse;
+  p.err = a->error_word;
+  if (plan.num_splits > 1) {
+    const size_t rows = (size_t)a->sum_q * a->num_heads * plan.num_splits;
+    p.part_o = reinterpret_cast<float*>(a->workspace);
+    p.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(a->workspace) +
+                                          align_up(rows * kHeadDim * sizeof(float), 256));
+  }
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  if (a->profile_event_begin) {
+    ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_begin), stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
+  }
+  ce = launch_decode_cuda_core(p, plan.grid, stream);
+  if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
+  if (a->profile_event_end) {
+    ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_end), stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
+  }
+  if (plan.num_splits > 1) {
+    ce = launch_combine(p, stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
+  }
+  return SMLA_OK;
+}
+
+const char* smla_status_string(smla_status s) {
+  switch (s) {
+    case SMLA_OK: return "SMLA_OK";
+    case SMLA_ERR_INVALID_ARG: return "SMLA_ERR_INVALID_ARG";
+    case SMLA_ERR_UNSUPPORTED: return "SMLA_ERR_UNSUPPORTED";
+    case SMLA_ERR_WORKSPACE_TOO_SMALL: return "SMLA_ERR_WORKSPACE_TOO_SMALL";
+    case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA";
+  }
+  return "SMLA_ERR_UNKNOWN";
+}
+
+const char* smla_last_error(void) { return g_last_error.c_str(); }
+
+int smla_abi_version(void) { return SMLA_ABI_VERSION; }
+
+}  // extern "C"

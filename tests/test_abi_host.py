@@ -1,0 +1,130 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every
+declared symbol, its struct layout matches the header, and host-detectable
+argument errors return their own status codes (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_mla_decode_token_gb300 import binding as B
+from sparse_mla_decode_token_gb300 import build as smla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    smla_build.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(smla_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"smla_decode", "smla_plan_decode", "smla_workspace_size", "smla_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(B.EXPORTS)
+    assert B.smla_abi_version() == 1
+
+
+def test_struct_layout_matches_header(tmp_path):
+    fields = {"smla_args": [f for f, _ in B.SmlaArgs._fields_],
+              "smla_plan": [f for f, _ in B.SmlaPlan._fields_]}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st}.{f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", str(src), "-o", str(exe)], check=True)
+    out = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                   check=True).stdout.splitlines())
+    for st, cls in (("smla_args", B.SmlaArgs), ("smla_plan", B.SmlaPlan)):
+        assert int(out[st]) == ctypes.sizeof(cls), st
+        for f in fields[st]:
+            assert int(out[f"{st}.{f}"]) == getattr(cls, f).offset, f"{st}.{f}"
+
+
+def test_header_constants_match_pages():
+    import json
+    c = json.load(open(os.path.join(ROOT, "tests", "golden", "page_constants.json")))
+    text = open(HEADER).read()
+    assert re.search(r"#define SMLA_HEAD_DIM (\d+)", text).group(1) == str(c["head_dim"]["value"])
+    assert re.search(r"#define SMLA_SWA_COLS (\d+)", text).group(1) == str(c["swa_columns"]["value"])
+
+
+def good_args():
+    a = B.SmlaArgs()
+    a.sum_q, a.batch, a.num_heads, a.width, a.dtype = 4, 2, 128, 640, B.SMLA_BF16
+    a.swa_rows, a.comp_rows = 256, 1024
+    return a
+
+
+def status(lib, a):
+    return lib.smla_decode(ctypes.byref(a) if a is not None else None, None)
+
+
+@pytest.mark.parametrize("mutate,code,needle", [
+    (lambda a: setattr(a, "num_heads", 96), B.SMLA_ERR_UNSUPPORTED, "num_heads"),
+    (lambda a: setattr(a, "num_heads", 16), B.SMLA_ERR_UNSUPPORTED, "num_heads"),
+    (lambda a: setattr(a, "dtype", 7), B.SMLA_ERR_INVALID_ARG, "dtype"),
+    (lambda a: setattr(a, "width", 127), B.SMLA_ERR_INVALID_ARG, "width"),
+    (lambda a: setattr(a, "sum_q", 5), B.SMLA_ERR_INVALID_ARG, "multiple of batch"),
+    (lambda a: setattr(a, "sum_q", -1), B.SMLA_ERR_INVALID_ARG, "sum_q"),
+    (lambda a: setattr(a, "batch", 0), B.SMLA_ERR_INVALID_ARG, "batch"),
+    (lambda a: setattr(a, "num_splits", 65), B.SMLA_ERR_INVALID_ARG, "num_splits"),
+    (lambda a: setattr(a, "max_splits", -2), B.SMLA_ERR_INVALID_ARG, "max_splits"),
+    (lambda a: setattr(a, "kernel", 9), B.SMLA_ERR_INVALID_ARG, "kernel"),
+    (lambda a: setattr(a, "swa_row_stride", 500), B.SMLA_ERR_INVALID_ARG, "stride"),
+    (lambda a: setattr(a, "comp_row_stride", 516), B.SMLA_ERR_INVALID_ARG, "stride"),
+    (lambda a: setattr(a, "q_stride_token", 128 * 512 + 4), B.SMLA_ERR_INVALID_ARG, "q_stride_token"),
+    (lambda a: setattr(a, "indices_row_stride", 600), B.SMLA_ERR_INVALID_ARG, "indices_row_stride"),
+    (lambda a: setattr(a, "comp_rows", -1), B.SMLA_ERR_INVALID_ARG, "row count"),
+])
+def test_host_argument_errors(lib, mutate, code, needle):
+    a = good_args()
+    mutate(a)
+    assert status(lib, a) == code
+    assert needle in B.smla_last_error()
+
+
+def test_null_args_and_empty_batch(lib):
+    assert status(lib, None) == B.SMLA_ERR_INVALID_ARG
+    a = good_args()
+    a.sum_q = 0
+    assert status(lib, a) == B.SMLA_OK            # nothing to launch, no device needed
+    a.dtype = B.SMLA_E4M3
+    a.swa_row_stride = 528                        # 528 B: multiple of 16 for FP8 rows
+    assert status(lib, a) == B.SMLA_OK
+
+
+def test_varlen_needs_no_divisibility(lib):
+    a = good_args()
+    a.sum_q = 0
+    a.cum_seq_lens_q = 16                          # any non-NULL value marks varlen; not read on host
+    assert status(lib, a) == B.SMLA_OK
+
+
+def test_status_strings(lib):
+    for code, name in ((0, "SMLA_OK"), (1, "SMLA_ERR_INVALID_ARG"), (2, "SMLA_ERR_UNSUPPORTED"),
+                       (3, "SMLA_ERR_WORKSPACE_TOO_SMALL"), (4, "SMLA_ERR_CUDA")):
+        assert B.smla_status_string(code) == name
+
+
+def test_binding_raises_on_missing_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        B.lib()

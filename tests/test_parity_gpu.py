@@ -1,0 +1,322 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances: max |dO| <= 2e-2 (BF16 inputs) or 4e-2 (FP8 E4M3 inputs),
+|dLSE| <= 1e-3, and the set of attended slots exact (masking probes)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mla_decode_token_gb300 import binding as B
+from sparse_mla_decode_token_gb300 import workloads as W
+
+from gpu_helpers import compare, device_inputs, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [B.KERNEL_CUDA_CORE]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mla_decode_token_gb300 import build
+    build.build()
+    B.lib()
+
+
+# ------------------------------------------------------- the five workloads
+
+# tokens checked per workload (the oracle evaluates them one by one)
+SAMPLE = {1: None, 2: None, 3: [0, 1, 37, 64, 100, 127], 4: [0, 1, 2, 50, 99, 160, 161], 5: None}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_config_parity(n, kernel):
+    w = W.config_workload(n)
+    out, lse, plan = run_gpu(w, kernel=kernel)
+    tokens = SAMPLE[n]
+    if tokens is not None:
+        tokens = [t for t in tokens if t < w.sum_q]
+    compare(w, out, lse, tokens=tokens)
+
+
+# ------------------------------------------- small cases: tiles + ragged tails
+
+def small_case(seed, *, dtype="bf16", H=128, width=128 + 300, batch=3, q_lens=1,
+               sinks=True, holes=True, topk="random", comp_rows=2048, seq_len=100000):
+    rng = np.random.default_rng(seed)
+    q_lens_arr = np.broadcast_to(np.asarray(q_lens), (batch,))
+    T = int(q_lens_arr.sum())
+    n_comp = width - 128
+    comp_valid = rng.integers(n_comp // 2, n_comp + 1, size=T) if holes else None
+    if topk == "random":
+        topk_lens = rng.integers(129, width + 1, size=T)
+    elif topk == "none":
+        topk_lens = None
+    else:
+        topk_lens = topk
+    return W.make_workload(name=f"small{seed}", seed=seed, dtype=dtype, batch=batch, q_lens=q_lens,
+                           num_heads=H, swa_rows=128 * batch + 64, comp_rows=comp_rows,
+                           width=width, seq_lens=seq_len, ring_len=128, comp_valid=comp_valid,
+                           topk_lens=topk_lens, sinks=sinks)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("splits", [1, 2, 3, 0])
+def test_small_parity(kernel, dtype, H, splits):
+    w = small_case(100 + H + splits, dtype=dtype, H=H)
+    out, lse, plan = run_gpu(w, kernel=kernel, num_splits=splits)
+    if splits:
+        assert plan["num_splits"] == splits
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_varlen_parity(kernel):
+    w = small_case(7, dtype="bf16", H=64, batch=6, q_lens=[1, 4, 2, 3, 1, 4], seq_len=5000)
+    assert w.cum_seq_lens_q is not None
+    out, lse, _ = run_gpu(w, kernel=kernel)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_swa_only_width_128(kernel):
+    w = small_case(8, dtype="e4m3", H=128, width=128, holes=False, topk="none")
+    out, lse, _ = run_gpu(w, kernel=kernel)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_forced_max_splits(kernel):
+    w = small_case(9, dtype="bf16", H=64, width=128 + 900, batch=2)
+    out, lse, plan = run_gpu(w, kernel=kernel, num_splits=B.MAX_SPLITS)
+    assert plan["num_splits"] == B.MAX_SPLITS
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_short_sequences_trim_swa_window(kernel):
+    # seq_len < 128: only the first pos + 1 SWA columns are in the window
+    w = small_case(10, dtype="bf16", H=64, batch=4, q_lens=2, seq_len=[3, 60, 127, 128], topk="none")
+    # put real rows into every SWA column so that the window, not -1, does the masking
+    rng = np.random.default_rng(10)
+    for t in range(w.sum_q):
+        w.indices[t, :128] = rng.choice(w.swa_kv.shape[0], 128, replace=False)
+    out, lse, _ = run_gpu(w, kernel=kernel)
+    compare(w, out, lse)
+
+
+# ------------------------------------------------------------ masking probes
+
+def probe_case(indices, *, seq_lens, topk_lens=None, H=64, dtype="bf16", sinks=None, bmm2=1.0):
+    """q = 0 and basis-vector rows: row r of the pools has a single 1 at dim r % 512
+    (SWA rows at dims 0..255, compressed rows at 256..511), so every output dim
+    shows whether its slot contributed, and LSE2 = log2(number of slots)."""
+    indices = np.asarray(indices, np.int32)
+    T = indices.shape[0]
+    one = 0x3F80 if dtype == "bf16" else 0x38
+    nptype = np.uint16 if dtype == "bf16" else np.uint8
+    swa = np.zeros((256, 512), nptype)
+    comp = np.zeros((256, 512), nptype)
+    for r in range(256):
+        swa[r, r] = one
+        comp[r, 256 + r] = one
+    seq_lens = np.asarray(seq_lens, np.int32)
+    return W.Workload(name="probe", dtype=dtype, batch=len(seq_lens), num_heads=H,
+                      q=np.zeros((T, H, 512), nptype), swa_kv=swa, comp_kv=comp, indices=indices,
+                      topk_lens=None if topk_lens is None else np.asarray(topk_lens, np.int32),
+                      seq_lens=seq_lens, cum_seq_lens_q=None,
+                      sinks=None if sinks is None else np.asarray(sinks, np.float32),
+                      bmm1_scale=1.0, bmm2_scale=bmm2)
+
+
+def check_probe(w, out, lse):
+    """Exact attended-slot set per token, checked against the oracle's slot list."""
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    for t in range(w.sum_q):
+        slots = oracle.valid_slots(t, indices=w.indices, topk_lens=w.topk_lens, seq_lens=w.seq_lens,
+                                   cum_seq_lens_q=None, batch=w.batch, swa_rows=256, comp_rows=256)
+        counts = np.zeros(512)
+        for (_, pool, row) in slots:
+            counts[row if pool == "swa" else 256 + row] += 1
+        n = len(slots)
+        nz_gpu = o[t] != 0
+        assert np.array_equal(nz_gpu, np.broadcast_to(counts > 0, nz_gpu.shape)), f"token {t}: slot set differs"
+        if n:
+            np.testing.assert_allclose(o[t], np.broadcast_to(counts / n * w.bmm2_scale, o[t].shape),
+                                       atol=TOL_PROBE)
+            np.testing.assert_allclose(l[t], math.log2(n), atol=1e-5)
+        else:
+            assert np.all(np.isneginf(l[t]))
+
+
+TOL_PROBE = 4e-3
+
+
+def probe_row(swa, comp, width):
+    row = np.full(width, -1, np.int32)
+    row[:len(swa)] = swa
+    row[128:128 + len(comp)] = comp
+    return row
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_masking_probes(kernel, dtype):
+    W_ = 128 + 200
+    rng = np.random.default_rng(11)
+    rows = []
+    # 0: -1 holes in both segments
+    r = probe_row(rng.permutation(256)[:128], rng.permutation(256)[:200], W_)
+    r[[0, 5, 127, 128, 200, 327]] = -1
+    rows.append(r)
+    # 1: topk_lens = 128 (SWA only)
+    rows.append(probe_row(rng.permutation(256)[:128], rng.permutation(256)[:200], W_))
+    # 2: topk_lens = W
+    rows.append(probe_row(rng.permutation(256)[:128], rng.permutation(256)[:200], W_))
+    # 3: random topk_lens with -1 tail
+    rows.append(probe_row(rng.permutation(256)[:100], rng.permutation(256)[:150], W_))
+    # 4: fully masked token
+    rows.append(np.full(W_, -1, np.int32))
+    # 5: everything beyond topk_lens = 0
+    rows.append(probe_row(rng.permutation(256)[:128], rng.permutation(256)[:200], W_))
+    # 6: duplicate rows count twice
+    rows.append(probe_row([3, 3, 3, 9], [7, 7, 8], W_))
+    # 7: short sequence (pos = 4): only 5 SWA columns in the window
+    rows.append(probe_row(rng.permutation(256)[:128], [1, 2], W_))
+    idx = np.stack(rows)
+    topk = np.array([W_, 128, W_, 200, W_, 0, W_, W_])
+    seq = [10 ** 6] * 7 + [5]
+    w = probe_case(idx, seq_lens=seq, topk_lens=topk, dtype=dtype, bmm2=0.5)
+    out, lse, _ = run_gpu(w, kernel=kernel)
+    check_probe(w, out, lse)
+    for splits in (2, 5):
+        out, lse, _ = run_gpu(w, kernel=kernel, num_splits=splits)
+        check_probe(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_out_of_range_index_is_masked_and_flagged(kernel):
+    W_ = 128 + 8
+    idx = np.stack([probe_row([0, 1, 2], [4, 300, 5], W_), probe_row([0, -7], [4], W_),
+                    probe_row([0], [1], W_)])
+    w = probe_case(idx, seq_lens=[10 ** 6] * 3)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse, _ = run_gpu(w, kernel=kernel, error_word=err)
+    assert int(err.item()) & B.DEVERR_INDEX_OUT_OF_RANGE
+    masked = w.indices.copy()
+    masked[0, 129] = -1
+    masked[1, 1] = -1
+    w2 = probe_case(masked, seq_lens=[10 ** 6] * 3)
+    check_probe(w2, out, lse)
+    err.zero_()
+    run_gpu(w2, kernel=kernel, error_word=err)
+    assert int(err.item()) == 0
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_empty_batch_is_a_noop():
+    w = small_case(12, H=64)
+    d = device_inputs(w)
+    out = torch.empty((0, 64, 512), dtype=torch.bfloat16, device="cuda")
+    args = B.make_args(q=d["q"][:0], swa_kv=d["swa"], compressed_kv=d["comp"],
+                       sparse_indices=d["indices"][:0], seq_lens=d["seq_lens"], out=out)
+    B.smla_decode(args)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_scales_as_device_tensors(kernel):
+    w = small_case(13, dtype="e4m3", H=128)
+    o1, l1, _ = run_gpu(w, kernel=kernel)
+    o2, l2, _ = run_gpu(w, kernel=kernel, bmm_as_tensor=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_deterministic(kernel):
+    w = small_case(14, dtype="bf16", H=128)
+    d = device_inputs(w)
+    o1, l1, _ = run_gpu(w, d, kernel=kernel, num_splits=3)
+    o2, l2, _ = run_gpu(w, d, kernel=kernel, num_splits=3)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_paged_and_strided_layouts(kernel):
+    """Pools as paged HND views [pages, 1, page_size, 512] and a padded row stride;
+    the query as a slice of a wider buffer (token stride > H * 512)."""
+    w = small_case(15, dtype="bf16", H=64, comp_rows=64 * 32)
+    d = device_inputs(w)
+    ref_o, ref_l, _ = run_gpu(w, d, kernel=kernel)
+    comp_paged = d["comp"].view(64, 1, 32, 512)
+    swa_pad = torch.zeros((d["swa"].shape[0], 520), dtype=d["swa"].dtype, device="cuda")
+    swa_pad[:, :512] = d["swa"]
+    q_wide = torch.zeros((w.sum_q, 64 * 512 + 64), dtype=d["q"].dtype, device="cuda")
+    q_wide[:, :64 * 512] = d["q"].reshape(w.sum_q, -1)
+    q_view = torch.as_strided(q_wide, (w.sum_q, 64, 512), (64 * 512 + 64, 512, 1))
+    out = torch.empty_like(ref_o)
+    lse = torch.empty_like(ref_l)
+    args = B.make_args(q=q_view, swa_kv=swa_pad[:, :512], compressed_kv=comp_paged,
+                       sparse_indices=d["indices"], seq_lens=d["seq_lens"], out=out,
+                       sparse_topk_lens=d["topk_lens"], sinks=d["sinks"],
+                       bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, out_lse=lse, kernel=kernel)
+    assert args.swa_row_stride == 520 and args.q_stride_token == 64 * 512 + 64
+    B.smla_decode(args)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+
+
+def test_workspace_too_small_is_rejected():
+    w = small_case(16, H=64)
+    d = device_inputs(w)
+    out = torch.empty((w.sum_q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    args = B.make_args(q=d["q"], swa_kv=d["swa"], compressed_kv=d["comp"], sparse_indices=d["indices"],
+                       seq_lens=d["seq_lens"], out=out, num_splits=4)
+    need = B.smla_plan_decode(args).workspace_bytes
+    assert need > 0
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), need - 256
+    with pytest.raises(B.SmlaError) as e:
+        B.smla_decode(args)
+    assert e.value.status == B.SMLA_ERR_WORKSPACE_TOO_SMALL
+    args.out = out.data_ptr() + 2                  # misaligned output
+    args.workspace_bytes = need
+    with pytest.raises(B.SmlaError) as e:
+        B.smla_decode(args)
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG
+
+
+def test_many_tokens_grid():
+    """More than 65535 tokens: tokens live on grid.x, so no launch limit is hit.
+
+    q = 0 keeps the inputs small: every output is the mean of the token's rows."""
+    T, H = 70000, 64
+    rng = np.random.default_rng(17)
+    gen = torch.Generator().manual_seed(17)
+    swa_bits = W._to_bf16_bits(torch.randn(256, 512, generator=gen))
+    comp_bits = W._to_bf16_bits(torch.randn(512, 512, generator=gen))
+    idx = np.full((T, 136), -1, np.int32)
+    idx[:, :8] = rng.integers(0, 256, size=(T, 8))
+    idx[:, 128:136] = rng.integers(0, 512, size=(T, 8))
+    zero_q = np.broadcast_to(np.zeros((1, H, 512), np.uint16), (T, H, 512))   # a view, no memory
+    w = W.Workload(name="many", dtype="bf16", batch=T, num_heads=H, q=zero_q, swa_kv=swa_bits,
+                   comp_kv=comp_bits, indices=idx, topk_lens=None,
+                   seq_lens=np.full(T, 10 ** 6, np.int32), cum_seq_lens_q=None, sinks=None,
+                   bmm1_scale=1.0, bmm2_scale=1.0)
+    bf = lambda a: torch.from_numpy(a).view(torch.int16).view(torch.bfloat16).cuda()
+    d = dict(q=torch.zeros((T, H, 512), dtype=torch.bfloat16, device="cuda"), swa=bf(swa_bits),
+             comp=bf(comp_bits), indices=torch.from_numpy(idx).cuda(), topk_lens=None,
+             seq_lens=torch.from_numpy(w.seq_lens).cuda(), cum=None, sinks=None)
+    out, lse, plan = run_gpu(w, d)
+    assert plan["grid"] >= T
+    compare(w, out, lse, tokens=[0, 1, 65535, 65536, T - 1])
