@@ -271,6 +271,8 @@ def test_paged_and_strided_layouts(kernel):
                        sparse_topk_lens=d["topk_lens"], sinks=d["sinks"],
                        bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, out_lse=lse, kernel=kernel)
     assert args.swa_row_stride == 520 and args.q_stride_token == 64 * 512 + 64
+    ws = torch.empty(max(B.smla_plan_decode(args).workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
     B.smla_decode(args)
     torch.cuda.synchronize()
     assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
