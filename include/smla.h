@@ -68,6 +68,8 @@ typedef enum smla_kernel {
 
 /* Bits the kernels OR into *error_word (device-side detection, no trap). */
 #define SMLA_DEVERR_INDEX_OUT_OF_RANGE 0x1  /* index < -1 or >= pool rows: slot treated as masked */
+#define SMLA_DEVERR_TIMEOUT 0x2             /* a bounded on-device wait expired; outputs are invalid */
+#define SMLA_DEVERR_INTERNAL 0x4            /* an internal limit was hit; outputs are invalid */
 
 /*
  * Arguments of one decode call.  Zero-initialise and fill what you use.

@@ -77,6 +77,9 @@ smla_status check_shapes(const smla_args* a) {
   return SMLA_OK;
 }
 
+// Kernel that SMLA_KERNEL_AUTO selects.
+constexpr int kAutoKernel = SMLA_KERNEL_CUDA_CORE;
+
 int g_sm_count[64];
 
 smla_status sm_count(int device, int* out) {
@@ -98,23 +101,45 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
   st = sm_count(device, &sms);
   if (st != SMLA_OK) return st;
   memset(plan, 0, sizeof(*plan));
-  if (a->kernel == SMLA_KERNEL_TCGEN05)
-    return fail(SMLA_ERR_UNSUPPORTED, "the tcgen05 kernel is not built into this library");
-  plan->kernel = SMLA_KERNEL_CUDA_CORE;
-  plan->ctas_per_split = cuda_core_ctas_per_split(a->num_heads);
-  plan->threads = cuda_core_threads();
-  plan->smem_bytes = cuda_core_smem_bytes();
-  const int resident = 2;                         // CTAs per SM at this smem size
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
+  const int kernel = a->kernel == SMLA_KERNEL_AUTO ? kAutoKernel : a->kernel;
   int S = a->num_splits;
-  if (S == 0) {
-    const int64_t units = (int64_t)a->sum_q * plan->ctas_per_split;
-    const int64_t target = (int64_t)sms * resident;
-    int64_t want = units > 0 ? (target + units - 1) / units : 1;
-    const int64_t by_width = (a->width + 255) / 256;  // keep >= 256 columns per split
-    if (want > by_width) want = by_width;
-    if (want > max_splits) want = max_splits;
-    S = (int)(want < 1 ? 1 : want);
+  if (kernel == SMLA_KERNEL_TCGEN05) {
+    // One 2-CTA cluster per (token, split), one cluster per pair of SMs.
+    plan->kernel = SMLA_KERNEL_TCGEN05;
+    plan->ctas_per_split = 2;
+    plan->threads = tc_threads();
+    plan->smem_bytes = tc_smem_bytes(a->dtype);
+    const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
+    if (s_min > SMLA_MAX_SPLITS)
+      return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
+    if (S != 0 && S < s_min)
+      return fail(SMLA_ERR_INVALID_ARG, "num_splits %d < %d: the tcgen05 kernel takes at most %d columns per split",
+                  S, s_min, SMLA_TC_MAX_SPLIT_COLS);
+    if (S == 0) {
+      const int64_t pairs = sms / 2;
+      int64_t want = a->sum_q > 0 ? (pairs + a->sum_q - 1) / a->sum_q : 1;
+      const int64_t by_width = (a->width + 255) / 256;  // keep >= 4 tiles of 64 slots per split
+      if (want > by_width) want = by_width;
+      if (want > max_splits) want = max_splits;
+      if (want < s_min) want = s_min;
+      S = (int)(want < 1 ? 1 : want);
+    }
+  } else {
+    plan->kernel = SMLA_KERNEL_CUDA_CORE;
+    plan->ctas_per_split = cuda_core_ctas_per_split(a->num_heads);
+    plan->threads = cuda_core_threads();
+    plan->smem_bytes = cuda_core_smem_bytes();
+    const int resident = 2;                         // CTAs per SM at this smem size
+    if (S == 0) {
+      const int64_t units = (int64_t)a->sum_q * plan->ctas_per_split;
+      const int64_t target = (int64_t)sms * resident;
+      int64_t want = units > 0 ? (target + units - 1) / units : 1;
+      const int64_t by_width = (a->width + 255) / 256;  // keep >= 256 columns per split
+      if (want > by_width) want = by_width;
+      if (want > max_splits) want = max_splits;
+      S = (int)(want < 1 ? 1 : want);
+    }
   }
   plan->num_splits = S;
   const int64_t grid = (int64_t)a->sum_q * S * plan->ctas_per_split;
@@ -128,6 +153,12 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
 }
 
 }  // namespace
+
+smla_status record_error(smla_status st, const char* msg) {
+  g_last_error = msg;
+  return st;
+}
+
 }  // namespace smla
 
 using namespace smla;
@@ -213,7 +244,8 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
     ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_begin), stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
   }
-  ce = launch_decode_cuda_core(p, plan.grid, stream);
+  ce = plan.kernel == SMLA_KERNEL_TCGEN05 ? launch_decode_tc(p, plan.grid, stream)
+                                          : launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
   if (a->profile_event_end) {
     ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_end), stream);

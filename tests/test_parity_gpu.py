@@ -16,7 +16,7 @@ from gpu_helpers import compare, device_inputs, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [B.KERNEL_CUDA_CORE]
+KERNELS = [B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05]
 
 
 @pytest.fixture(scope="module", autouse=True)
