@@ -157,6 +157,31 @@ smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes
  */
 smla_status smla_decode(const smla_args* args, void* stream);
 
+/*
+ * Allocation-free variant of smla_decode (the documentation pages have no
+ * counterpart; it exists for callers that cannot allocate device memory, e.g.
+ * an inference runtime's plugin enqueue callback that must not allocate, a
+ * process whose device memory is fully reserved by another allocator, or a
+ * plain C caller with no device allocator of its own).
+ *
+ * Same arguments and results as smla_decode, except that args->workspace and
+ * args->workspace_bytes are ignored: the split-K scratch is a library-owned
+ * __device__ array of SMLA_STATIC_WORKSPACE_BYTES that every GPU loading the
+ * library holds until the process exits.  Calls that need more scratch than
+ * that (see smla_workspace_size) return SMLA_ERR_WORKSPACE_TOO_SMALL and launch
+ * nothing; lower num_splits / max_splits or use smla_decode.  The function
+ * calls no allocator.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array, and each launch
+ * overwrites the scratch it reads, so nothing needs clearing between calls;
+ * but calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race on the array and give wrong results.  Order them on one stream.
+ */
+#define SMLA_STATIC_WORKSPACE_BYTES (64u << 20)
+smla_status smla_decode_static_workspace(const smla_args* args, void* stream);
+
 /* Static text for a status code. */
 const char* smla_status_string(smla_status status);
 

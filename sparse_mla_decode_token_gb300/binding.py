@@ -77,6 +77,7 @@ EXPORTS = {
     "smla_plan_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(SmlaPlan)]),
     "smla_workspace_size": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "smla_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
+    "smla_decode_static_workspace": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
     "smla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "smla_last_error": (ctypes.c_char_p, []),
     "smla_abi_version": (ctypes.c_int, []),
@@ -135,6 +136,18 @@ def smla_decode(args: SmlaArgs, stream: Optional[int] = None) -> None:
     if stream is None:
         stream = torch.cuda.current_stream().cuda_stream
     _check(lib().smla_decode(ctypes.byref(args), _c_void_p(stream)))
+
+
+STATIC_WORKSPACE_BYTES = 64 << 20
+
+
+def smla_decode_static_workspace(args: SmlaArgs, stream: Optional[int] = None) -> None:
+    """Like ``smla_decode`` but with the library's own static split-K scratch
+    (``args.workspace`` is ignored; nothing is allocated).  For callers that
+    cannot allocate device memory; calls that overlap on the GPU race."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(lib().smla_decode_static_workspace(ctypes.byref(args), _c_void_p(stream)))
 
 
 # ---------------------------------------------------------- tensor marshalling
