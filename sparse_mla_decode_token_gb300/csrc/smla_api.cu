@@ -78,7 +78,7 @@ smla_status check_shapes(const smla_args* a) {
 }
 
 // Kernel that SMLA_KERNEL_AUTO selects.
-constexpr int kAutoKernel = SMLA_KERNEL_CUDA_CORE;
+constexpr int kAutoKernel = SMLA_KERNEL_TCGEN05;
 
 int g_sm_count[64];
 
