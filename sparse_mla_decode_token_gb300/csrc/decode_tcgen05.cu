@@ -36,26 +36,29 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kN = 64;              // slots per tile
+constexpr int kMaxN = 64;           // largest tile (slots per tile)
 constexpr int kHalfDims = 256;      // output dims per CTA
 constexpr int kThreads = 288;       // 4 producer warps, 1 MMA warp, 4 softmax warps
 constexpr int kProducerThreads = 128;
 constexpr int kMmaWarp = 4;          // warps 5-8 run the softmax and the epilogue
+constexpr int kSoftmaxWarp0 = 5;
 constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;       // O: 256 fp32 columns
-constexpr uint32_t kSCol = 256;     // S: two buffers of 64 fp32 columns
+constexpr uint32_t kSCol = 256;     // S: two buffers of N fp32 columns, then P: two buffers of 16 columns
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kMaxStages = 8;
 
 struct TcSmall {
   uint64_t q_full;
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
-  uint64_t xin_full, xout_free, o_full;
-  int32_t meta_n[8];
-  int32_t rows[2][kN];
+  uint64_t xin_full[2], xout_free[2];
+  uint64_t o_full;
+  int32_t meta_n[kMaxStages];
+  int32_t rows[2][kMaxN];
   int32_t rows_n[2];
   uint32_t tmem_base;
   int32_t abort_flag;
@@ -64,26 +67,29 @@ struct TcSmall {
 template <bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
   static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
   static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
-  static constexpr int kStages = kFp8 ? 4 : 2;
+  static constexpr int kStages = 6;
   static constexpr int kKStep = 32 / kElem;                    // MMA K per instruction
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
   static constexpr int kK2 = kN / kKStep;                      // PV K steps
+  static constexpr int kPCols = kN * kElem / 4;                // TMEM columns of one P buffer
+  static constexpr uint32_t kPCol = kSCol + 2 * kN;
   static constexpr int kRegionQ = 128 * 128;                   // 128 rows x 128 B
-  static constexpr int kRegionKV = kN * 128;                   // 64 rows x 128 B
+  static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
   static constexpr int kQBytes = kRegions * kRegionQ;
   static constexpr int kStageBytes = kRegions * kRegionKV;
-  static constexpr int kPBytes = 128 * 128;
-  static constexpr int kXBytes = 128 * kN * 4;
+  static constexpr int kXBytes = 128 * kN * 4;                 // one exchange buffer (fp32 S rows)
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffX = kOffP + 2 * kPBytes;
-  static constexpr int kOffIdx = kOffX + kXBytes;
+  static constexpr int kOffX = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffIdx = kOffX + 2 * kXBytes;
   static constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
-  static_assert(kStages <= 8, "barrier arrays hold 8 stages");
+  static_assert(kStages <= kMaxStages, "barrier arrays");
+  static_assert(kN <= kMaxN, "row lists");
+  static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -142,6 +148,7 @@ template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<kFp8>;
+  constexpr int kN = C::kN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
@@ -150,7 +157,6 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   int32_t* idx_s = reinterpret_cast<int32_t*>(base + C::kOffIdx);
   const uint32_t q_addr = base_addr + C::kOffQ;
   const uint32_t kv_addr = base_addr + C::kOffKV;
-  const uint32_t p_addr = base_addr + C::kOffP;
   const uint32_t x_addr = base_addr + C::kOffX;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -174,11 +180,11 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
 
   // ---------------------------------------------------------------- set-up
   {
-    // zero the KV stages and P buffers (rows past a tile's slot count then hold
-    // finite data), and the Q rows of absent heads
+    // zero the KV stages (rows past a tile's slot count then hold finite data)
+    // and the Q rows of absent heads
     const uint4 z = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
-    const int zn = (C::kOffX - C::kOffKV) / 16;
+    const int zn = C::kStages * C::kStageBytes / 16;
     for (int i = tid; i < zn; i += kThreads) zp[i] = z;
     if (H < 128) {
       for (int kb = 0; kb < C::kRegions; ++kb) {
@@ -196,12 +202,12 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), 128);
-        mbar_init(bar(sm.p_full[b]), 128);
+        mbar_init(bar(sm.s_empty[b]), 4);
+        mbar_init(bar(sm.p_full[b]), 4);
         mbar_init(bar(sm.p_empty[b]), 1);
+        mbar_init(bar(sm.xin_full[b]), 1);
+        mbar_init(bar(sm.xout_free[b]), 4);
       }
-      mbar_init(bar(sm.xin_full), 128);
-      mbar_init(bar(sm.xout_free), 128);
       mbar_init(bar(sm.o_full), 1);
       sm.abort_flag = 0;
       fence_mbar_init_cluster();
@@ -234,7 +240,7 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
       const int st = j % C::kStages;
       wait_bar(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1, false);
       if (warp == 0) {
-        // next tile: up to 64 valid slots of one pool, in column order
+        // next tile: up to N valid slots of one pool, in column order
         int cnt = 0, pool = 0;
         while (cnt < kN && seg < 2) {
           const int lo = seg == 0 ? c0 : max(c0, kSwaCols);
@@ -307,22 +313,23 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issue
+    // Order: QK of tile k, then PV of tile k-2, so that QK runs two tiles ahead
+    // of the softmax and PV never waits behind a QK.
     constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
     constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
     bool ok = warp_wait(cx, bar(sm.q_full), 0);
-    int j = 0;
+    int k = 0;
     auto issue_pv = [&](int jj) -> bool {
       const int b = jj & 1, st = jj % C::kStages;
       if (!warp_wait(cx, bar(sm.p_full[b]), (jj >> 1) & 1)) return false;
-      fence_proxy_async_smem();
       tc_fence_after();
       if (lane == 0) {
         const uint32_t stage = kv_addr + st * C::kStageBytes;
 #pragma unroll
-        for (int k = 0; k < C::kK2; ++k) {
-          const uint64_t a = desc_sw128(p_addr + b * C::kPBytes + k * 32, 16, 1024);
-          const uint64_t v = desc_sw128(stage + k * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
-          mma<kFp8>(tmem + kOCol, a, v, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::kK2; ++kk) {
+          const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
+          mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
+                           idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(sm.p_empty[b]));
         mma_commit(bar(sm.kv_empty[st]));
@@ -331,29 +338,29 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
       return true;
     };
     if (ok) {
-      for (;; ++j) {
-        const int st = j % C::kStages;
-        if (!warp_wait(cx, bar(sm.kv_full[st]), (j / C::kStages) & 1)) { ok = false; break; }
+      for (;; ++k) {
+        const int st = k % C::kStages;
+        if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) { ok = false; break; }
         const int n = sm.meta_n[st];
         if (n == 0) break;
-        const int b = j & 1;
-        if (!warp_wait(cx, bar(sm.s_empty[b]), ((j >> 1) & 1) ^ 1)) { ok = false; break; }
+        const int b = k & 1;
+        if (!warp_wait(cx, bar(sm.s_empty[b]), ((k >> 1) & 1) ^ 1)) { ok = false; break; }
         fence_proxy_async_smem();
         tc_fence_after();
         if (lane == 0) {
           const uint32_t stage = kv_addr + st * C::kStageBytes;
 #pragma unroll
-          for (int k = 0; k < C::kK1; ++k) {
-            const uint64_t a = desc_sw128(q_addr + (k >> 2) * C::kRegionQ + (k & 3) * 32, 16, 1024);
-            const uint64_t kd = desc_sw128(stage + (k >> 2) * C::kRegionKV + (k & 3) * 32, 16, 1024);
-            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, k > 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::kK1; ++kk) {
+            const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
+            const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
+            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(sm.s_full[b]));
         }
         __syncwarp();
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        if (k >= 2 && !issue_pv(k - 2)) { ok = false; break; }
       }
-      if (ok && j > 0) ok = issue_pv(j - 1);
+      for (int jj = max(0, k - 2); ok && jj < k; ++jj) ok = issue_pv(jj);
     }
     if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every MMA issued above is done
     __syncwarp();
@@ -362,65 +369,98 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;
     const bool active = q4 * 32 < H;                   // warp-uniform
+    const bool leader = warp == kSoftmaxWarp0 && lane == 0;
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
-    const uint32_t x_peer = map_to_rank(x_addr, peer);
-    const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full), peer);
-    const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free), peer);
+    const uint32_t xbytes = (uint32_t)(H * kN * 4);    // bytes the peer pushes per tile
+    // peer addresses of exchange buffer / barrier b are these plus b * (stride)
+    const uint32_t x_peer0 = map_to_rank(x_addr, peer);
+    const uint32_t xin_full_peer0 = map_to_rank(bar(sm.xin_full[0]), peer);
+    const uint32_t xout_free_peer0 = map_to_rank(bar(sm.xout_free[0]), peer);
+    constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
+    if (leader) {
+      mbar_arrive_expect_tx(bar(sm.xin_full[0]), xbytes);
+      mbar_arrive_expect_tx(bar(sm.xin_full[1]), xbytes);
+    }
+    if (!active) {
+      // rows of absent heads: P = 0 in both buffers, so O and S stay 0 there
+      uint32_t zr[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) zr[i] = 0u;
+      tmem_st16(tl + C::kPCol, zr);
+      tmem_st16(tl + C::kPCol + C::kPCols, zr);
+      tmem_wait_st();
+    }
+    // load this CTA's partial S of tile jj into v (warp-collective)
+    auto load_s = [&](int jj, float (&v)[kN]) {
+      uint32_t r[32];
+#pragma unroll
+      for (int h32 = 0; h32 < kN / 32; ++h32) {
+        tmem_ld32(tl + kSCol + (jj & 1) * kN + h32 * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[h32 * 32 + i] = __uint_as_float(r[i]);
+      }
+    };
+    // send this CTA's partial S of tile jj to the peer (tile jj's S must be ready)
+    auto push = [&](int jj) -> bool {
+      const int b = jj & 1;
+      if (!warp_wait(cx, bar(sm.s_full[b]), (jj >> 1) & 1)) return false;
+      tc_fence_after();
+      if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[b]), ((jj >> 1) & 1) ^ 1, true)) return false;
+      if (active) {
+        float v[kN];
+        load_s(jj, v);
+#pragma unroll
+        for (int c4 = 0; c4 < kN / 4; ++c4)
+          st_async_v4(x_peer0 + b * C::kXBytes + (uint32_t)((c4 * 128 + h) * 16), v[4 * c4], v[4 * c4 + 1],
+                      v[4 * c4 + 2], v[4 * c4 + 3], xin_full_peer0 + b * kBarStride);
+      }
+      return true;
+    };
+
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
+    bool ok = warp_wait(cx, bar(sm.kv_full[0]), 0);
+    int n_cur = ok ? sm.meta_n[0] : 0;
+    if (n_cur > 0) ok = push(0);
     int j = 0;
-    for (;; ++j) {
-      const int st = j % C::kStages;
-      if (!(ok = warp_wait(cx, bar(sm.kv_full[st]), (j / C::kStages) & 1))) break;
-      const int n = sm.meta_n[st];
-      if (n == 0) break;
+    while (ok && n_cur > 0) {
+      // ---- consume tile j: S = S_0 + S_1
       const int b = j & 1;
-      if (!(ok = warp_wait(cx, bar(sm.s_full[b]), (j >> 1) & 1))) break;
+      if (!(ok = warp_wait(cx, bar(sm.xin_full[b]), (j >> 1) & 1, true))) break;
       tc_fence_after();
       float sv[kN];
       if (active) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tl + kSCol + b * kN, r0);
-        tmem_ld32(tl + kSCol + b * kN + 32, r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = __uint_as_float(r0[i]);
-          sv[32 + i] = __uint_as_float(r1[i]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(sm.s_empty[b]));
-      // S = S_0 + S_1: push my partial to the peer, add the peer's partial
-      if (!(ok = warp_wait(cx, bar(sm.xout_free), (j & 1) ^ 1, true))) break;
-      if (active) {
-#pragma unroll
-        for (int c4 = 0; c4 < kN / 4; ++c4)
-          st_cluster_v4(x_peer + (uint32_t)((c4 * 128 + h) * 16), sv[4 * c4], sv[4 * c4 + 1], sv[4 * c4 + 2],
-                        sv[4 * c4 + 3]);
-      }
-      mbar_arrive_cluster(xin_full_peer);
-      if (!(ok = warp_wait(cx, bar(sm.xin_full), j & 1, true))) break;
-      if (active) {
+        load_s(j, sv);
 #pragma unroll
         for (int c4 = 0; c4 < kN / 4; ++c4) {
-          const float4 v = ld_shared_v4(x_addr + (uint32_t)((c4 * 128 + h) * 16));
+          const float4 v = ld_shared_v4(x_addr + b * C::kXBytes + (uint32_t)((c4 * 128 + h) * 16));
           sv[4 * c4] += v.x;
           sv[4 * c4 + 1] += v.y;
           sv[4 * c4 + 2] += v.z;
           sv[4 * c4 + 3] += v.w;
         }
       }
-      mbar_arrive_cluster(xout_free_peer);
-      // online softmax, base 2, lazy rescale
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(sm.s_empty[b]));                    // S buffer b may be overwritten
+        mbar_arrive_cluster_relaxed(xout_free_peer0 + b * kBarStride);   // exchange buffer b read out
+      }
+      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[b]), xbytes);   // for tile j + 2
+      // ---- look ahead: push tile j+1 so that the exchange overlaps this tile's softmax
+      const int st1 = (j + 1) % C::kStages;
+      if (!(ok = warp_wait(cx, bar(sm.kv_full[st1]), ((j + 1) / C::kStages) & 1))) break;
+      const int n_next = sm.meta_n[st1];
+      if (n_next > 0 && !(ok = push(j + 1))) break;
+      // ---- online softmax, base 2, lazy rescale
       bool rescale = false;
       float alpha = 1.f;
       if (active) {
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kN; ++i) {
-          sv[i] = (i < n) ? sv[i] * c : -INFINITY;
+          sv[i] = (i < n_cur) ? sv[i] * c : -INFINITY;
           mx = fmaxf(mx, sv[i]);
         }
         if (mx > m_run + kRescaleThreshold) {
@@ -454,27 +494,22 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
         tmem_wait_st();
       }
       if (active) {
-        const uint32_t prow = p_addr + b * C::kPBytes;
+        uint32_t pr[16];
         if constexpr (kFp8) {
 #pragma unroll
-          for (int c16 = 0; c16 < kN / 16; ++c16) {
-            const float* v = sv + 16 * c16;
-            st_shared_v4(prow + sw128_offset(h, c16), pack_e4m3x4(v[0], v[1], v[2], v[3]),
-                         pack_e4m3x4(v[4], v[5], v[6], v[7]), pack_e4m3x4(v[8], v[9], v[10], v[11]),
-                         pack_e4m3x4(v[12], v[13], v[14], v[15]));
-          }
+          for (int i = 0; i < 16; ++i) pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
         } else {
 #pragma unroll
-          for (int c8 = 0; c8 < kN / 8; ++c8) {
-            const float* v = sv + 8 * c8;
-            st_shared_v4(prow + sw128_offset(h, c8), pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-          }
+          for (int i = 0; i < 16; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
         }
+        tmem_st16(tl + C::kPCol + b * C::kPCols, pr);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(sm.p_full[b]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.p_full[b]));
+      ++j;
+      n_cur = n_next;
     }
     const int ntiles = j;
     if (ok && ntiles > 0) {
@@ -507,13 +542,13 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
         if (S == 1) {
           uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            o[k] = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                              pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+          for (int q = 0; q < 4; ++q)
+            o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         } else {
           float4* o = reinterpret_cast<float4*>(p.part_o + (row_th * S + s) * kHeadDim + d0);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
       if (rank == 0) {
