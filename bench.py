@@ -260,10 +260,11 @@ def run_gpu(args):
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
+    err_word = torch.zeros(1, dtype=torch.int32, device=dev)
     args_c = B.make_args(q=d_q, swa_kv=d_swa, compressed_kv=d_comp, sparse_indices=d_idx,
                          seq_lens=d_seq, out=out, sparse_topk_lens=d_lens, cum_seq_lens_q=d_cum,
                          sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
-                         out_lse=lse, kernel=args.kernel)
+                         out_lse=lse, kernel=args.kernel, error_word=err_word)
     plan = B.smla_plan_decode(args_c, local)
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
@@ -380,6 +381,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
+        "device_error_word": int(err_word.item()),
         "clocks": clocks.summary(),
     }
     print(json.dumps(line))

@@ -29,9 +29,18 @@ def device_inputs(w, device="cuda"):
     )
 
 
+DEVERR_FATAL = 0x2 | 0x4      # a bounded on-device wait expired / an internal limit was hit
+
+
 def run_gpu(w, d=None, *, num_splits=0, max_splits=0, kernel=B.KERNEL_AUTO, bmm_as_tensor=False,
             error_word=None, sync=True):
-    """Run the decode on the GPU; returns (out bf16 tensor, lse tensor, plan dict)."""
+    """Run the decode on the GPU; returns (out bf16 tensor, lse tensor, plan dict).
+
+    Every run carries a device error word; a timeout or internal-limit bit fails
+    the call (index range errors are left to the caller to inspect)."""
+    own_err = error_word is None
+    if own_err:
+        error_word = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = device_inputs(w) if d is None else d
     T, H = w.sum_q, w.num_heads
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
@@ -55,6 +64,7 @@ def run_gpu(w, d=None, *, num_splits=0, max_splits=0, kernel=B.KERNEL_AUTO, bmm_
     B.smla_decode(args)
     if sync:
         torch.cuda.synchronize()
+        assert int(error_word.item()) & DEVERR_FATAL == 0, f"device error word {int(error_word.item()):#x}"
     return out, lse, (plan.as_dict() if plan is not None else None)
 
 
