@@ -3,21 +3,31 @@
 // Work unit: one (token, split) runs on a cluster of two CTAs.  CTA r of the
 // pair owns output dims [256 r, 256 r + 256): an fp32 accumulator for 128 heads
 // x 512 dims is 256 KB, the whole tensor memory of one SM, so the output is
-// split across the pair.  Per tile of up to 64 selected slots:
+// split across the pair.  Per tile of up to N selected slots (N = 64 for E4M3,
+// 32 for BF16):
 //
-//   producer warps 0-3  gather the pair's half of every selected row (256 dims)
-//                       with 16-byte cp.async into a 128-byte-swizzled,
-//                       UMMA-canonical shared-memory tile (index compaction first:
-//                       masked slots are never loaded)
-//   MMA warp 4          S_r = Q_r K_r^T   (M = 128 heads, N = 64 slots, K = 256 dims)
-//                       O_r += P V_r      (M = 128 heads, N = 256 dims, K = 64 slots)
-//                       one elected thread issues tcgen05.mma, accumulators in TMEM
-//   softmax warps 5-8   one thread per head: read S_r from TMEM, send it to the
-//                       peer CTA through distributed shared memory, add the
-//                       peer's half (S = S_0 + S_1, identical in both CTAs),
-//                       online softmax in base 2 with lazy rescaling of O, write
-//                       P (BF16 or E4M3) for the PV MMA; finally normalise O and
-//                       store it (BF16 output or fp32 split partial) plus LSE.
+//   set-up (all warps)  stage the split's index columns and compact the valid
+//                       slots (block-wide scan) into a list: SWA slots, then
+//                       compressed slots; tiles are runs of N list entries of
+//                       one pool (masked slots are never loaded)
+//   producer warps 0-3  warp w gathers tiles w, w+4, ...: the pair's half of
+//                       every selected row (256 dims) with TMA tile::gather4
+//                       (four rows per instruction) into a 128-byte-swizzled,
+//                       UMMA-canonical shared-memory tile; TMA requests of one
+//                       warp are served one after another, so four warps issue
+//   MMA warp 4          S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
+//                       O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
+//                       P read from TMEM); one thread issues tcgen05.mma, QK two
+//                       tiles ahead of PV; accumulators live in TMEM
+//   softmax warps 5-12  two warpgroups, one per half of the tile's slots; one
+//                       thread per (head, half): read S_r from TMEM, push it to
+//                       the peer CTA with st.async (completing bytes on the
+//                       peer's mbarrier), add the peer's partial (S = S_0 + S_1,
+//                       identical in both CTAs), exchange the half-row maxima
+//                       between the warpgroups, online softmax in base 2 with
+//                       lazy rescaling of O, write P (BF16 or E4M3) into TMEM;
+//                       finally normalise O and store it (BF16 output or fp32
+//                       split partial) plus the LSE.
 //
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
@@ -26,7 +36,10 @@
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises an abort flag,
 // ORs SMLA_DEVERR_TIMEOUT into the error word, lets every role leave its loop,
-// waits for its own copies and MMAs, frees its TMEM and returns.
+// waits for its own copies and MMAs, frees its TMEM and returns.  No role
+// waits on an unbounded hardware barrier inside its loop.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -36,16 +49,20 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kMaxN = 64;           // largest tile (slots per tile)
-constexpr int kHalfDims = 256;      // output dims per CTA
-constexpr int kThreads = 288;       // 4 producer warps, 1 MMA warp, 4 softmax warps
-constexpr int kProducerThreads = 128;
-constexpr int kMmaWarp = 4;          // warps 5-8 run the softmax and the epilogue
-constexpr int kSoftmaxWarp0 = 5;
+constexpr int kMaxN = 64;            // largest tile (slots per tile)
+constexpr int kHalfDims = 256;       // output dims per CTA
+constexpr int kProducerWarps = 4;    // TMA gathers: warp w issues tiles w, w + 4, ...
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kSoftmaxWarp0 = kMmaWarp + 1;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
+constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of a staged index row
+constexpr int kChunksPerWarp = (kMaxChunks + kWarps - 1) / kWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 0;       // O: 256 fp32 columns
-constexpr uint32_t kSCol = 256;     // S: two buffers of N fp32 columns, then P: two buffers of 16 columns
+constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
+constexpr uint32_t kSCol = 256;      // S: two buffers of N fp32 columns, then P: two buffers of 16 columns
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxStages = 8;
@@ -56,10 +73,14 @@ struct TcSmall {
   uint64_t kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t xin_full[2], xout_free[2];
+  uint64_t red_full[2];                  // half-row maxima of a tile written by all 8 softmax warps
+  uint64_t lsum_full;
   uint64_t o_full;
-  int32_t meta_n[kMaxStages];
-  int32_t rows[2][kMaxN];
-  int32_t rows_n[2];
+  float red[2][2][128];                  // [tile parity][warpgroup][head]
+  float lsum[2][128];                    // [warpgroup][head]
+  int32_t chunk_off[kMaxChunks];        // compacted-slot count of each 32-column chunk, then its offset
+  int32_t nswa;                          // valid slots in the SWA columns of the split
+  int32_t nvalid;                        // valid slots of the split
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -68,6 +89,7 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
+  static constexpr int kHalfN = kN / 2;                        // slots per softmax warpgroup
   static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
   static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
   static constexpr int kStages = 6;
@@ -75,6 +97,7 @@ struct Cfg {
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
   static constexpr int kK2 = kN / kKStep;                      // PV K steps
   static constexpr int kPCols = kN * kElem / 4;                // TMEM columns of one P buffer
+  static constexpr int kPColsHalf = kPCols / 2;                // written by one softmax warpgroup
   static constexpr uint32_t kPCol = kSCol + 2 * kN;
   static constexpr int kRegionQ = 128 * 128;                   // 128 rows x 128 B
   static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
@@ -88,9 +111,22 @@ struct Cfg {
   static constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
   static_assert(kStages <= kMaxStages, "barrier arrays");
+  static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
+  static_assert(kStages >= kProducerWarps,
+                "a producer warp waits on a stage only after the stage's previous release has completed");
   static_assert(kN <= kMaxN, "row lists");
+  static_assert(kPColsHalf == 8 || kPColsHalf == 16, "P half-buffer width");
   static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Kernel parameters: the shared decode parameters plus one TMA descriptor per
+// KV pool ([rows, 512] with the pool's row stride; box = 128 bytes x 1 row;
+// 128-byte swizzle), as required by tile::gather4.
+struct TcParams {
+  CUtensorMap tm_swa;
+  CUtensorMap tm_comp;
+  DecodeParams p;
 };
 
 struct Ctx {
@@ -103,7 +139,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
   for (uint32_t it = 0;; ++it) {
     bool done = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     if (done) return true;
-    if ((it & 63u) == 63u) {
+    if ((it & 3u) == 3u) {
       if (*reinterpret_cast<volatile int32_t*>(cx.abort_flag)) return false;
       uint64_t now = globaltimer();
       if (t0 == 0) {
@@ -123,10 +159,6 @@ __device__ __forceinline__ bool warp_wait(const Ctx& cx, uint32_t bar, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
 // K-major region whose 8-row groups are 1024 bytes apart.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int ch) {
@@ -144,11 +176,43 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// kH consecutive fp32 TMEM columns of this thread's lane (warp-collective).
+template <int kH>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[kH]) {
+  if constexpr (kH == 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  } else {
+    static_assert(kH == 16, "half tile width");
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  }
+}
+
+// kW consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+template <int kW>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&r)[kW]) {
+  if constexpr (kW == 16) {
+    tmem_st16(taddr, r);
+  } else {
+    static_assert(kW == 8, "P half-buffer width");
+    tmem_st8(taddr, r);
+  }
+}
+
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+decode_tc_kernel(const __grid_constant__ TcParams P) {
   using C = Cfg<kFp8>;
+  const DecodeParams& p = P.p;
   constexpr int kN = C::kN;
+  constexpr int kHN = C::kHalfN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
@@ -166,19 +230,41 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   const int unit = blockIdx.x >> 1;
   const int s = unit % S;
   const int t = unit / S;
-  const TokenInfo ti = token_info(p, t);
-  int c0, c1;
-  split_range(ti.n_lim, S, s, &c0, &c1);
+  const int H = p.H;
+  // Column range of this split, from the table width only (so that the index
+  // loads need not wait for any device value): [c0, c0 + ceil(W / S)).
+  const int per_split = (p.W + S - 1) / S;
+  const int c0 = min(p.W, s * per_split);
+  int c1 = min(p.W, c0 + per_split);
   if (c1 - c0 > kMaxCols) {           // the planner prevents this; never read past the staging buffer
     if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
     c1 = c0 + kMaxCols;
   }
-  const int ncols = c1 - c0;
-  const int H = p.H;
 
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
 
   // ---------------------------------------------------------------- set-up
+  // Q first: its copies need nothing but (t, rank)
+  {
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
+                              ((int64_t)t * p.q_stride_token + (int64_t)rank * kHalfDims) * C::kElem;
+    for (int c = tid; c < H * C::kChunks; c += kThreads) {
+      const int h = c / C::kChunks, cc = c % C::kChunks;
+      cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7),
+                  qb + (int64_t)h * kHeadDim * C::kElem + cc * 16);
+    }
+  }
+  // the split's index columns, in flight together with the token metadata loads
+  const int nchunks = (c1 - c0 + 31) / 32;
+  const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+  int32_t rv[kChunksPerWarp];
+#pragma unroll
+  for (int q = 0; q < kChunksPerWarp; ++q) {
+    const int col = c0 + (warp + q * kWarps) * 32 + lane;
+    rv[q] = (col < c1) ? __ldg(irow + col) : -1;
+  }
+  const TokenInfo ti = token_info(p, t);
+  c1 = min(c1, max(c0, ti.n_lim));    // active columns of the split
   {
     // zero the KV stages (rows past a tile's slot count then hold finite data)
     // and the Q rows of absent heads
@@ -192,25 +278,83 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
         for (int i = tid; i < (128 - H) * 8; i += kThreads) qz[i] = z;
       }
     }
-    const int32_t* irow = p.ind + (int64_t)t * p.ind_stride + c0;
-    for (int i = tid; i < ncols; i += kThreads) idx_s[i] = __ldg(irow + i);
     if (tid == 0) {
-      mbar_init(bar(sm.q_full), kProducerThreads);
+      mbar_init(bar(sm.q_full), kThreads);
       for (int i = 0; i < C::kStages; ++i) {
-        mbar_init(bar(sm.kv_full[i]), kProducerThreads + 1);
+        mbar_init(bar(sm.kv_full[i]), 1);
         mbar_init(bar(sm.kv_empty[i]), 1);
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), 4);
-        mbar_init(bar(sm.p_full[b]), 4);
+        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps);
+        mbar_init(bar(sm.p_full[b]), kSoftmaxWarps);
         mbar_init(bar(sm.p_empty[b]), 1);
         mbar_init(bar(sm.xin_full[b]), 1);
-        mbar_init(bar(sm.xout_free[b]), 4);
+        mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps);
+        mbar_init(bar(sm.red_full[b]), kSoftmaxWarps);
       }
+      mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
       mbar_init(bar(sm.o_full), 1);
       sm.abort_flag = 0;
+      sm.nswa = 0;
       fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    cp_async_arrive_noinc(bar(sm.q_full));   // completes once this thread's Q copies land
+    // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
+    // slots first, then valid compressed slots, each in column order
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int k = warp + q * kWarps;
+      if (k < nchunks) {
+        const int col = c0 + k * 32 + lane;
+        const int idx = rv[q];
+        rv[q] = -1;
+        if (col < c1) {
+          const bool swa = col < kSwaCols;
+          bool ok = idx != -1 && (!swa || col < ti.w_swa);
+          if (ok) {
+            const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+            if (idx < 0 || (int64_t)idx >= nrows) {
+              ok = false;
+              if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+            }
+          }
+          if (ok) rv[q] = idx;
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+        const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
+        if (lane == 0) {
+          sm.chunk_off[k] = __popc(ball);
+          if (ball_swa) atomicAdd(&sm.nswa, __popc(ball_swa));
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive scan of the chunk counts (at most kMaxChunks = 72 entries)
+      int carry = 0;
+      for (int base0 = 0; base0 < nchunks; base0 += 32) {
+        const int k = base0 + lane;
+        const int v = k < nchunks ? sm.chunk_off[k] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        if (k < nchunks) sm.chunk_off[k] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) sm.nvalid = carry;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int k = warp + q * kWarps;
+      if (k < nchunks) {
+        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+        if (rv[q] >= 0) idx_s[sm.chunk_off[k] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+      }
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
     fence_proxy_async_smem();
@@ -220,97 +364,41 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   }
   const uint32_t tmem = sm.tmem_base;
   const Ctx cx{&sm.abort_flag, p.err};
+  // tiles: runs of up to N compacted slots of one pool
+  const int nswa = sm.nswa, nvalid = sm.nvalid;
+  const int tswa = (nswa + kN - 1) / kN;
+  const int ntiles = tswa + (nvalid - nswa + kN - 1) / kN;
+  auto tile_start = [&](int j) { return j < tswa ? j * kN : nswa + (j - tswa) * kN; };
+  auto tile_n = [&](int j) { return min(kN, (j < tswa ? nswa : nvalid) - tile_start(j)); };
 
-  if (warp < kMmaWarp) {
+  if (warp < kProducerWarps) {
     // ============================================================ producer
-    const int ptid = tid;
-    {
-      const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
-                                ((int64_t)t * p.q_stride_token + (int64_t)rank * kHalfDims) * C::kElem;
-      for (int c = ptid; c < H * C::kChunks; c += kProducerThreads) {
-        const int h = c / C::kChunks, cc = c % C::kChunks;
-        cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7),
-                    qb + (int64_t)h * kHeadDim * C::kElem + cc * 16);
-      }
-      cp_async_arrive_noinc(bar(sm.q_full));
+    if (tid == 0) {
+      prefetch_tensormap(&P.tm_swa);
+      prefetch_tensormap(&P.tm_comp);
     }
-    // index compaction state (warp 0 only)
-    int seg = 0, cursor = 0;
-    for (int j = 0;; ++j) {
+    for (int j = warp; j < ntiles; j += kProducerWarps) {
       const int st = j % C::kStages;
-      wait_bar(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1, false);
-      if (warp == 0) {
-        // next tile: up to N valid slots of one pool, in column order
-        int cnt = 0, pool = 0;
-        while (cnt < kN && seg < 2) {
-          const int lo = seg == 0 ? c0 : max(c0, kSwaCols);
-          const int hi = seg == 0 ? min(c1, kSwaCols) : c1;
-          if (cursor < lo) cursor = lo;
-          if (cursor >= hi) {
-            ++seg;
-            if (cnt > 0) break;
-            continue;
-          }
-          const int col = cursor + lane;
-          int row = -1;
-          if (col < hi) {
-            const int idx = idx_s[col - c0];
-            bool ok = idx != -1 && (seg == 1 || col < ti.w_swa);
-            if (ok) {
-              const int64_t nrows = seg == 0 ? p.swa_rows : p.comp_rows;
-              if (idx < 0 || (int64_t)idx >= nrows) {
-                ok = false;
-                if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
-              }
-            }
-            if (ok) row = idx;
-          }
-          const unsigned ball = __ballot_sync(0xffffffffu, row >= 0);
-          const int nv = __popc(ball);
-          const int room = kN - cnt;
-          const int rk = __popc(ball & ((1u << lane) - 1u));
-          if (row >= 0 && rk < room) sm.rows[j & 1][cnt + rk] = row;
-          if (nv > 0) pool = seg;
-          if (nv <= room) {
-            cnt += nv;
-            cursor = min(cursor + 32, hi);
-          } else {
-            const unsigned last = __ballot_sync(0xffffffffu, row >= 0 && rk == room - 1);
-            cursor += __ffs(last);       // column after the last slot taken
-            cnt = kN;
-          }
-        }
-        const bool stop = cnt == 0 || *reinterpret_cast<volatile int32_t*>(&sm.abort_flag) != 0;
-        if (lane == 0) sm.rows_n[j & 1] = stop ? 0 : (cnt | (pool << 16));
-      }
-      named_barrier_sync(1, kProducerThreads);
-      const int packed = sm.rows_n[j & 1];
-      const int n = packed & 0xffff;
-      if (n == 0) {
-        cp_async_arrive_noinc(bar(sm.kv_full[st]));
-        if (ptid == 0) {
-          sm.meta_n[st] = 0;
-          mbar_arrive(bar(sm.kv_full[st]));
-        }
-        break;
-      }
-      const bool swa_pool = (packed >> 16) == 0;
-      const unsigned char* pool_base = reinterpret_cast<const unsigned char*>(swa_pool ? p.swa : p.comp);
-      const int64_t stride = swa_pool ? p.swa_stride : p.comp_stride;
+      if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
+      const int start = tile_start(j), n = tile_n(j);
+      const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
+      if (lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
+      __syncwarp();
+      const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
       const uint32_t stage = kv_addr + st * C::kStageBytes;
-      for (int c = ptid; c < n * C::kChunks; c += kProducerThreads) {
-        const int r = c / C::kChunks, cc = c % C::kChunks;
-        const int64_t row = sm.rows[j & 1][r];
-        cp_async_16(stage + (cc >> 3) * C::kRegionKV + sw128_offset(r, cc & 7),
-                    pool_base + (row * stride + (int64_t)rank * kHalfDims) * C::kElem + cc * 16);
-      }
-      cp_async_arrive_noinc(bar(sm.kv_full[st]));
-      if (ptid == 0) {
-        sm.meta_n[st] = n;
-        mbar_arrive(bar(sm.kv_full[st]));
+      const int32_t* rows = idx_s + start;
+      const int groups = (n4 / 4) * C::kRegions;
+      for (int gi = lane; gi < groups; gi += 32) {
+        const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
+        tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
+                    rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
+                    bar(sm.kv_full[st]));
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    // leave no TMA write in flight (normally the consumers have waited for all of them)
+    for (int j = warp; j < ntiles; j += kProducerWarps)
+      if (j >= ntiles - C::kStages) warp_wait(cx, bar(sm.kv_full[j % C::kStages]), (j / C::kStages) & 1);
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issue
     // Order: QK of tile k, then PV of tile k-2, so that QK runs two tiles ahead
@@ -338,11 +426,9 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
       return true;
     };
     if (ok) {
-      for (;; ++k) {
+      for (; k < ntiles; ++k) {
         const int st = k % C::kStages;
         if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) { ok = false; break; }
-        const int n = sm.meta_n[st];
-        if (n == 0) break;
         const int b = k & 1;
         if (!warp_wait(cx, bar(sm.s_empty[b]), ((k >> 1) & 1) ^ 1)) { ok = false; break; }
         fence_proxy_async_smem();
@@ -366,6 +452,7 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
     __syncwarp();
   } else {
     // ============================================================ softmax / epilogue
+    const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup: slots [g*N/2, g*N/2 + N/2) of a tile
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;
     const bool active = q4 * 32 < H;                   // warp-uniform
@@ -373,164 +460,193 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
     const uint32_t xbytes = (uint32_t)(H * kN * 4);    // bytes the peer pushes per tile
-    // peer addresses of exchange buffer / barrier b are these plus b * (stride)
     const uint32_t x_peer0 = map_to_rank(x_addr, peer);
     const uint32_t xin_full_peer0 = map_to_rank(bar(sm.xin_full[0]), peer);
     const uint32_t xout_free_peer0 = map_to_rank(bar(sm.xout_free[0]), peer);
     constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
+    const uint32_t s_col = kSCol + g * kHN;            // this warpgroup's S columns within a buffer
+    const int c4_0 = g * (kHN / 4);                    // its first 16-byte chunk in an exchange buffer
     if (leader) {
       mbar_arrive_expect_tx(bar(sm.xin_full[0]), xbytes);
       mbar_arrive_expect_tx(bar(sm.xin_full[1]), xbytes);
     }
     if (!active) {
-      // rows of absent heads: P = 0 in both buffers, so O and S stay 0 there
-      uint32_t zr[16];
+      // rows of absent heads: P = 0 in both buffers, so O stays 0 there
+      uint32_t zr[C::kPColsHalf];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) zr[i] = 0u;
-      tmem_st16(tl + C::kPCol, zr);
-      tmem_st16(tl + C::kPCol + C::kPCols, zr);
+      for (int i = 0; i < C::kPColsHalf; ++i) zr[i] = 0u;
+      tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + g * C::kPColsHalf, zr);
+      tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + C::kPCols + g * C::kPColsHalf, zr);
       tmem_wait_st();
     }
-    // load this CTA's partial S of tile jj into v (warp-collective)
-    auto load_s = [&](int jj, float (&v)[kN]) {
-      uint32_t r[32];
-#pragma unroll
-      for (int h32 = 0; h32 < kN / 32; ++h32) {
-        tmem_ld32(tl + kSCol + (jj & 1) * kN + h32 * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[h32 * 32 + i] = __uint_as_float(r[i]);
-      }
-    };
-    // send this CTA's partial S of tile jj to the peer (tile jj's S must be ready)
+    // send this CTA's partial S (my half of tile jj) to the peer
     auto push = [&](int jj) -> bool {
       const int b = jj & 1;
       if (!warp_wait(cx, bar(sm.s_full[b]), (jj >> 1) & 1)) return false;
       tc_fence_after();
       if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[b]), ((jj >> 1) & 1) ^ 1, true)) return false;
       if (active) {
-        float v[kN];
-        load_s(jj, v);
+        float v[kHN];
+        tmem_load_cols<kHN>(tl + s_col + b * kN, v);
+        const uint32_t dst = x_peer0 + b * C::kXBytes;
+        const uint32_t mb = xin_full_peer0 + b * kBarStride;
 #pragma unroll
-        for (int c4 = 0; c4 < kN / 4; ++c4)
-          st_async_v4(x_peer0 + b * C::kXBytes + (uint32_t)((c4 * 128 + h) * 16), v[4 * c4], v[4 * c4 + 1],
-                      v[4 * c4 + 2], v[4 * c4 + 3], xin_full_peer0 + b * kBarStride);
+        for (int q = 0; q < kHN / 4; ++q)
+          st_async_v4(dst + (uint32_t)(((c4_0 + q) * 128 + h) * 16), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                      v[4 * q + 3], mb);
       }
       return true;
     };
 
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = warp_wait(cx, bar(sm.kv_full[0]), 0);
-    int n_cur = ok ? sm.meta_n[0] : 0;
-    if (n_cur > 0) ok = push(0);
+    bool ok = true;
+    if (ntiles > 0) ok = push(0);
     int j = 0;
-    while (ok && n_cur > 0) {
-      // ---- consume tile j: S = S_0 + S_1
+    for (; ok && j < ntiles; ++j) {
+      const int n_cur = tile_n(j);
+      // ---- consume tile j: S = S_0 + S_1 on my half of its slots
       const int b = j & 1;
       if (!(ok = warp_wait(cx, bar(sm.xin_full[b]), (j >> 1) & 1, true))) break;
       tc_fence_after();
-      float sv[kN];
+      float sv[kHN];
+      float mloc = -INFINITY;                          // stays -inf when my half holds no slot
+      const int valid = n_cur - g * kHN;               // slots of my half that exist (may be <= 0)
       if (active) {
-        load_s(j, sv);
+        tmem_load_cols<kHN>(tl + s_col + b * kN, sv);
+        const uint32_t xb = x_addr + b * C::kXBytes;
 #pragma unroll
-        for (int c4 = 0; c4 < kN / 4; ++c4) {
-          const float4 v = ld_shared_v4(x_addr + b * C::kXBytes + (uint32_t)((c4 * 128 + h) * 16));
-          sv[4 * c4] += v.x;
-          sv[4 * c4 + 1] += v.y;
-          sv[4 * c4 + 2] += v.z;
-          sv[4 * c4 + 3] += v.w;
+        for (int q = 0; q < kHN / 4; ++q) {
+          const float4 v = ld_shared_v4(xb + (uint32_t)(((c4_0 + q) * 128 + h) * 16));
+          uint64_t a0 = f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(v.x, v.y));
+          uint64_t a1 = f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(v.z, v.w));
+          f2_unpack(a0, sv[4 * q], sv[4 * q + 1]);
+          f2_unpack(a1, sv[4 * q + 2], sv[4 * q + 3]);
         }
+        if (valid >= kHN) {
+          float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+          for (int i = 0; i < kHN; ++i) {
+            mx = fmaxf(mx, sv[i]);
+            mn = fminf(mn, sv[i]);
+          }
+          mloc = (c >= 0.f) ? mx * c : mn * c;         // max over my half of s * c
+        } else if (valid > 0) {
+          float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+          for (int i = 0; i < kHN; ++i) {
+            if (i < valid) {
+              mx = fmaxf(mx, sv[i]);
+              mn = fminf(mn, sv[i]);
+            }
+          }
+          mloc = (c >= 0.f) ? mx * c : mn * c;
+        }
+        sm.red[b][g][h] = mloc;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(sm.s_empty[b]));                    // S buffer b may be overwritten
-        mbar_arrive_cluster_relaxed(xout_free_peer0 + b * kBarStride);   // exchange buffer b read out
+        mbar_arrive(bar(sm.s_empty[b]));                                   // S buffer b may be overwritten
+        mbar_arrive_cluster_relaxed(xout_free_peer0 + b * kBarStride);      // exchange buffer b read out
+        mbar_arrive(bar(sm.red_full[b]));
       }
-      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[b]), xbytes);   // for tile j + 2
+      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[b]), xbytes);      // for tile j + 2
       // ---- look ahead: push tile j+1 so that the exchange overlaps this tile's softmax
-      const int st1 = (j + 1) % C::kStages;
-      if (!(ok = warp_wait(cx, bar(sm.kv_full[st1]), ((j + 1) / C::kStages) & 1))) break;
-      const int n_next = sm.meta_n[st1];
-      if (n_next > 0 && !(ok = push(j + 1))) break;
-      // ---- online softmax, base 2, lazy rescale
+      if (j + 1 < ntiles && !(ok = push(j + 1))) break;
+      // ---- tile maximum across the two warpgroups, online softmax in base 2
+      if (!(ok = warp_wait(cx, bar(sm.red_full[b]), (j >> 1) & 1))) break;
       bool rescale = false;
       float alpha = 1.f;
       if (active) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kN; ++i) {
-          sv[i] = (i < n_cur) ? sv[i] * c : -INFINITY;
-          mx = fmaxf(mx, sv[i]);
-        }
-        if (mx > m_run + kRescaleThreshold) {
+        const float mt = fmaxf(mloc, sm.red[b][g ^ 1][h]);
+        if (mt > m_run + kRescaleThreshold) {
           rescale = true;
-          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mx);
+          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mt);
           l_run *= alpha;
-          m_run = mx;
+          m_run = mt;
         }
-        float sum = 0.f;
+        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_run, -m_run);
+        uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < kN; ++i) {
-          sv[i] = fast_exp2(sv[i] - m_run);
-          sum += sv[i];
+        for (int i = 0; i < kHN; i += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), c2, nm2), x0, x1);
+          sv[i] = fast_exp2(x0);
+          sv[i + 1] = fast_exp2(x1);
         }
-        l_run += sum;
+        if (valid < kHN) {
+#pragma unroll
+          for (int i = 0; i < kHN; ++i)
+            if (i >= valid) sv[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kHN; i += 2) sum2 = f2_add(sum2, f2_pack(sv[i], sv[i + 1]));
+        float s0, s1;
+        f2_unpack(sum2, s0, s1);
+        l_run += s0 + s1;
       }
       if (!(ok = warp_wait(cx, bar(sm.p_empty[b]), ((j >> 1) & 1) ^ 1))) break;
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O must hold tile j-1's contribution before it is rescaled
+        // O must hold tile j-1's contribution before it is rescaled; each
+        // warpgroup rescales its half of the 256 O columns
         if (!(ok = warp_wait(cx, bar(sm.p_empty[(j - 1) & 1]), ((j - 1) >> 1) & 1))) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 32; ++cc) {
+        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+          const uint32_t col = kOCol + g * (kHalfDims / 2) + cc * 32;
           uint32_t r[32];
-          tmem_ld32(tl + kOCol + cc * 32, r);
+          tmem_ld32(tl + col, r);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tl + kOCol + cc * 32, r);
+          tmem_st32(tl + col, r);
         }
         tmem_wait_st();
       }
       if (active) {
-        uint32_t pr[16];
+        uint32_t pr[C::kPColsHalf];
         if constexpr (kFp8) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+          for (int i = 0; i < C::kPColsHalf; ++i)
+            pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+          for (int i = 0; i < C::kPColsHalf; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
         }
-        tmem_st16(tl + C::kPCol + b * C::kPCols, pr);
+        tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + b * C::kPCols + g * C::kPColsHalf, pr);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(sm.p_full[b]));
-      ++j;
-      n_cur = n_next;
     }
     const int ntiles = j;
+    // total row sum = both warpgroups' partial sums (both used the same maxima)
+    if (active) sm.lsum[g][h] = l_run;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(sm.lsum_full));
+    if (ok) ok = warp_wait(cx, bar(sm.lsum_full), 0);
     if (ok && ntiles > 0) {
       ok = warp_wait(cx, bar(sm.o_full), 0);
       tc_fence_after();
     }
     if (active) {
-      const bool have = ok && ntiles > 0 && l_run > 0.f;
-      const float lse = have ? m_run + fast_log2(l_run) : -INFINITY;
-      float f = have ? 1.f / l_run : 0.f;
+      const float l_tot = ok ? sm.lsum[0][h] + sm.lsum[1][h] : 0.f;
+      const bool have = ok && ntiles > 0 && l_tot > 0.f;
+      const float lse = have ? m_run + fast_log2(l_tot) : -INFINITY;
+      float f = have ? 1.f / l_tot : 0.f;
       if (S == 1) {
         f *= load_scale(p.bmm2, p.bmm2_dev);
         if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
       }
       const int64_t row_th = (int64_t)t * H + h;
 #pragma unroll 1
-      for (int cc = 0; cc < kHalfDims / 32; ++cc) {
+      for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+        const int col = g * (kHalfDims / 2) + cc * 32;
         float v[32];
-        if (ok && ntiles > 0) {
+        if (have) {
           uint32_t r[32];
-          tmem_ld32(tl + kOCol + cc * 32, r);
+          tmem_ld32(tl + kOCol + col, r);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
@@ -538,7 +654,7 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        const int d0 = (int)rank * kHalfDims + cc * 32;
+        const int d0 = (int)rank * kHalfDims + col;
         if (S == 1) {
           uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
 #pragma unroll
@@ -551,7 +667,7 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
           for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       }
-      if (rank == 0) {
+      if (rank == 0 && g == 0) {
         if (S == 1) {
           if (p.out_lse) p.out_lse[row_th] = lse;
         } else {
@@ -572,22 +688,62 @@ decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   cluster_sync();                          // the peer is done with this CTA's shared memory
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_fn(EncodeTiledFn* out) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  *out = fn;
+  return cudaSuccess;
+}
+
+// [rows, 512] pool view; box 128 bytes x 1 row; 128-byte swizzle.
+cudaError_t encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_stride, int dtype) {
+  EncodeTiledFn fn = nullptr;
+  cudaError_t e = encode_fn(&fn);
+  if (e != cudaSuccess) return e;
+  const int elem = dtype == SMLA_BF16 ? 2 : 1;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(row_stride * elem)};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype == SMLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int tc_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes; }
 int tc_threads() { return kThreads; }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+  TcParams P;
+  memset(&P, 0, sizeof(P));
+  P.p = p;
+  cudaError_t e = encode_pool_map(&P.tm_swa, p.swa, p.swa_rows, p.swa_stride, p.dtype);
+  if (e != cudaSuccess) return e;
+  e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype);
+  if (e != cudaSuccess) return e;
   const int smem = tc_smem_bytes(p.dtype);
-  cudaError_t e;
   if (p.dtype == SMLA_BF16) {
     e = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_tc_kernel<false><<<grid, kThreads, smem, stream>>>(p);
+    decode_tc_kernel<false><<<grid, kThreads, smem, stream>>>(P);
   } else {
     e = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_tc_kernel<true><<<grid, kThreads, smem, stream>>>(p);
+    decode_tc_kernel<true><<<grid, kThreads, smem, stream>>>(P);
   }
   return cudaGetLastError();
 }
