@@ -19,15 +19,18 @@
 //                       O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
 //                       P read from TMEM); one thread issues tcgen05.mma, QK two
 //                       tiles ahead of PV; accumulators live in TMEM
-//   softmax warps 5-12  two warpgroups, one per half of the tile's slots; one
-//                       thread per (head, half): read S_r from TMEM, push it to
-//                       the peer CTA with st.async (completing bytes on the
-//                       peer's mbarrier), add the peer's partial (S = S_0 + S_1,
-//                       identical in both CTAs), exchange the half-row maxima
-//                       between the warpgroups, online softmax in base 2 with
-//                       lazy rescaling of O, write P (BF16 or E4M3) into TMEM;
+//   softmax warps 5-12  two warpgroups taking whole tiles in turn (warpgroup
+//                       g takes tiles j with j % 2 == g), one thread per head:
+//                       read S_r from TMEM, push it to the peer CTA with
+//                       st.async (completing bytes on the peer's mbarrier), add
+//                       the peer's partial (S = S_0 + S_1, identical in both
+//                       CTAs), settle the running reference maximum m(j) from
+//                       m(j-1) (handed over by the other warpgroup through
+//                       shared memory), exponentials in base 2 with lazy
+//                       rescaling of O, write P (BF16 or E4M3) into TMEM;
 //                       finally normalise O and store it (BF16 output or fp32
-//                       split partial) plus the LSE.
+//                       split partial) plus the LSE.  One warpgroup's
+//                       exponentials overlap the other's loads and exchange.
 //
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
@@ -73,10 +76,11 @@ struct TcSmall {
   uint64_t kv_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t xin_full[2], xout_free[2];
-  uint64_t red_full[2];                  // half-row maxima of a tile written by all 8 softmax warps
+  uint64_t m_ready[2];                   // m_buf[g] written by warpgroup g's four warps
   uint64_t lsum_full;
   uint64_t o_full;
-  float red[2][2][128];                  // [tile parity][warpgroup][head]
+  float m_end[2][128];                   // final reference maximum per [warpgroup][head]
+  float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
   float lsum[2][128];                    // [warpgroup][head]
   int32_t chunk_off[kMaxChunks];        // compacted-slot count of each 32-column chunk, then its offset
   int32_t nswa;                          // valid slots in the SWA columns of the split
@@ -89,7 +93,6 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
-  static constexpr int kHalfN = kN / 2;                        // slots per softmax warpgroup
   static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
   static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
   static constexpr int kStages = 6;
@@ -97,7 +100,6 @@ struct Cfg {
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
   static constexpr int kK2 = kN / kKStep;                      // PV K steps
   static constexpr int kPCols = kN * kElem / 4;                // TMEM columns of one P buffer
-  static constexpr int kPColsHalf = kPCols / 2;                // written by one softmax warpgroup
   static constexpr uint32_t kPCol = kSCol + 2 * kN;
   static constexpr int kRegionQ = 128 * 128;                   // 128 rows x 128 B
   static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
@@ -115,8 +117,13 @@ struct Cfg {
   static_assert(kStages >= kProducerWarps,
                 "a producer warp waits on a stage only after the stage's previous release has completed");
   static_assert(kN <= kMaxN, "row lists");
-  static_assert(kPColsHalf == 8 || kPColsHalf == 16, "P half-buffer width");
-  static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
+  static_assert(kPCols == 16, "P buffer width");
+  // S + X of all but the last 32-column group of a tile, per warpgroup, while the
+  // tile maximum is being settled (only the last group stays in registers)
+  static constexpr uint32_t kScratchCol = kPCol + 2 * kPCols;
+  static constexpr int kGroups = kN / 32;
+  static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
+  static_assert(kScratchCol + 2 * (kGroups - 1) * 32 <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -159,6 +166,11 @@ __device__ __forceinline__ bool warp_wait(const Ctx& cx, uint32_t bar, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Makes `x` opaque to the optimiser at this point, so that addresses derived
+// from it inside a loop are formed there rather than kept in registers across
+// the loop.
+__device__ __forceinline__ void opaque(uint32_t& x) { asm volatile("" : "+r"(x)); }
+
 // Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
 // K-major region whose 8-row groups are 1024 bytes apart.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int ch) {
@@ -195,24 +207,12 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[kH]) {
   }
 }
 
-// kW consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
-template <int kW>
-__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&r)[kW]) {
-  if constexpr (kW == 16) {
-    tmem_st16(taddr, r);
-  } else {
-    static_assert(kW == 8, "P half-buffer width");
-    tmem_st8(taddr, r);
-  }
-}
-
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
   using C = Cfg<kFp8>;
   const DecodeParams& p = P.p;
   constexpr int kN = C::kN;
-  constexpr int kHN = C::kHalfN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
@@ -286,12 +286,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps);
-        mbar_init(bar(sm.p_full[b]), kSoftmaxWarps);
+        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+        mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
         mbar_init(bar(sm.p_empty[b]), 1);
         mbar_init(bar(sm.xin_full[b]), 1);
-        mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps);
-        mbar_init(bar(sm.red_full[b]), kSoftmaxWarps);
+        mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps / 2);
+        mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
       }
       mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
       mbar_init(bar(sm.o_full), 1);
@@ -452,177 +452,197 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     __syncwarp();
   } else {
     // ============================================================ softmax / epilogue
-    const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup: slots [g*N/2, g*N/2 + N/2) of a tile
+    // Two warpgroups take turns: warpgroup g handles tiles j with j % 2 == g
+    // (all N slots; S, P and exchange buffer g).  The only hand-off between
+    // consecutive tiles is the running reference maximum m(j), published by
+    // the warpgroup of tile j as soon as it is known, so one warpgroup's
+    // exponentials overlap the other's loads and exchange.
+    const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;
     const bool active = q4 * 32 < H;                   // warp-uniform
-    const bool leader = warp == kSoftmaxWarp0 && lane == 0;
+    const bool leader = (warp - kSoftmaxWarp0) % 4 == 0 && lane == 0;   // one thread per warpgroup
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
     const uint32_t xbytes = (uint32_t)(H * kN * 4);    // bytes the peer pushes per tile
-    const uint32_t x_peer0 = map_to_rank(x_addr, peer);
-    const uint32_t xin_full_peer0 = map_to_rank(bar(sm.xin_full[0]), peer);
-    const uint32_t xout_free_peer0 = map_to_rank(bar(sm.xout_free[0]), peer);
     constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
-    const uint32_t s_col = kSCol + g * kHN;            // this warpgroup's S columns within a buffer
-    const int c4_0 = g * (kHN / 4);                    // its first 16-byte chunk in an exchange buffer
-    if (leader) {
-      mbar_arrive_expect_tx(bar(sm.xin_full[0]), xbytes);
-      mbar_arrive_expect_tx(bar(sm.xin_full[1]), xbytes);
-    }
+    const uint32_t x_mine = x_addr + g * C::kXBytes;
+    const uint32_t x_peer = map_to_rank(x_mine, peer);
+    const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer) + g * kBarStride;
+    const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[0]), peer) + g * kBarStride;
+    const uint32_t s_cols = kSCol + g * kN;            // S buffer g
+    const uint32_t p_cols = C::kPCol + g * C::kPCols;  // P buffer g
+    if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
     if (!active) {
-      // rows of absent heads: P = 0 in both buffers, so O stays 0 there
-      uint32_t zr[C::kPColsHalf];
+      // rows of absent heads: P = 0, so O stays 0 there
+      uint32_t zr[C::kPCols];
 #pragma unroll
-      for (int i = 0; i < C::kPColsHalf; ++i) zr[i] = 0u;
-      tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + g * C::kPColsHalf, zr);
-      tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + C::kPCols + g * C::kPColsHalf, zr);
+      for (int i = 0; i < C::kPCols; ++i) zr[i] = 0u;
+      tmem_st16(tl + p_cols, zr);
       tmem_wait_st();
     }
-    // send this CTA's partial S (my half of tile jj) to the peer
+    // send this CTA's partial S of tile jj (a tile of my warpgroup) to the peer
     auto push = [&](int jj) -> bool {
-      const int b = jj & 1;
-      if (!warp_wait(cx, bar(sm.s_full[b]), (jj >> 1) & 1)) return false;
+      if (!warp_wait(cx, bar(sm.s_full[g]), (jj >> 1) & 1)) return false;
       tc_fence_after();
-      if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[b]), ((jj >> 1) & 1) ^ 1, true)) return false;
+      if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[g]), ((jj >> 1) & 1) ^ 1, true)) return false;
       if (active) {
-        float v[kHN];
-        tmem_load_cols<kHN>(tl + s_col + b * kN, v);
-        const uint32_t dst = x_peer0 + b * C::kXBytes;
-        const uint32_t mb = xin_full_peer0 + b * kBarStride;
+        uint32_t xb = x_peer + (uint32_t)(h * 16);
+        opaque(xb);   // keeps the per-chunk addresses below from being hoisted into registers
 #pragma unroll
-        for (int q = 0; q < kHN / 4; ++q)
-          st_async_v4(dst + (uint32_t)(((c4_0 + q) * 128 + h) * 16), v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                      v[4 * q + 3], mb);
+        for (int hb = 0; hb < kN / 32; ++hb) {
+          float v[32];
+          tmem_load_cols<32>(tl + s_cols + hb * 32, v);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_async_v4(xb + (uint32_t)((hb * 8 + q) * 128 * 16), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3],
+                        xin_full_peer);
+        }
       }
       return true;
     };
 
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_last = -INFINITY, l_run = 0.f;            // reference and row sum of my warpgroup's tiles
     bool ok = true;
-    if (ntiles > 0) ok = push(0);
-    int j = 0;
-    for (; ok && j < ntiles; ++j) {
+    if (g < ntiles) ok = push(g);
+    int j = g;
+    for (; ok && j < ntiles; j += 2) {
       const int n_cur = tile_n(j);
-      // ---- consume tile j: S = S_0 + S_1 on my half of its slots
-      const int b = j & 1;
-      if (!(ok = warp_wait(cx, bar(sm.xin_full[b]), (j >> 1) & 1, true))) break;
+      // ---- S = S_0 + S_1 and the tile maximum of s * c
+      if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
       tc_fence_after();
-      float sv[kHN];
-      float mloc = -INFINITY;                          // stays -inf when my half holds no slot
-      const int valid = n_cur - g * kHN;               // slots of my half that exist (may be <= 0)
+      // the last 32-column group stays in sv; earlier groups go to this warpgroup's scratch columns
+      constexpr int kG = C::kGroups;
+      const uint32_t scratch = tl + C::kScratchCol + g * (kG - 1) * 32;
+      float sv[32];
+      float mt = -INFINITY;
       if (active) {
-        tmem_load_cols<kHN>(tl + s_col + b * kN, sv);
-        const uint32_t xb = x_addr + b * C::kXBytes;
+        float mx = -INFINITY, mn = INFINITY;
+        uint32_t xb = x_mine + (uint32_t)(h * 16);
+        opaque(xb);
 #pragma unroll
-        for (int q = 0; q < kHN / 4; ++q) {
-          const float4 v = ld_shared_v4(xb + (uint32_t)(((c4_0 + q) * 128 + h) * 16));
-          uint64_t a0 = f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(v.x, v.y));
-          uint64_t a1 = f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(v.z, v.w));
-          f2_unpack(a0, sv[4 * q], sv[4 * q + 1]);
-          f2_unpack(a1, sv[4 * q + 2], sv[4 * q + 3]);
-        }
-        if (valid >= kHN) {
-          float mx = -INFINITY, mn = INFINITY;
+        for (int hb = 0; hb < kG; ++hb) {
+          tmem_load_cols<32>(tl + s_cols + hb * 32, sv);
 #pragma unroll
-          for (int i = 0; i < kHN; ++i) {
-            mx = fmaxf(mx, sv[i]);
-            mn = fminf(mn, sv[i]);
+          for (int q = 0; q < 8; ++q) {
+            const float4 x = ld_shared_v4(xb + (uint32_t)((hb * 8 + q) * 128 * 16));
+            f2_unpack(f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(x.x, x.y)), sv[4 * q], sv[4 * q + 1]);
+            f2_unpack(f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(x.z, x.w)), sv[4 * q + 2], sv[4 * q + 3]);
           }
-          mloc = (c >= 0.f) ? mx * c : mn * c;         // max over my half of s * c
-        } else if (valid > 0) {
-          float mx = -INFINITY, mn = INFINITY;
+          if (n_cur >= (hb + 1) * 32) {
 #pragma unroll
-          for (int i = 0; i < kHN; ++i) {
-            if (i < valid) {
+            for (int i = 0; i < 32; ++i) {
               mx = fmaxf(mx, sv[i]);
               mn = fminf(mn, sv[i]);
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (hb * 32 + i < n_cur) {
+                mx = fmaxf(mx, sv[i]);
+                mn = fminf(mn, sv[i]);
+              }
+            }
           }
-          mloc = (c >= 0.f) ? mx * c : mn * c;
+          if (hb + 1 < kG) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sv[i]);
+            tmem_st32(scratch + hb * 32, r);
+          }
         }
-        sm.red[b][g][h] = mloc;
+        mt = (c >= 0.f) ? mx * c : mn * c;
       }
+      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(sm.s_empty[b]));                                   // S buffer b may be overwritten
-        mbar_arrive_cluster_relaxed(xout_free_peer0 + b * kBarStride);      // exchange buffer b read out
-        mbar_arrive(bar(sm.red_full[b]));
+        mbar_arrive(bar(sm.s_empty[g]));                          // S buffer g may be overwritten
+        mbar_arrive_cluster_relaxed(xout_free_peer);               // exchange buffer g read out
       }
-      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[b]), xbytes);      // for tile j + 2
-      // ---- look ahead: push tile j+1 so that the exchange overlaps this tile's softmax
-      if (j + 1 < ntiles && !(ok = push(j + 1))) break;
-      // ---- tile maximum across the two warpgroups, online softmax in base 2
-      if (!(ok = warp_wait(cx, bar(sm.red_full[b]), (j >> 1) & 1))) break;
-      bool rescale = false;
-      float alpha = 1.f;
+      // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
+      float m_prev = -INFINITY;
+      if (j > 0) {
+        if (!(ok = warp_wait(cx, bar(sm.m_ready[g ^ 1]), ((j - 1) >> 1) & 1))) break;
+        m_prev = sm.m_buf[g ^ 1][h];
+      }
+      const float m_cur = (mt > m_prev + kRescaleThreshold) ? mt : m_prev;
+      sm.m_buf[g][h] = m_cur;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
+      // ---- P = 2^(s c - m(j)) group by group (last group first, from registers),
+      // each group written to P buffer g as soon as it is packed; this
+      // warpgroup's row sum, rescaled to m(j)
+      if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
+      tc_fence_after();
+      constexpr int kPG = C::kPCols / kG;               // packed P columns per 32-column group
       if (active) {
-        const float mt = fmaxf(mloc, sm.red[b][g ^ 1][h]);
-        if (mt > m_run + kRescaleThreshold) {
-          rescale = true;
-          alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - mt);
-          l_run *= alpha;
-          m_run = mt;
-        }
-        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_run, -m_run);
+        l_run *= (m_last == -INFINITY) ? 0.f : fast_exp2(m_last - m_cur);
+        m_last = m_cur;
+        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_cur, -m_cur);
         uint64_t sum2 = f2_pack(0.f, 0.f);
+        if (kG > 1) tmem_wait_st();
 #pragma unroll
-        for (int i = 0; i < kHN; i += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), c2, nm2), x0, x1);
-          sv[i] = fast_exp2(x0);
-          sv[i + 1] = fast_exp2(x1);
+        for (int k = 0; k < kG; ++k) {
+          const int hb = kG - 1 - k;
+          if (hb < kG - 1) tmem_load_cols<32>(scratch + hb * 32, sv);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), c2, nm2), x0, x1);
+            sv[i] = fast_exp2(x0);
+            sv[i + 1] = fast_exp2(x1);
+          }
+          if (n_cur < (hb + 1) * 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (hb * 32 + i >= n_cur) sv[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) sum2 = f2_add(sum2, f2_pack(sv[i], sv[i + 1]));
+          uint32_t pr[kPG];
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int i = 0; i < kPG; ++i) pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+            tmem_st8(tl + p_cols + hb * kPG, pr);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kPG; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+            tmem_st16(tl + p_cols + hb * kPG, pr);
+          }
         }
-        if (valid < kHN) {
-#pragma unroll
-          for (int i = 0; i < kHN; ++i)
-            if (i >= valid) sv[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < kHN; i += 2) sum2 = f2_add(sum2, f2_pack(sv[i], sv[i + 1]));
         float s0, s1;
         f2_unpack(sum2, s0, s1);
         l_run += s0 + s1;
       }
-      if (!(ok = warp_wait(cx, bar(sm.p_empty[b]), ((j >> 1) & 1) ^ 1))) break;
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O must hold tile j-1's contribution before it is rescaled; each
-        // warpgroup rescales its half of the 256 O columns
-        if (!(ok = warp_wait(cx, bar(sm.p_empty[(j - 1) & 1]), ((j - 1) >> 1) & 1))) break;
+      // ---- O rescale when the reference moved (O holds tiles < j at m(j-1))
+      const bool rescale = active && j > 0 && m_cur != m_prev;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!(ok = warp_wait(cx, bar(sm.p_empty[g ^ 1]), ((j - 1) >> 1) & 1))) break;
         tc_fence_after();
+        const float alpha = rescale ? fast_exp2(m_prev - m_cur) : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
-          const uint32_t col = kOCol + g * (kHalfDims / 2) + cc * 32;
-          uint32_t r[32];
-          tmem_ld32(tl + col, r);
+        for (int cc = 0; cc < kHalfDims / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(tl + kOCol + cc * 16, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tl + col, r);
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st16(tl + kOCol + cc * 16, r);
         }
-        tmem_wait_st();
       }
-      if (active) {
-        uint32_t pr[C::kPColsHalf];
-        if constexpr (kFp8) {
-#pragma unroll
-          for (int i = 0; i < C::kPColsHalf; ++i)
-            pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < C::kPColsHalf; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-        }
-        tmem_store_cols<C::kPColsHalf>(tl + C::kPCol + b * C::kPCols + g * C::kPColsHalf, pr);
-        tmem_wait_st();
-      }
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.p_full[b]));
+      if (lane == 0) mbar_arrive(bar(sm.p_full[g]));
+      // ---- look ahead: my next tile's partial S to the peer
+      if (j + 2 < ntiles && !(ok = push(j + 2))) break;
     }
-    const int ntiles = j;
-    // total row sum = both warpgroups' partial sums (both used the same maxima)
-    if (active) sm.lsum[g][h] = l_run;
+    // total row sum: both warpgroups' sums brought to the final reference
+    if (active) {
+      sm.lsum[g][h] = l_run;
+      sm.m_end[g][h] = m_last;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(sm.lsum_full));
     if (ok) ok = warp_wait(cx, bar(sm.lsum_full), 0);
@@ -631,9 +651,17 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       tc_fence_after();
     }
     if (active) {
-      const float l_tot = ok ? sm.lsum[0][h] + sm.lsum[1][h] : 0.f;
+      float l_tot = 0.f, m_fin = -INFINITY;
+      if (ok) {
+        const float ma = sm.m_end[0][h], mb = sm.m_end[1][h];
+        m_fin = fmaxf(ma, mb);
+        if (m_fin != -INFINITY) {
+          if (ma != -INFINITY) l_tot += sm.lsum[0][h] * fast_exp2(ma - m_fin);
+          if (mb != -INFINITY) l_tot += sm.lsum[1][h] * fast_exp2(mb - m_fin);
+        }
+      }
       const bool have = ok && ntiles > 0 && l_tot > 0.f;
-      const float lse = have ? m_run + fast_log2(l_tot) : -INFINITY;
+      const float lse = have ? m_fin + fast_log2(l_tot) : -INFINITY;
       float f = have ? 1.f / l_tot : 0.f;
       if (S == 1) {
         f *= load_scale(p.bmm2, p.bmm2_dev);
