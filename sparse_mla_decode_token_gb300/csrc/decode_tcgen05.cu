@@ -54,9 +54,10 @@ using namespace ptx;
 
 constexpr int kMaxN = 64;            // largest tile (slots per tile)
 constexpr int kHalfDims = 256;       // output dims per CTA
-constexpr int kProducerWarps = 4;    // TMA gathers: warp w issues tiles w, w + 4, ...
-constexpr int kMmaWarp = kProducerWarps;
-constexpr int kSoftmaxWarp0 = kMmaWarp + 1;
+constexpr int kProducerWarps = 6;    // TMA gathers: every producer warp issues a share of every tile
+constexpr int kMmaWarp = kProducerWarps;        // QK issue; allocates and frees TMEM
+constexpr int kPvWarp = kMmaWarp + 1;           // PV issue
+constexpr int kSoftmaxWarp0 = kPvWarp + 1;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
 constexpr int kWarps = kThreads / 32;
@@ -65,7 +66,8 @@ constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of
 constexpr int kChunksPerWarp = (kMaxChunks + kWarps - 1) / kWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
-constexpr uint32_t kSCol = 256;      // S: two buffers of N fp32 columns, then P: two buffers of 16 columns
+constexpr uint32_t kSCol = 256;      // S: three buffers of N fp32 columns, then P: two buffers of 16 columns
+constexpr int kSBufs = 3;
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxStages = 8;
@@ -74,11 +76,12 @@ struct TcSmall {
   uint64_t q_full;
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
+  uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[2], p_empty[2];
   uint64_t xin_full[2], xout_free[2];
   uint64_t m_ready[2];                   // m_buf[g] written by warpgroup g's four warps
   uint64_t lsum_full;
-  uint64_t o_full;
+  uint64_t o_full;                       // every PV done (committed by the PV warp)
+  uint64_t qk_done;                      // every QK done (committed by the QK warp)
   float m_end[2][128];                   // final reference maximum per [warpgroup][head]
   float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
   float lsum[2][128];                    // [warpgroup][head]
@@ -100,7 +103,7 @@ struct Cfg {
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
   static constexpr int kK2 = kN / kKStep;                      // PV K steps
   static constexpr int kPCols = kN * kElem / 4;                // TMEM columns of one P buffer
-  static constexpr uint32_t kPCol = kSCol + 2 * kN;
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kN;
   static constexpr int kRegionQ = 128 * 128;                   // 128 rows x 128 B
   static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
   static constexpr int kQBytes = kRegions * kRegionQ;
@@ -114,16 +117,10 @@ struct Cfg {
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
   static_assert(kStages <= kMaxStages, "barrier arrays");
   static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
-  static_assert(kStages >= kProducerWarps,
-                "a producer warp waits on a stage only after the stage's previous release has completed");
   static_assert(kN <= kMaxN, "row lists");
   static_assert(kPCols == 16, "P buffer width");
-  // S + X of all but the last 32-column group of a tile, per warpgroup, while the
-  // tile maximum is being settled (only the last group stays in registers)
-  static constexpr uint32_t kScratchCol = kPCol + 2 * kPCols;
-  static constexpr int kGroups = kN / 32;
   static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
-  static_assert(kScratchCol + 2 * (kGroups - 1) * 32 <= kTmemCols, "tensor memory budget");
+  static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -160,16 +157,19 @@ __device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t p
   }
 }
 
+// Wait for a barrier that completes once already-issued asynchronous work is
+// done; bounded by the same timeout but not cut short by the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
 // All lanes of the warp wait; the result is warp-uniform.
 __device__ __forceinline__ bool warp_wait(const Ctx& cx, uint32_t bar, uint32_t parity, bool cluster_scope = false) {
   bool ok = wait_bar(cx, bar, parity, cluster_scope);
   return __all_sync(0xffffffffu, ok);
 }
-
-// Makes `x` opaque to the optimiser at this point, so that addresses derived
-// from it inside a loop are formed there rather than kept in registers across
-// the loop.
-__device__ __forceinline__ void opaque(uint32_t& x) { asm volatile("" : "+r"(x)); }
 
 // Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
 // K-major region whose 8-row groups are 1024 bytes apart.
@@ -180,31 +180,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
-
-// kH consecutive fp32 TMEM columns of this thread's lane (warp-collective).
-template <int kH>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[kH]) {
-  if constexpr (kH == 32) {
-    uint32_t r[32];
-    tmem_ld32(taddr, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-  } else {
-    static_assert(kH == 16, "half tile width");
-    uint32_t r[16];
-    tmem_ld16(taddr, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-  }
 }
 
 template <bool kFp8>
@@ -285,8 +260,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         mbar_init(bar(sm.kv_empty[i]), 1);
       }
       for (int b = 0; b < 2; ++b) {
-        mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+
         mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
         mbar_init(bar(sm.p_empty[b]), 1);
         mbar_init(bar(sm.xin_full[b]), 1);
@@ -294,7 +268,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
       }
       mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
+      for (int b = 0; b < kSBufs; ++b) {
+        mbar_init(bar(sm.s_full[b]), 1);
+        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+      }
       mbar_init(bar(sm.o_full), 1);
+      mbar_init(bar(sm.qk_done), 1);
       sm.abort_flag = 0;
       sm.nswa = 0;
       fence_mbar_init_cluster();
@@ -373,43 +352,82 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 
   if (warp < kProducerWarps) {
     // ============================================================ producer
+    // A warp's TMA requests are served one after another (about 50 ns per
+    // gather4), so the tile's requests are spread over all producer warps.
+    // While tile j is gathered, the rows of tile j + kStages (the next user of
+    // the same stage) are prefetched into L2, so that its gather meets L2
+    // rather than HBM latency.
     if (tid == 0) {
       prefetch_tensormap(&P.tm_swa);
       prefetch_tensormap(&P.tm_comp);
     }
-    for (int j = warp; j < ntiles; j += kProducerWarps) {
+    const int64_t half_off = (int64_t)rank * kHalfDims * C::kElem;   // this CTA's half of a row, in bytes
+    auto prefetch_tile = [&](int jt) {
+      const int start = tile_start(jt), n = tile_n(jt);
+      const bool swa = jt < tswa;
+      const unsigned char* pool = static_cast<const unsigned char*>(swa ? p.swa : p.comp) + half_off;
+      const int64_t row_bytes = (swa ? p.swa_stride : p.comp_stride) * C::kElem;
+      for (int li = warp * 32 + lane; li < n * C::kRegions; li += kProducerWarps * 32) {
+        const int r = li / C::kRegions, kb = li % C::kRegions;
+        prefetch_l2(pool + (int64_t)idx_s[start + r] * row_bytes + kb * 128);
+      }
+    };
+    for (int j = 0; j < ntiles; ++j) {
       const int st = j % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
       const int start = tile_start(j), n = tile_n(j);
       const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
-      if (lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
-      __syncwarp();
+      if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
       const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
       const uint32_t stage = kv_addr + st * C::kStageBytes;
       const int32_t* rows = idx_s + start;
       const int groups = (n4 / 4) * C::kRegions;
-      for (int gi = lane; gi < groups; gi += 32) {
+      for (int gi = warp + kProducerWarps * lane; gi < groups; gi += kProducerWarps * 32) {
         const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
         tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
                     rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
                     bar(sm.kv_full[st]));
       }
+      if (j + C::kStages < ntiles) prefetch_tile(j + C::kStages);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    // leave no TMA write in flight (normally the consumers have waited for all of them)
-    for (int j = warp; j < ntiles; j += kProducerWarps)
-      if (j >= ntiles - C::kStages) warp_wait(cx, bar(sm.kv_full[j % C::kStages]), (j / C::kStages) & 1);
+    // leave no TMA write of this warp in flight (normally the consumers have waited for all of them)
+    for (int j = max(0, ntiles - C::kStages); j < ntiles; ++j)
+      warp_wait(cx, bar(sm.kv_full[j % C::kStages]), (j / C::kStages) & 1);
   } else if (warp == kMmaWarp) {
-    // ============================================================ MMA issue
-    // Order: QK of tile k, then PV of tile k-2, so that QK runs two tiles ahead
-    // of the softmax and PV never waits behind a QK.
+    // ============================================================ QK issue
+    // QK and PV are issued by different warps so that a QK never waits behind
+    // a PV (which waits for the softmax): the QK of tile k depends only on its
+    // data and a free S buffer.
     constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
-    constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
     bool ok = warp_wait(cx, bar(sm.q_full), 0);
-    int k = 0;
-    auto issue_pv = [&](int jj) -> bool {
+    for (int k = 0; ok && k < ntiles; ++k) {
+      const int st = k % C::kStages;
+      if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) break;
+      const int b = k % kSBufs;
+      if (!warp_wait(cx, bar(sm.s_empty[b]), ((k / kSBufs) & 1) ^ 1)) break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t stage = kv_addr + st * C::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kK1; ++kk) {
+          const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
+          const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
+          mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(sm.s_full[b]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(bar(sm.qk_done));   // completes once every QK issued above is done
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ============================================================ PV issue
+    constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
+    for (int jj = 0; jj < ntiles; ++jj) {
       const int b = jj & 1, st = jj % C::kStages;
-      if (!warp_wait(cx, bar(sm.p_full[b]), (jj >> 1) & 1)) return false;
+      if (!warp_wait(cx, bar(sm.p_full[b]), (jj >> 1) & 1)) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t stage = kv_addr + st * C::kStageBytes;
@@ -423,32 +441,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         mma_commit(bar(sm.kv_empty[st]));
       }
       __syncwarp();
-      return true;
-    };
-    if (ok) {
-      for (; k < ntiles; ++k) {
-        const int st = k % C::kStages;
-        if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) { ok = false; break; }
-        const int b = k & 1;
-        if (!warp_wait(cx, bar(sm.s_empty[b]), ((k >> 1) & 1) ^ 1)) { ok = false; break; }
-        fence_proxy_async_smem();
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t stage = kv_addr + st * C::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < C::kK1; ++kk) {
-            const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
-            const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
-            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(sm.s_full[b]));
-        }
-        __syncwarp();
-        if (k >= 2 && !issue_pv(k - 2)) { ok = false; break; }
-      }
-      for (int jj = max(0, k - 2); ok && jj < k; ++jj) ok = issue_pv(jj);
     }
-    if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every MMA issued above is done
+    if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every PV issued above is done
     __syncwarp();
   } else {
     // ============================================================ softmax / epilogue
@@ -470,7 +464,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     const uint32_t x_peer = map_to_rank(x_mine, peer);
     const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer) + g * kBarStride;
     const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[0]), peer) + g * kBarStride;
-    const uint32_t s_cols = kSCol + g * kN;            // S buffer g
     const uint32_t p_cols = C::kPCol + g * C::kPCols;  // P buffer g
     if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
     if (!active) {
@@ -483,19 +476,21 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     }
     // send this CTA's partial S of tile jj (a tile of my warpgroup) to the peer
     auto push = [&](int jj) -> bool {
-      if (!warp_wait(cx, bar(sm.s_full[g]), (jj >> 1) & 1)) return false;
+      const int sb = jj % kSBufs;
+      if (!warp_wait(cx, bar(sm.s_full[sb]), (jj / kSBufs) & 1)) return false;
       tc_fence_after();
       if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[g]), ((jj >> 1) & 1) ^ 1, true)) return false;
       if (active) {
-        uint32_t xb = x_peer + (uint32_t)(h * 16);
-        opaque(xb);   // keeps the per-chunk addresses below from being hoisted into registers
+        const uint32_t xb = x_peer + (uint32_t)(h * 16);
 #pragma unroll
-        for (int hb = 0; hb < kN / 32; ++hb) {
-          float v[32];
-          tmem_load_cols<32>(tl + s_cols + hb * 32, v);
+        for (int hb = 0; hb < kN / 16; ++hb) {
+          uint32_t v[16];
+          tmem_ld16(tl + kSCol + sb * kN + hb * 16, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_async_v4(xb + (uint32_t)((hb * 8 + q) * 128 * 16), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3],
+          for (int q = 0; q < 4; ++q)
+            st_async_v4(xb + (uint32_t)((hb * 4 + q) * 128 * 16), __uint_as_float(v[4 * q]),
+                        __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]),
                         xin_full_peer);
         }
       }
@@ -506,58 +501,48 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     bool ok = true;
     if (g < ntiles) ok = push(g);
     int j = g;
+    const uint64_t c2 = f2_pack(c, c);
     for (; ok && j < ntiles; j += 2) {
       const int n_cur = tile_n(j);
-      // ---- S = S_0 + S_1 and the tile maximum of s * c
+      const int sb = j % kSBufs;
       if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
       tc_fence_after();
-      // the last 32-column group stays in sv; earlier groups go to this warpgroup's scratch columns
-      constexpr int kG = C::kGroups;
-      const uint32_t scratch = tl + C::kScratchCol + g * (kG - 1) * 32;
-      float sv[32];
+      float sv[kN];
       float mt = -INFINITY;
       if (active) {
-        float mx = -INFINITY, mn = INFINITY;
-        uint32_t xb = x_mine + (uint32_t)(h * 16);
-        opaque(xb);
 #pragma unroll
-        for (int hb = 0; hb < kG; ++hb) {
-          tmem_load_cols<32>(tl + s_cols + hb * 32, sv);
+        for (int hb = 0; hb < kN / 32; ++hb) {
+          uint32_t r[32];
+          tmem_ld32(tl + kSCol + sb * kN + hb * 32, r);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 x = ld_shared_v4(xb + (uint32_t)((hb * 8 + q) * 128 * 16));
-            f2_unpack(f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(x.x, x.y)), sv[4 * q], sv[4 * q + 1]);
-            f2_unpack(f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(x.z, x.w)), sv[4 * q + 2], sv[4 * q + 3]);
-          }
-          if (n_cur >= (hb + 1) * 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              mx = fmaxf(mx, sv[i]);
-              mn = fminf(mn, sv[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (hb * 32 + i < n_cur) {
-                mx = fmaxf(mx, sv[i]);
-                mn = fminf(mn, sv[i]);
-              }
-            }
-          }
-          if (hb + 1 < kG) {
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sv[i]);
-            tmem_st32(scratch + hb * 32, r);
-          }
+          for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
         }
-        mt = (c >= 0.f) ? mx * c : mn * c;
+        tmem_wait_ld();
+        const float4* xp = reinterpret_cast<const float4*>(base + C::kOffX + g * C::kXBytes) + h;
+#pragma unroll
+        for (int q = 0; q < kN / 4; ++q) {
+          const float4 x = xp[q * 128];
+          f2_unpack(f2_mul(f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(x.x, x.y)), c2), sv[4 * q],
+                    sv[4 * q + 1]);
+          f2_unpack(f2_mul(f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(x.z, x.w)), c2), sv[4 * q + 2],
+                    sv[4 * q + 3]);
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (n_cur >= kN) {
+#pragma unroll
+          for (int i = 0; i < kN; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if (i < n_cur) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        }
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(sm.s_empty[g]));                          // S buffer g may be overwritten
+        mbar_arrive(bar(sm.s_empty[sb]));                         // S buffer sb may be overwritten
         mbar_arrive_cluster_relaxed(xout_free_peer);               // exchange buffer g read out
       }
       // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
@@ -570,50 +555,46 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       sm.m_buf[g][h] = m_cur;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
-      // ---- P = 2^(s c - m(j)) group by group (last group first, from registers),
-      // each group written to P buffer g as soon as it is packed; this
-      // warpgroup's row sum, rescaled to m(j)
+      // ---- look ahead: my next tile's partial S to the peer (before this tile's
+      // exponentials, so that the peer has it by the time it gets there)
+      if (j + 2 < ntiles && !(ok = push(j + 2))) break;
+      // ---- P = 2^(x - m(j)); this warpgroup's row sum, rescaled to m(j)
       if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
       tc_fence_after();
-      constexpr int kPG = C::kPCols / kG;               // packed P columns per 32-column group
       if (active) {
         l_run *= (m_last == -INFINITY) ? 0.f : fast_exp2(m_last - m_cur);
         m_last = m_cur;
-        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_cur, -m_cur);
-        uint64_t sum2 = f2_pack(0.f, 0.f);
-        if (kG > 1) tmem_wait_st();
+        const uint64_t nm2 = f2_pack(-m_cur, -m_cur);
 #pragma unroll
-        for (int k = 0; k < kG; ++k) {
-          const int hb = kG - 1 - k;
-          if (hb < kG - 1) tmem_load_cols<32>(scratch + hb * 32, sv);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(sv[i], sv[i + 1]), c2, nm2), x0, x1);
-            sv[i] = fast_exp2(x0);
-            sv[i + 1] = fast_exp2(x1);
-          }
-          if (n_cur < (hb + 1) * 32) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (hb * 32 + i >= n_cur) sv[i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) sum2 = f2_add(sum2, f2_pack(sv[i], sv[i + 1]));
-          uint32_t pr[kPG];
-          if constexpr (kFp8) {
-#pragma unroll
-            for (int i = 0; i < kPG; ++i) pr[i] = pack_e4m3x4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
-            tmem_st8(tl + p_cols + hb * kPG, pr);
-          } else {
-#pragma unroll
-            for (int i = 0; i < kPG; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-            tmem_st16(tl + p_cols + hb * kPG, pr);
-          }
+        for (int i = 0; i < kN; i += 2) {
+          float x0, x1;
+          f2_unpack(f2_add(f2_pack(sv[i], sv[i + 1]), nm2), x0, x1);
+          sv[i] = fast_exp2(x0);
+          sv[i + 1] = fast_exp2(x1);
         }
-        float s0, s1;
-        f2_unpack(sum2, s0, s1);
-        l_run += s0 + s1;
+        if (n_cur < kN) {
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if (i >= n_cur) sv[i] = 0.f;
+        }
+        uint64_t s4[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < kN; i += 2) s4[(i >> 1) & 1] = f2_add(s4[(i >> 1) & 1], f2_pack(sv[i], sv[i + 1]));
+        float s0, s1, s2, s3;
+        f2_unpack(s4[0], s0, s1);
+        f2_unpack(s4[1], s2, s3);
+        l_run += (s0 + s1) + (s2 + s3);
+        uint32_t pr[C::kPCols];
+        if constexpr (kFp8) {
+#pragma unroll
+          for (int i = 0; i < C::kPCols; ++i)
+            pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i], sv[4 * i + 1]), __NV_SATFINITE, __NV_E4M3) |
+                    ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i + 2], sv[4 * i + 3]), __NV_SATFINITE, __NV_E4M3) << 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+        }
+        tmem_st16(tl + p_cols, pr);
       }
       // ---- O rescale when the reference moved (O holds tiles < j at m(j-1))
       const bool rescale = active && j > 0 && m_cur != m_prev;
@@ -635,8 +616,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(sm.p_full[g]));
-      // ---- look ahead: my next tile's partial S to the peer
-      if (j + 2 < ntiles && !(ok = push(j + 2))) break;
     }
     // total row sum: both warpgroups' sums brought to the final reference
     if (active) {
@@ -708,7 +687,9 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   // ---------------------------------------------------------------- teardown
   __syncthreads();
   if (warp == kMmaWarp) {
-    warp_wait(cx, bar(sm.o_full), 0);     // no MMA may still write TMEM
+    // no MMA may still use TMEM (bounded, and not cut short by the abort flag)
+    drain_wait(bar(sm.qk_done), 0);
+    drain_wait(bar(sm.o_full), 0);
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
