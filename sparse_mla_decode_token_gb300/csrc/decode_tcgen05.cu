@@ -354,24 +354,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // ============================================================ producer
     // A warp's TMA requests are served one after another (about 50 ns per
     // gather4), so the tile's requests are spread over all producer warps.
-    // While tile j is gathered, the rows of tile j + kStages (the next user of
-    // the same stage) are prefetched into L2, so that its gather meets L2
-    // rather than HBM latency.
     if (tid == 0) {
       prefetch_tensormap(&P.tm_swa);
       prefetch_tensormap(&P.tm_comp);
     }
-    const int64_t half_off = (int64_t)rank * kHalfDims * C::kElem;   // this CTA's half of a row, in bytes
-    auto prefetch_tile = [&](int jt) {
-      const int start = tile_start(jt), n = tile_n(jt);
-      const bool swa = jt < tswa;
-      const unsigned char* pool = static_cast<const unsigned char*>(swa ? p.swa : p.comp) + half_off;
-      const int64_t row_bytes = (swa ? p.swa_stride : p.comp_stride) * C::kElem;
-      for (int li = warp * 32 + lane; li < n * C::kRegions; li += kProducerWarps * 32) {
-        const int r = li / C::kRegions, kb = li % C::kRegions;
-        prefetch_l2(pool + (int64_t)idx_s[start + r] * row_bytes + kb * 128);
-      }
-    };
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
@@ -388,7 +374,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
                     rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
                     bar(sm.kv_full[st]));
       }
-      if (j + C::kStages < ntiles) prefetch_tile(j + C::kStages);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     // leave no TMA write of this warp in flight (normally the consumers have waited for all of them)

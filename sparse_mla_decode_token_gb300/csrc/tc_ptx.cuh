@@ -342,11 +342,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
-// Fetch the 128-byte line holding `addr` into L2 (no register result).
-__device__ __forceinline__ void prefetch_l2(const void* addr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
