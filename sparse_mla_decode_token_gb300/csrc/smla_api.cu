@@ -117,8 +117,10 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
       return fail(SMLA_ERR_INVALID_ARG, "num_splits %d < %d: the tcgen05 kernel takes at most %d columns per split",
                   S, s_min, SMLA_TC_MAX_SPLIT_COLS);
     if (S == 0) {
+      // as many splits as keep every cluster in one wave (a second, partial
+      // wave costs a whole unit of time for a few clusters)
       const int64_t pairs = sms / 2;
-      int64_t want = a->sum_q > 0 ? (pairs + a->sum_q - 1) / a->sum_q : 1;
+      int64_t want = a->sum_q > 0 ? pairs / a->sum_q : 1;
       const int64_t by_width = (a->width + 255) / 256;  // keep >= 4 tiles of 64 slots per split
       if (want > by_width) want = by_width;
       if (want > max_splits) want = max_splits;
