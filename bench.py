@@ -361,6 +361,7 @@ def run_gpu(args):
     roof["algorithmic_bytes_per_launch"] = gathered_bytes
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
     roof["main_kernel_us"] = 1e6 * main_s
+    roof["kernels_timed"] = "split kernel" if plan.num_splits == 1 else "split kernel + combine (programmatic dependent launch)"
     roof["roofline_frac_whole_step"] = max(t_hbm, t_tc) / (total_s / (K * 1.0)) if ws_ == 1 else None
 
     if rank != 0:

@@ -123,7 +123,9 @@ typedef struct smla_args {
   int32_t* error_word;              /* optional device int32; kernels OR SMLA_DEVERR_* bits into it */
 
   /* Optional cudaEvent_t handles recorded on the stream immediately before
-   * and after the main decode kernel (not the combine).  For profiling. */
+   * the split kernel and after the last kernel of the call (the split kernel
+   * when num_splits == 1, else the combine, which is launched as a
+   * programmatic dependent of the split kernel).  For profiling. */
   void* profile_event_begin;
   void* profile_event_end;
 } smla_args;

@@ -25,22 +25,41 @@ combine_kernel(const DecodeParams p) {
   if (th >= (int64_t)p.sum_q * p.H) return;
   const int h = (int)(th % p.H);
   const float* lse_s = p.part_lse + th * S;
+  const float4* o_s = reinterpret_cast<const float4*>(p.part_o + th * S * kHeadDim + d);
+  // the split kernel's partials become visible here (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // loads in batches of kBatch independent requests, so that their latencies overlap
+  constexpr int kBatch = 8;
   float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(lse_s + s));
+  for (int s0 = 0; s0 < S; s0 += kBatch) {
+    float l[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) l[k] = s0 + k < S ? __ldg(lse_s + s0 + k) : -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) mx = fmaxf(mx, l[k]);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (mx != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      float ls = __ldg(lse_s + s);
-      if (ls == -INFINITY) continue;
-      float w = fast_exp2(ls - mx);
-      float4 o = __ldg(reinterpret_cast<const float4*>(p.part_o + (th * S + s) * kHeadDim + d));
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
-      wsum += w;
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+      float w[kBatch];
+      float4 o[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const bool in = s0 + k < S;
+        const float ls = in ? __ldg(lse_s + s0 + k) : -INFINITY;
+        w[k] = ls == -INFINITY ? 0.f : fast_exp2(ls - mx);   // an empty split's partial is all zero
+        o[k] = in ? __ldg(o_s + (int64_t)(s0 + k) * (kHeadDim / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        acc.x = fmaf(w[k], o[k].x, acc.x);
+        acc.y = fmaf(w[k], o[k].y, acc.y);
+        acc.z = fmaf(w[k], o[k].z, acc.z);
+        acc.w = fmaf(w[k], o[k].w, acc.w);
+        wsum += w[k];
+      }
     }
   }
   float lse = -INFINITY, f = 0.f;
@@ -63,8 +82,20 @@ combine_kernel(const DecodeParams p) {
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
   const int64_t heads = (int64_t)p.sum_q * p.H;
   const int64_t grid = (heads + kHeadsPerCta - 1) / kHeadsPerCta;
-  combine_kernel<<<(unsigned)grid, kHeadsPerCta * kThreadsPerHead, 0, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the combine grid may be scheduled while the
+  // split kernel drains; griddepcontrol.wait in the kernel orders its reads
+  // after the split kernel's writes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kHeadsPerCta * kThreadsPerHead);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 }  // namespace smla

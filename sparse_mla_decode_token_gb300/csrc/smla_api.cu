@@ -249,13 +249,13 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   ce = plan.kernel == SMLA_KERNEL_TCGEN05 ? launch_decode_tc(p, plan.grid, stream)
                                           : launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
-  if (a->profile_event_end) {
-    ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_end), stream);
-    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
-  }
   if (plan.num_splits > 1) {
     ce = launch_combine(p, stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
+  }
+  if (a->profile_event_end) {
+    ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_end), stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
   }
   return SMLA_OK;
 }
