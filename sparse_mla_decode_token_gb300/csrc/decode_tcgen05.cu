@@ -121,6 +121,7 @@ struct Cfg {
   static_assert(kPCols == 16, "P buffer width");
   static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
   static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
+  static_assert(kStages * kStageBytes + 2 * kXBytes >= 2 * 128 * 512, "partial staging fits in the KV stages and exchange buffers");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -182,7 +183,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <bool kFp8>
+// kPartial: the launch has num_splits > 1 and writes fp32 split partials; its
+// epilogue stages the partial rows in shared memory for contiguous stores (a
+// separate instantiation, so that the single-split code is compiled alone).
+template <bool kFp8, bool kPartial>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
   using C = Cfg<kFp8>;
@@ -632,6 +636,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
       }
       const int64_t row_th = (int64_t)t * H + h;
+      if constexpr (!kPartial) {
 #pragma unroll 1
       for (int cc = 0; cc < kHalfDims / 64; ++cc) {
         const int col = g * (kHalfDims / 2) + cc * 32;
@@ -665,6 +670,45 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         } else {
           p.part_lse[row_th * S + s] = lse;
         }
+      }
+      } else {
+        // fp32 partial rows go through shared memory (the KV stages and
+        // exchange buffers are free once every PV is done), so that the global
+        // stores below are whole 512-byte row segments rather than one 16-byte
+        // piece per row per warp instruction.  Warpgroup g stages its 128
+        // columns; 16-byte chunks are XOR-swizzled by the row to spread banks.
+        unsigned char* row = base + C::kOffKV + g * (128 * 512) + h * 512;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+          const int col = g * (kHalfDims / 2) + cc * 32;
+          float v[32];
+          if (have) {
+            uint32_t r[32];
+            tmem_ld32(tl + kOCol + col, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(row + (((cc * 8 + q) ^ (h & 7)) << 4)) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
+      }
+    }
+    // copy-out of this warpgroup's staged partial columns, 512 contiguous bytes per row
+    if constexpr (kPartial) {
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(128) : "memory");
+      const unsigned char* stg = base + C::kOffKV + g * (128 * 512);
+      const int w4 = (warp - kSoftmaxWarp0) & 3;
+      const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
+      for (int r = w4; r < H; r += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(stg + r * 512 + ((lane ^ (r & 7)) << 4));
+        *reinterpret_cast<float4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + lane * 4) = x;
       }
     }
   }
@@ -730,15 +774,18 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
   e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype);
   if (e != cudaSuccess) return e;
   const int smem = tc_smem_bytes(p.dtype);
-  if (p.dtype == SMLA_BF16) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_tc_kernel<false><<<grid, kThreads, smem, stream>>>(P);
-  } else {
-    e = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_tc_kernel<true><<<grid, kThreads, smem, stream>>>(P);
-  }
+  auto launch = [&](auto kernel) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, stream>>>(P);
+    return cudaSuccess;
+  };
+  const bool partial = p.num_splits > 1;
+  if (p.dtype == SMLA_BF16)
+    e = partial ? launch(decode_tc_kernel<false, true>) : launch(decode_tc_kernel<false, false>);
+  else
+    e = partial ? launch(decode_tc_kernel<true, true>) : launch(decode_tc_kernel<true, false>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
