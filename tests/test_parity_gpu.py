@@ -170,7 +170,8 @@ def probe_row(swa, comp, width):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
-def test_masking_probes(kernel, dtype):
+@pytest.mark.parametrize("H", [64, 128])
+def test_masking_probes(kernel, dtype, H):
     W_ = 128 + 200
     rng = np.random.default_rng(11)
     rows = []
@@ -195,7 +196,7 @@ def test_masking_probes(kernel, dtype):
     idx = np.stack(rows)
     topk = np.array([W_, 128, W_, 200, W_, 0, W_, W_])
     seq = [10 ** 6] * 7 + [5]
-    w = probe_case(idx, seq_lens=seq, topk_lens=topk, dtype=dtype, bmm2=0.5)
+    w = probe_case(idx, seq_lens=seq, topk_lens=topk, H=H, dtype=dtype, bmm2=0.5)
     out, lse, _ = run_gpu(w, kernel=kernel)
     check_probe(w, out, lse)
     for splits in (2, 5):
