@@ -181,6 +181,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device="cpu") -> float:
+    """The largest x over the replicas (the job's time is that of its slowest
+    replica).  Needs an initialised process group when ws > 1."""
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank: int, seconds: float, ws: int, device="cpu") -> float:
+    """Whole-job tokens/s of ws independent replicas: all tokens over the
+    slowest replica's time."""
+    return tokens_per_rank * ws / max_over_ranks(seconds, ws, device)
+
+
 def workload_config(w, n: int) -> dict:
     return {"workload": W.CONFIG_NAMES[n], "dtype": w.dtype, "batch": w.batch, "sum_q": w.sum_q,
             "num_heads": w.num_heads, "head_dim": HEAD_DIM, "index_width": w.width,
@@ -332,15 +349,9 @@ def run_gpu(args):
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     main_ms = [a.elapsed_time(b) for a, b in ev_main]
     e2e_ms = [a.elapsed_time(b) for a, b in ev_e2e]
-    total_s = sum(step_ms) / 1e3
-    if ws_ > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    n_tok_all = w.sum_q * K * ws_
-    value = n_tok_all / total_s
-    e2e_value = w.sum_q * K * ws_ / (sum(e2e_ms) / 1e3)
+    total_s = max_over_ranks(sum(step_ms) / 1e3, ws_, dev)
+    value = w.sum_q * K * ws_ / total_s                 # all replicas' tokens over the slowest replica's time
+    e2e_value = replica_throughput(w.sum_q * K, sum(e2e_ms) / 1e3, ws_, dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_seq, h_lens, h_cum) if t is not None)
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
