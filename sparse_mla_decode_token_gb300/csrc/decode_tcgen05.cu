@@ -494,10 +494,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     for (; ok && j < ntiles; j += 2) {
       const int n_cur = tile_n(j);
       const int sb = j % kSBufs;
-      if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
-      tc_fence_after();
+      // S(j) is final (this warpgroup pushed it): its TMEM load overlaps the wait for the peer's half
       float sv[kN];
-      float mt = -INFINITY;
       if (active) {
 #pragma unroll
         for (int hb = 0; hb < kN / 32; ++hb) {
@@ -506,6 +504,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
         }
+      }
+      if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
+      tc_fence_after();
+      float mt = -INFINITY;
+      if (active) {
         tmem_wait_ld();
         const float4* xp = reinterpret_cast<const float4*>(base + C::kOffX + g * C::kXBytes) + h;
 #pragma unroll

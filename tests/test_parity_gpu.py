@@ -87,6 +87,21 @@ def test_varlen_parity(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype,H,q_lens,width", [("bf16", 64, [1, 150, 40], 128 + 128),
+                                                   ("e4m3", 128, [2, 64, 1], 128 + 448)])
+def test_mixed_prefill_and_decode_batch(kernel, dtype, H, q_lens, width):
+    """Requests with q_len from 1 to 150 in one call (a mixed prefill/decode
+    batch, flattened tokens on the grid, per-token windows shifted by i).
+    The E4M3 case selects >= ~300 slots per token: with ~130 slots the E4M3
+    quantisation of P alone (P relative to the lazily held reference maximum)
+    reaches ~0.04 in max |dO| in an fp32 simulation of the kernel's arithmetic."""
+    w = small_case(21 + H, dtype=dtype, H=H, width=width, batch=len(q_lens), q_lens=q_lens, seq_len=4000)
+    assert w.cum_seq_lens_q is not None and w.sum_q == sum(q_lens)
+    out, lse, _ = run_gpu(w, kernel=kernel)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_swa_only_width_128(kernel):
     w = small_case(8, dtype="e4m3", H=128, width=128, holes=False, topk="none")
     out, lse, _ = run_gpu(w, kernel=kernel)
