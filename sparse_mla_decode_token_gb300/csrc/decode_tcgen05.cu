@@ -314,8 +314,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
     }
     __syncthreads();
-    if (warp == 0) {   // exclusive scan of the chunk counts (at most kMaxChunks = 72 entries)
+    // every warp scans the chunk counts itself (at most kMaxChunks = 72, three
+    // shuffle scans), which saves a serialised scan and a block barrier
+    int chunk_base[kChunksPerWarp];
+    {
       int carry = 0;
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
       for (int base0 = 0; base0 < nchunks; base0 += 32) {
         const int k = base0 + lane;
         const int v = k < nchunks ? sm.chunk_off[k] : 0;
@@ -325,18 +330,23 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           const int u = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += u;
         }
-        if (k < nchunks) sm.chunk_off[k] = carry + incl - v;
+        // exclusive prefix of this warp's chunks k = warp + q * kWarps in this group of 32
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int kq = warp + q * kWarps;
+          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
+          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
+        }
         carry += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (lane == 0) sm.nvalid = carry;
+      if (warp == 0 && lane == 0) sm.nvalid = carry;
     }
-    __syncthreads();
 #pragma unroll
     for (int q = 0; q < kChunksPerWarp; ++q) {
       const int k = warp + q * kWarps;
       if (k < nchunks) {
         const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        if (rv[q] >= 0) idx_s[sm.chunk_off[k] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+        if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
       }
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
