@@ -7,19 +7,22 @@
 // 32 for BF16):
 //
 //   set-up (all warps)  stage the split's index columns and compact the valid
-//                       slots (block-wide scan) into a list: SWA slots, then
-//                       compressed slots; tiles are runs of N list entries of
-//                       one pool (masked slots are never loaded)
-//   producer warps 0-3  warp w gathers tiles w, w+4, ...: the pair's half of
-//                       every selected row (256 dims) with TMA tile::gather4
-//                       (four rows per instruction) into a 128-byte-swizzled,
-//                       UMMA-canonical shared-memory tile; TMA requests of one
-//                       warp are served one after another, so four warps issue
-//   MMA warp 4          S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
-//                       O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
-//                       P read from TMEM); one thread issues tcgen05.mma, QK two
-//                       tiles ahead of PV; accumulators live in TMEM
-//   softmax warps 5-12  two warpgroups taking whole tiles in turn (warpgroup
+//                       slots (per-warp ballots and scans) into a list: SWA
+//                       slots, then compressed slots; tiles are runs of N list
+//                       entries of one pool (masked slots are never loaded)
+//   producer warps 0-5  the pair's half of every selected row (256 dims) with
+//                       TMA tile::gather4 (four rows of 128 bytes per request)
+//                       into a 128-byte-swizzled, UMMA-canonical shared-memory
+//                       tile; a warp's TMA requests are served one after
+//                       another, so every tile's 32 requests are spread over
+//                       the six warps
+//   QK warp 6           S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
+//                       into one of three TMEM S buffers; also allocates and
+//                       frees TMEM
+//   PV warp 7           O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
+//                       P read from TMEM); a separate issuer so that no QK
+//                       waits behind a PV that waits for the softmax
+//   softmax warps 8-15  two warpgroups taking whole tiles in turn (warpgroup
 //                       g takes tiles j with j % 2 == g), one thread per head:
 //                       read S_r from TMEM, push it to the peer CTA with
 //                       st.async (completing bytes on the peer's mbarrier), add
@@ -28,9 +31,11 @@
 //                       m(j-1) (handed over by the other warpgroup through
 //                       shared memory), exponentials in base 2 with lazy
 //                       rescaling of O, write P (BF16 or E4M3) into TMEM;
-//                       finally normalise O and store it (BF16 output or fp32
-//                       split partial) plus the LSE.  One warpgroup's
-//                       exponentials overlap the other's loads and exchange.
+//                       finally normalise O and store it (BF16 output, or fp32
+//                       split partials staged through shared memory) plus the
+//                       LSE.  Each warpgroup pushes its next tile's partial S
+//                       before its exponentials; one warpgroup's exponentials
+//                       overlap the other's loads and exchange.
 //
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
