@@ -281,7 +281,7 @@ def run_gpu(args):
     args_c = B.make_args(q=d_q, swa_kv=d_swa, compressed_kv=d_comp, sparse_indices=d_idx,
                          seq_lens=d_seq, out=out, sparse_topk_lens=d_lens, cum_seq_lens_q=d_cum,
                          sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
-                         out_lse=lse, kernel=args.kernel, error_word=err_word)
+                         out_lse=lse, kernel=args.kernel, num_splits=args.num_splits, error_word=err_word)
     plan = B.smla_plan_decode(args_c, local)
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
@@ -407,6 +407,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    ap.add_argument("--num-splits", type=int, default=0, help="0 = the planner's choice")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle timing")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -121,7 +121,7 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
       // wave costs a whole unit of time for a few clusters)
       const int64_t pairs = sms / 2;
       int64_t want = a->sum_q > 0 ? pairs / a->sum_q : 1;
-      const int64_t by_width = (a->width + 255) / 256;  // keep >= 4 tiles of 64 slots per split
+      const int64_t by_width = (a->width + 63) / 64;    // keep >= 64 columns per split
       if (want > by_width) want = by_width;
       if (want > max_splits) want = max_splits;
       if (want < s_min) want = s_min;
