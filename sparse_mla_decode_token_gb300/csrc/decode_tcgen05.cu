@@ -14,8 +14,8 @@
 //                       TMA tile::gather4 (four rows of 128 bytes per request)
 //                       into a 128-byte-swizzled, UMMA-canonical shared-memory
 //                       tile; a warp's TMA requests are served one after
-//                       another, so every tile's 32 requests are spread over
-//                       the six warps
+//                       another, so a tile's 32 requests are spread over the
+//                       three warps of one of two groups taking alternate tiles
 //   QK warp 6           S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
 //                       into one of three TMEM S buffers; also allocates and
 //                       frees TMEM
@@ -59,7 +59,8 @@ using namespace ptx;
 
 constexpr int kMaxN = 64;            // largest tile (slots per tile)
 constexpr int kHalfDims = 256;       // output dims per CTA
-constexpr int kProducerWarps = 6;    // TMA gathers: every producer warp issues a share of every tile
+constexpr int kProducerWarps = 6;    // TMA gathers
+constexpr int kProducerGroups = 2;   // tiles alternate between two groups of three warps that share each tile
 constexpr int kMmaWarp = kProducerWarps;        // QK issue; allocates and frees TMEM
 constexpr int kPvWarp = kMmaWarp + 1;           // PV issue
 constexpr int kSoftmaxWarp0 = kPvWarp + 1;
@@ -372,22 +373,29 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   if (warp < kProducerWarps) {
     // ============================================================ producer
     // A warp's TMA requests are served one after another (about 50 ns per
-    // gather4), so the tile's requests are spread over all producer warps.
+    // gather4), so a tile's requests are spread over the three warps of its
+    // group; two groups take alternate tiles (measured: one group of six
+    // sharing every tile reaches ~15 GB/s per SM from HBM, warps owning whole
+    // tiles ~24 GB/s but with a long issue time per tile; two groups of three
+    // were fastest in the full kernel).
     if (tid == 0) {
       prefetch_tensormap(&P.tm_swa);
       prefetch_tensormap(&P.tm_comp);
     }
-    for (int j = 0; j < ntiles; ++j) {
+    // Producer group pg (kWarpsPerGroup warps) gathers tiles pg, pg + kProducerGroups, ...
+    constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
+    const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
+    for (int j = pg; j < ntiles; j += kProducerGroups) {
       const int st = j % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
       const int start = tile_start(j), n = tile_n(j);
       const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
-      if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
       const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
       const uint32_t stage = kv_addr + st * C::kStageBytes;
       const int32_t* rows = idx_s + start;
       const int groups = (n4 / 4) * C::kRegions;
-      for (int gi = warp + kProducerWarps * lane; gi < groups; gi += kProducerWarps * 32) {
+      for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
         const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
         tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
                     rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
