@@ -48,6 +48,8 @@
 // waits on an unbounded hardware barrier inside its loop.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -757,7 +759,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 cudaError_t encode_fn(EncodeTiledFn* out) {
-  static EncodeTiledFn fn = nullptr;
+  static std::atomic<EncodeTiledFn> cached{nullptr};   // looked up once; callers may be on several threads
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -765,6 +768,7 @@ cudaError_t encode_fn(EncodeTiledFn* out) {
     if (e != cudaSuccess) return e;
     if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
     fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    cached.store(fn, std::memory_order_release);
   }
   *out = fn;
   return cudaSuccess;

@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <string>
 
 #include "common.cuh"
@@ -80,17 +81,17 @@ smla_status check_shapes(const smla_args* a) {
 // Kernel that SMLA_KERNEL_AUTO selects.
 constexpr int kAutoKernel = SMLA_KERNEL_TCGEN05;
 
-int g_sm_count[64];
+std::atomic<int> g_sm_count[64];   // per device; 0 = not queried yet (callers may be on several threads)
 
 smla_status sm_count(int device, int* out) {
   if (device < 0 || device >= 64) return fail(SMLA_ERR_INVALID_ARG, "device %d out of range", device);
-  if (g_sm_count[device] == 0) {
-    int n = 0;
+  int n = g_sm_count[device].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
-    g_sm_count[device] = n;
+    g_sm_count[device].store(n, std::memory_order_relaxed);
   }
-  *out = g_sm_count[device];
+  *out = n;
   return SMLA_OK;
 }
 
