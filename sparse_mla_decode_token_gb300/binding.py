@@ -184,7 +184,20 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
               workspace: Optional[torch.Tensor] = None,
               num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
               error_word: Optional[torch.Tensor] = None) -> SmlaArgs:
-    """Fill ``smla_args`` from tensors (no copies; wrong layouts raise)."""
+    """Fill ``smla_args`` from tensors (no copies; wrong layouts raise).  Every
+    tensor must live on the CUDA device of ``q`` (the library reads raw device
+    pointers; a host pointer would fault the GPU), and the call must then be
+    made with that device current (``sparse_mla_decode`` does both)."""
+    dev = q.device
+    for name, t in (("q", q), ("swa_kv", swa_kv), ("compressed_kv", compressed_kv),
+                    ("sparse_indices", sparse_indices), ("seq_lens", seq_lens), ("out", out),
+                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
+                    ("sinks", sinks), ("out_lse", out_lse), ("workspace", workspace),
+                    ("error_word", error_word), ("bmm1_scale", bmm1_scale), ("bmm2_scale", bmm2_scale)):
+        if isinstance(t, torch.Tensor) and (t.device.type != "cuda" or t.device != dev):
+            raise ValueError(f"{name} is on {t.device}; every tensor must be on the CUDA device of q ({dev})")
+    if dev.type != "cuda":
+        raise ValueError(f"q is on {dev}; the decode runs on a CUDA device")
     if q.dim() == 4:                       # dense [B, q_len, H, 512]
         q = q.reshape(-1, q.shape[2], q.shape[3])
     if q.dim() != 3 or q.shape[-1] != HEAD_DIM or q.stride(-1) != 1 or q.stride(1) != HEAD_DIM:
@@ -260,7 +273,8 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
                      sinks=sinks, bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
                      out_lse=out_lse, workspace=workspace_buffer, num_splits=num_splits,
                      max_splits=max_splits, kernel=kernel, error_word=error_word)
-    smla_decode(args, stream)
+    with torch.cuda.device(query.device):   # the library plans and launches on the current device
+        smla_decode(args, stream)
     return out, out_lse
 
 

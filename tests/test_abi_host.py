@@ -128,3 +128,17 @@ def test_binding_raises_on_missing_library(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         B.lib()
+
+
+def test_binding_rejects_host_tensors():
+    """Host tensors never reach the library (a host pointer read by a kernel
+    would fault the GPU): make_args raises before any CUDA call."""
+    import torch
+    from sparse_mla_decode_token_gb300 import binding as B
+    q = torch.zeros(2, 64, 512, dtype=torch.bfloat16)
+    kv = torch.zeros(256, 512, dtype=torch.bfloat16)
+    idx = torch.zeros(2, 256, dtype=torch.int32)
+    seq = torch.full((2,), 300, dtype=torch.int32)
+    out = torch.empty(2, 64, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        B.make_args(q=q, swa_kv=kv, compressed_kv=kv, sparse_indices=idx, seq_lens=seq, out=out)
