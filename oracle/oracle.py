@@ -45,6 +45,21 @@ Readings where the pages are silent (each is listed in the design notes):
 * Duplicate indices each count as their own slot.
 * An index < -1 or >= the pool's row count is a caller error: raised by
   default, or treated as masked with ``invalid_index="mask"``.
+
+Page-table form of the compressed segment (trtllm_batch_decode_sparse_mla_dsv4,
+Parameters: hca_swa_indices, hca_compressed_block_tables, hca_seq_lens,
+swa_topk_lens, hca_sparse_indices_format):
+
+* the index table then holds only the 128 SWA columns; compressed slot c of
+  token t (logical column 128 + c) is row
+  ``block_tables[t, c // page_size] * page_size + c % page_size`` of the
+  compressed pool (the canonical page_id * page_size + page_offset expansion);
+* request b backs ``hca_seq_lens[b] - 128`` compressed slots (the count
+  includes the 128 window slots); slots past it are not read, and
+  ``sparse_topk_lens`` (logical columns) may cut further;
+* ``swa_topk_lens[t]`` (optional, in either form), clamped to [0, 128], is the
+  token's visible window and replaces the seq_lens rule.  Reading: the window
+  is a leading prefix of the SWA columns, as for the seq_lens rule.
 """
 from __future__ import annotations
 
@@ -135,22 +150,44 @@ def token_position(t, sum_q, batch, cum_seq_lens_q, seq_lens) -> int:
 
 def valid_slots(t: int, *, indices, topk_lens, seq_lens, cum_seq_lens_q,
                 batch: int, swa_rows: int, comp_rows: int,
-                invalid_index: str = "raise") -> list[tuple[int, str, int]]:
-    """List of (column j, pool name, row) that token t attends to, in column order."""
-    sum_q, width = indices.shape
+                invalid_index: str = "raise", width: Optional[int] = None,
+                swa_topk_lens=None, comp_block_tables=None,
+                comp_page_size: int = 0, hca_seq_lens=None) -> list[tuple[int, str, int]]:
+    """List of (column j, pool name, row) that token t attends to, in column order.
+
+    ``width`` is the logical column count W (default: the index table's
+    width); with ``comp_block_tables`` the compressed columns come from the
+    page table (see the module docstring) and ``indices`` needs only the 128
+    SWA columns.
+    """
+    sum_q = indices.shape[0]
+    width = indices.shape[1] if width is None else int(width)
     n_lim = width if topk_lens is None else min(max(int(topk_lens[t]), 0), width)
-    pos = token_position(t, sum_q, batch, cum_seq_lens_q, seq_lens)
-    w_swa = min(SWA_COLS, max(0, pos + 1))
+    b, i, q_len = token_request(t, sum_q, batch, cum_seq_lens_q)
+    if swa_topk_lens is None:
+        w_swa = min(SWA_COLS, max(0, int(seq_lens[b]) - q_len + i + 1))
+    else:
+        w_swa = min(max(int(swa_topk_lens[t]), 0), SWA_COLS)
+    paged = comp_block_tables is not None
+    if paged:
+        n_comp = max(0, int(hca_seq_lens[b]) - SWA_COLS)
     out = []
     for j in range(n_lim):
-        idx = int(indices[t, j])
-        if idx == -1:
-            continue
         if j < SWA_COLS:
-            if j >= w_swa:
+            idx = int(indices[t, j])
+            if idx == -1 or j >= w_swa:
                 continue
             pool, rows = "swa", swa_rows
+        elif paged:
+            c = j - SWA_COLS
+            if c >= n_comp:
+                continue
+            idx = int(comp_block_tables[t, c // comp_page_size]) * comp_page_size + c % comp_page_size
+            pool, rows = "comp", comp_rows
         else:
+            idx = int(indices[t, j])
+            if idx == -1:
+                continue
             pool, rows = "comp", comp_rows
         if not 0 <= idx < rows:
             if invalid_index == "raise":
@@ -235,7 +272,9 @@ def sparse_mla_decode(*, dtype: str, batch: int, q, swa_kv, comp_kv, indices,
                       bmm1_scale: float, bmm2_scale: float,
                       tokens: Optional[Sequence[int]] = None,
                       splits: Optional[int] = None, lse_with_sink: bool = False,
-                      invalid_index: str = "raise"):
+                      invalid_index: str = "raise", width: Optional[int] = None,
+                      swa_topk_lens=None, comp_block_tables=None,
+                      comp_page_size: int = 0, hca_seq_lens=None):
     """Return (O [T, H, 512] float64, LSE2 [T, H] float64) for ``tokens``.
 
     Arguments are raw element bits as the operation takes them (see the module
@@ -253,13 +292,15 @@ def sparse_mla_decode(*, dtype: str, batch: int, q, swa_kv, comp_kv, indices,
         slots = valid_slots(t, indices=indices, topk_lens=topk_lens, seq_lens=seq_lens,
                             cum_seq_lens_q=cum_seq_lens_q, batch=batch,
                             swa_rows=swa_kv.shape[0], comp_rows=comp_kv.shape[0],
-                            invalid_index=invalid_index)
+                            invalid_index=invalid_index, width=width,
+                            swa_topk_lens=swa_topk_lens, comp_block_tables=comp_block_tables,
+                            comp_page_size=comp_page_size, hca_seq_lens=hca_seq_lens)
         q_t = decode(q[t], dtype)                         # [H, 512]
         if splits is None:
             o, lse = attend(q_t, _gather(pools, slots, dtype), bmm1, bmm2, sinks, lse_with_sink)
         else:
-            width = indices.shape[1]
-            n_lim = width if topk_lens is None else min(max(int(topk_lens[t]), 0), width)
+            w_all = indices.shape[1] if width is None else int(width)
+            n_lim = w_all if topk_lens is None else min(max(int(topk_lens[t]), 0), w_all)
             per = -(-n_lim // splits) if n_lim > 0 else 0
             o_s, lse_s = [], []
             for s in range(splits):
@@ -283,4 +324,8 @@ def run_workload(w, **kw):
                              comp_kv=w.comp_kv, indices=w.indices, topk_lens=w.topk_lens,
                              seq_lens=w.seq_lens, cum_seq_lens_q=w.cum_seq_lens_q,
                              sinks=w.sinks, bmm1_scale=w.bmm1_scale,
-                             bmm2_scale=w.bmm2_scale, **kw)
+                             bmm2_scale=w.bmm2_scale, width=w.width,
+                             swa_topk_lens=getattr(w, "swa_topk_lens", None),
+                             comp_block_tables=getattr(w, "comp_block_tables", None),
+                             comp_page_size=getattr(w, "comp_page_size", 0),
+                             hca_seq_lens=getattr(w, "hca_seq_lens", None), **kw)

@@ -17,6 +17,13 @@ A ``Workload`` carries raw host buffers exactly as the operation takes them:
 * ``sinks``    -- ``[H]`` float32 or ``None``
 * ``bmm1_scale``, ``bmm2_scale`` -- float32-representable Python floats
 
+A page-table workload (``make_paged_workload``) instead holds only the 128 SWA
+columns in ``indices`` and gives the compressed segment as per-token rows of
+page IDs ``comp_block_tables`` with ``comp_page_size`` rows per page and
+per-request slot counts ``hca_seq_lens`` (FlashInfer
+``trtllm_batch_decode_sparse_mla_dsv4`` page, Parameters:
+hca_compressed_block_tables, hca_seq_lens, swa_topk_lens).
+
 The five named workloads follow the shapes of the FlashInfer
 ``trtllm_batch_decode_sparse_mla_dsv4`` page (head dim 512, 128 SWA columns,
 H in {64, 128}, BF16 or per-tensor FP8 E4M3) and the vLLM DeepSeek-V4 caller's
@@ -56,6 +63,12 @@ class Workload:
     bmm2_scale: float
     q_scale: float = 1.0
     kv_scale: float = 1.0
+    # page-table form of the compressed segment (None: index form)
+    comp_block_tables: Optional[np.ndarray] = None   # [sum_q, max_pages] int32 page IDs
+    comp_page_size: int = 0
+    hca_seq_lens: Optional[np.ndarray] = None        # [batch] int32: 128 window + compressed slots
+    swa_topk_lens: Optional[np.ndarray] = None       # [sum_q] int32 visible window, or None
+    logical_width: Optional[int] = None              # W when the index table holds SWA columns only
 
     @property
     def sum_q(self) -> int:
@@ -63,7 +76,11 @@ class Workload:
 
     @property
     def width(self) -> int:
-        return int(self.indices.shape[1])
+        return int(self.logical_width if self.logical_width is not None else self.indices.shape[1])
+
+    @property
+    def paged(self) -> bool:
+        return self.comp_block_tables is not None
 
     @property
     def elem_bytes(self) -> int:
@@ -135,6 +152,29 @@ def _unique_rows(rng: np.random.Generator, n_rows: int, k: int) -> np.ndarray:
     return rng.choice(n_rows, size=k, replace=False).astype(np.int32)
 
 
+def _draw_values(gen: torch.Generator, dtype: str, sum_q: int, num_heads: int,
+                 swa_rows: int, comp_rows: int):
+    """N(0, 1) query and pools, encoded; FP8 takes per-tensor scales amax / 448."""
+    qf = _normal(gen, (sum_q, num_heads, HEAD_DIM))
+    swaf = _normal(gen, (swa_rows, HEAD_DIM))
+    compf = _normal(gen, (comp_rows, HEAD_DIM))
+    if dtype == "e4m3":
+        q_scale = _pertensor_scale(qf)
+        kv_scale = _pertensor_scale(swaf, compf)
+    else:
+        q_scale = kv_scale = 1.0
+    return (_encode(qf, dtype, q_scale), _encode(swaf, dtype, kv_scale),
+            _encode(compf, dtype, kv_scale), q_scale, kv_scale)
+
+
+def _lengths(q_lens, seq_lens, batch: int):
+    q_lens = np.broadcast_to(np.asarray(q_lens, dtype=np.int64), (batch,)).copy()
+    seq_lens = np.broadcast_to(np.asarray(seq_lens, dtype=np.int64), (batch,)).astype(np.int32)
+    cum = np.zeros(batch + 1, dtype=np.int32)
+    cum[1:] = np.cumsum(q_lens)
+    return q_lens, seq_lens, cum
+
+
 # --------------------------------------------------------------------------
 # generic generator
 # --------------------------------------------------------------------------
@@ -157,30 +197,15 @@ def make_workload(*, name: str = "custom", seed: int, dtype: str, batch: int,
     assert dtype in ("bf16", "e4m3")
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
-    q_lens = np.broadcast_to(np.asarray(q_lens, dtype=np.int64), (batch,)).copy()
-    seq_lens = np.broadcast_to(np.asarray(seq_lens, dtype=np.int64), (batch,)).astype(np.int32)
+    q_lens, seq_lens, cum = _lengths(q_lens, seq_lens, batch)
     sum_q = int(q_lens.sum())
     if varlen is None:
         varlen = bool((q_lens != q_lens[0]).any())
-    cum = np.zeros(batch + 1, dtype=np.int32)
-    cum[1:] = np.cumsum(q_lens)
     ring_len = ring_len if ring_len is not None else swa_rows // batch
     n_comp_cols = width - SWA_COLS
     assert n_comp_cols >= 0
 
-    # values
-    qf = _normal(gen, (sum_q, num_heads, HEAD_DIM))
-    swaf = _normal(gen, (swa_rows, HEAD_DIM))
-    compf = _normal(gen, (comp_rows, HEAD_DIM))
-    if dtype == "e4m3":
-        q_scale = _pertensor_scale(qf)
-        kv_scale = _pertensor_scale(swaf, compf)
-    else:
-        q_scale = kv_scale = 1.0
-    q = _encode(qf, dtype, q_scale)
-    swa_kv = _encode(swaf, dtype, kv_scale)
-    comp_kv = _encode(compf, dtype, kv_scale)
-    del qf, swaf, compf
+    q, swa_kv, comp_kv, q_scale, kv_scale = _draw_values(gen, dtype, sum_q, num_heads, swa_rows, comp_rows)
 
     # index table
     pos = token_positions(seq_lens, q_lens)
@@ -209,8 +234,69 @@ def make_workload(*, name: str = "custom", seed: int, dtype: str, batch: int,
                     kv_scale=kv_scale)
 
 
+def make_paged_workload(*, name: str = "paged", seed: int, dtype: str, batch: int,
+                        q_lens, num_heads: int, swa_rows: int, comp_pages: int,
+                        page_size: int, max_pages: int, hca_seq_lens, seq_lens,
+                        ring_len: Optional[int] = None, topk_lens=None,
+                        swa_topk_lens=None, sinks: bool = False,
+                        varlen: Optional[bool] = None, fill_unused: int = -1,
+                        width: Optional[int] = None,
+                        softmax_scale: float = 1.0 / math.sqrt(HEAD_DIM)) -> Workload:
+    """Draw a workload whose compressed segment is a page table.
+
+    Every request owns ``max_pages`` distinct random pages of the compressed
+    pool (``comp_pages * page_size`` rows); its tokens share that page list.
+    Table entries past the request's footprint ``ceil((hca_seq_lens[b] - 128)
+    / page_size)`` hold ``fill_unused`` (never read as rows).  All 128 SWA
+    columns hold legal ring rows; the visible window is ``swa_topk_lens`` when
+    given, else the seq_lens rule.  ``width`` (logical columns) defaults to
+    ``128 + max_pages * page_size``.
+    """
+    assert dtype in ("bf16", "e4m3")
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    q_lens, seq_lens, cum = _lengths(q_lens, seq_lens, batch)
+    sum_q = int(q_lens.sum())
+    if varlen is None:
+        varlen = bool((q_lens != q_lens[0]).any())
+    ring_len = ring_len if ring_len is not None else swa_rows // batch
+    assert ring_len >= SWA_COLS and batch * ring_len <= swa_rows
+    comp_rows = comp_pages * page_size
+    assert max_pages <= comp_pages
+    hca = np.broadcast_to(np.asarray(hca_seq_lens, dtype=np.int64), (batch,)).astype(np.int32)
+    assert int(hca.max()) - SWA_COLS <= max_pages * page_size
+    width = SWA_COLS + max_pages * page_size if width is None else int(width)
+
+    q, swa_kv, comp_kv, q_scale, kv_scale = _draw_values(gen, dtype, sum_q, num_heads, swa_rows, comp_rows)
+
+    pos = token_positions(seq_lens, q_lens)
+    req_of_token = np.repeat(np.arange(batch), q_lens)
+    indices = np.empty((sum_q, SWA_COLS), dtype=np.int32)
+    tables = np.full((sum_q, max_pages), fill_unused, dtype=np.int32)
+    pages_of = [rng.choice(comp_pages, size=max_pages, replace=False).astype(np.int32) for _ in range(batch)]
+    for t in range(sum_q):
+        b = int(req_of_token[t])
+        p = int(pos[t]) - (SWA_COLS - 1) + np.arange(SWA_COLS)       # every column a legal ring row
+        indices[t] = b * ring_len + (p % ring_len)
+        used = -(-max(0, int(hca[b]) - SWA_COLS) // page_size)
+        tables[t, :used] = pages_of[b][:used]
+    if topk_lens is not None:
+        topk_lens = np.broadcast_to(np.asarray(topk_lens, dtype=np.int64), (sum_q,)).astype(np.int32)
+    if swa_topk_lens is not None:
+        swa_topk_lens = np.broadcast_to(np.asarray(swa_topk_lens, dtype=np.int64), (sum_q,)).astype(np.int32)
+    sink_vals = _normal(gen, (num_heads,)).numpy().astype(np.float32) if sinks else None
+    return Workload(name=name, dtype=dtype, batch=batch, num_heads=num_heads,
+                    q=q, swa_kv=swa_kv, comp_kv=comp_kv, indices=indices,
+                    topk_lens=topk_lens, seq_lens=seq_lens,
+                    cum_seq_lens_q=cum if varlen else None, sinks=sink_vals,
+                    bmm1_scale=f32(softmax_scale * q_scale * kv_scale), bmm2_scale=f32(kv_scale),
+                    q_scale=q_scale, kv_scale=kv_scale, comp_block_tables=tables,
+                    comp_page_size=page_size, hca_seq_lens=hca, swa_topk_lens=swa_topk_lens,
+                    logical_width=width)
+
+
 # --------------------------------------------------------------------------
-# the five named workloads
+# the named workloads
 # --------------------------------------------------------------------------
 
 CONFIG_NAMES = {

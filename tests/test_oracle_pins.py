@@ -361,6 +361,105 @@ def test_lse_with_sink_reading_differs_only_in_lse():
 
 # ----------------------------------------- planted mistakes are caught
 
+# ---------------------------------------------------------------- page-table form
+
+def _golden_page_table():
+    with open(os.path.join(HERE, "golden", "page_table_expansion.json")) as f:
+        return json.load(f)
+
+
+def test_page_table_slots_golden():
+    """Hand-worked slot lists of the page-table form (fixture cites its rules)."""
+    g = _golden_page_table()
+    T = len(g["block_tables"])
+    indices = np.array([[200 + 128 * t + j for j in range(128)] for t in range(T)], dtype=np.int32)
+    for e in g["expected"]:
+        t = e["token"]
+        got = orc.valid_slots(t, indices=indices, topk_lens=np.asarray(g["sparse_topk_lens"]),
+                              seq_lens=np.full(g["batch"], 100000), cum_seq_lens_q=None,
+                              batch=g["batch"], swa_rows=g["swa_rows"], comp_rows=g["comp_rows"],
+                              width=g["width"], swa_topk_lens=np.asarray(g["swa_topk_lens"]),
+                              comp_block_tables=np.asarray(g["block_tables"], dtype=np.int32),
+                              comp_page_size=g["page_size"], hca_seq_lens=np.asarray(g["hca_seq_lens"]))
+        if e.get("swa_all"):
+            want = [(j, "swa", 200 + 128 * t + j) for j in range(128)]
+        else:
+            want = [tuple(x) for x in e["slots"]]
+        assert got == want, (t, got, want)
+
+
+def test_page_table_single_slot_closed_form():
+    """One page-table slot: O = row * bmm2 and LSE2 = l * log2 e."""
+    rng = np.random.default_rng(5)
+    comp = rng.standard_normal((8, 512)).astype(np.float32)
+    q = rng.standard_normal((1, 4, 512)).astype(np.float32)
+    indices = np.zeros((1, 128), np.int32)
+    o, lse = case(H=4, q=q, comp=comp, indices=indices, bmm1=0.03, bmm2=0.5, width=130,
+                  swa_topk_lens=np.array([0], np.int32), comp_block_tables=np.array([[3]], np.int32),
+                  comp_page_size=2, hca_seq_lens=np.array([129], np.int32))
+    row = bf16_round(comp[6])                     # page 3, offset 0 -> row 3 * 2 + 0
+    qd = bf16_round(q[0])
+    np.testing.assert_allclose(o[0], np.broadcast_to(0.5 * row, (4, 512)), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0], 0.03 * (qd @ row) * LOG2E, rtol=1e-12, atol=1e-12)
+
+
+def _paged_small(fill_unused=-1, seed=11):
+    from sparse_mla_decode_token_gb300 import workloads as W
+    return W.make_paged_workload(seed=seed, dtype="bf16", batch=3, q_lens=[1, 2, 1], num_heads=4,
+                                 swa_rows=3 * 130, comp_pages=16, page_size=8, max_pages=5,
+                                 hca_seq_lens=[128 + 37, 128 + 8, 100], seq_lens=[5000, 60, 3000],
+                                 topk_lens=[160, 170, 140, 200], swa_topk_lens=[128, 17, 0, 64],
+                                 fill_unused=fill_unused, varlen=True, sinks=True)
+
+
+def test_page_table_equals_expanded_index_table():
+    """The page-table form equals the index form with the rows written out."""
+    w = _paged_small()
+    o, lse = orc.run_workload(w)
+    T, W = w.sum_q, w.width
+    ind = np.full((T, W), -1, np.int32)
+    ind[:, :128] = w.indices
+    cum = w.cum_seq_lens_q
+    for t in range(T):
+        b = int(np.searchsorted(cum, t, side="right") - 1)
+        n_c = max(0, int(w.hca_seq_lens[b]) - 128)
+        c = np.arange(n_c)
+        ind[t, 128:128 + n_c] = w.comp_block_tables[t, c // w.comp_page_size] * w.comp_page_size + c % w.comp_page_size
+        ind[t, :128][np.arange(128) >= min(max(int(w.swa_topk_lens[t]), 0), 128)] = -1
+    o2, lse2 = orc.sparse_mla_decode(dtype=w.dtype, batch=w.batch, q=w.q, swa_kv=w.swa_kv, comp_kv=w.comp_kv,
+                                     indices=ind, topk_lens=w.topk_lens, seq_lens=np.full(w.batch, 100000),
+                                     cum_seq_lens_q=cum, sinks=w.sinks, bmm1_scale=w.bmm1_scale,
+                                     bmm2_scale=w.bmm2_scale)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_page_table_entries_past_the_footprint_are_never_read():
+    o1, l1 = orc.run_workload(_paged_small(fill_unused=-1))
+    o2, l2 = orc.run_workload(_paged_small(fill_unused=7))
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_swa_topk_lens_equals_minus_one_mask():
+    """A visible window of k columns is the same as -1 in SWA columns >= k."""
+    rng = np.random.default_rng(3)
+    swa = rng.standard_normal((200, 512)).astype(np.float32)
+    q = rng.standard_normal((2, 4, 512)).astype(np.float32)
+    ind = np.stack([rng.choice(200, size=128, replace=False) for _ in range(2)]).astype(np.int32)
+    k = [37, 128]
+    o1, l1 = case(H=4, q=q, swa=swa, indices=ind, seq_lens=(100000, 100000),
+                  swa_topk_lens=np.asarray(k, np.int32))
+    masked = ind.copy()
+    masked[0, 37:] = -1
+    o2, l2 = case(H=4, q=q, swa=swa, indices=masked, seq_lens=(100000, 100000))
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    # the window overrides the seq_lens rule (position 9 would allow 10 columns)
+    o3, _ = case(H=4, q=q, swa=swa, indices=ind, seq_lens=(10, 100000), swa_topk_lens=np.asarray(k, np.int32))
+    np.testing.assert_array_equal(o1, o3)
+
+
 def test_pins_catch_a_dropped_sink(monkeypatch):
     """Plant a mistake in the oracle (sink left out) and check a pin fails."""
     orig = orc.attend
