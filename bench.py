@@ -44,13 +44,21 @@ HEAD_DIM, SWA_COLS = 512, 128
 
 def valid_slots_per_token(w) -> np.ndarray:
     """Slots each token reads: columns below clamp(topk_lens, 0, W) that are not
-    -1 and, for SWA columns, inside the window min(128, pos + 1)."""
-    T, width = w.indices.shape
+    -1 and, for SWA columns, inside the window min(128, pos + 1) (or the
+    per-row window lengths); in the page-table form the compressed columns
+    below the request's backed count hca_seq_lens[b]."""
+    T, width = w.sum_q, w.width
     n_lim = np.full(T, width) if w.topk_lens is None else np.clip(w.topk_lens, 0, width)
     q_lens = (np.full(w.batch, T // w.batch) if w.cum_seq_lens_q is None
               else np.diff(w.cum_seq_lens_q))
     pos = np.concatenate([np.arange(ql) + sl - ql for sl, ql in zip(w.seq_lens, q_lens)])
-    w_swa = np.clip(pos + 1, 0, SWA_COLS)
+    w_swa = np.clip(pos + 1 if w.swa_topk_lens is None else w.swa_topk_lens, 0, SWA_COLS)
+    if w.paged:
+        req = np.repeat(np.arange(w.batch), q_lens)
+        n_lim = np.minimum(n_lim, np.maximum(SWA_COLS, w.hca_seq_lens[req]))
+        j = np.arange(SWA_COLS)[None, :]
+        swa = ((j < n_lim[:, None]) & (w.indices != -1) & (j < w_swa[:, None])).sum(axis=1)
+        return swa + np.maximum(0, n_lim - SWA_COLS)
     j = np.arange(width)[None, :]
     active = (j < n_lim[:, None]) & (w.indices != -1) & ((j >= SWA_COLS) | (j < w_swa[:, None]))
     return active.sum(axis=1)
@@ -199,7 +207,8 @@ def replica_throughput(tokens_per_rank: int, seconds: float, ws: int, device="cp
 
 
 def workload_config(w, n: int) -> dict:
-    return {"workload": W.CONFIG_NAMES[n], "dtype": w.dtype, "batch": w.batch, "sum_q": w.sum_q,
+    extra = {"page_size": w.comp_page_size, "pages_per_token": int(w.comp_block_tables.shape[1])} if w.paged else {}
+    return {"workload": W.CONFIG_NAMES[n], **extra, "dtype": w.dtype, "batch": w.batch, "sum_q": w.sum_q,
             "num_heads": w.num_heads, "head_dim": HEAD_DIM, "index_width": w.width,
             "swa_rows": int(w.swa_kv.shape[0]), "compressed_rows": int(w.comp_kv.shape[0]),
             "sinks": w.sinks is not None, "varlen": w.cum_seq_lens_q is not None,
@@ -265,6 +274,9 @@ def run_gpu(args):
     h_lens = i32(w.topk_lens).pin_memory() if w.topk_lens is not None else None
     h_seq = i32(w.seq_lens).pin_memory()
     h_cum = i32(w.cum_seq_lens_q).pin_memory() if w.cum_seq_lens_q is not None else None
+    h_bt = i32(w.comp_block_tables).pin_memory() if w.paged else None
+    h_hca = i32(w.hca_seq_lens).pin_memory() if w.paged else None
+    h_win = i32(w.swa_topk_lens).pin_memory() if w.swa_topk_lens is not None else None
     # device-resident state: KV pools, sinks
     d_swa = kv(w.swa_kv).to(dev)
     d_comp = kv(w.comp_kv).to(dev)
@@ -272,6 +284,9 @@ def run_gpu(args):
     d_q, d_idx, d_seq = h_q.to(dev), h_idx.to(dev), h_seq.to(dev)
     d_lens = h_lens.to(dev) if h_lens is not None else None
     d_cum = h_cum.to(dev) if h_cum is not None else None
+    d_bt = h_bt.to(dev) if h_bt is not None else None
+    d_hca = h_hca.to(dev) if h_hca is not None else None
+    d_win = h_win.to(dev) if h_win is not None else None
     out = torch.empty((w.sum_q, w.num_heads, HEAD_DIM), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.sum_q, w.num_heads), dtype=torch.float32, device=dev)
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -281,7 +296,9 @@ def run_gpu(args):
     args_c = B.make_args(q=d_q, swa_kv=d_swa, compressed_kv=d_comp, sparse_indices=d_idx,
                          seq_lens=d_seq, out=out, sparse_topk_lens=d_lens, cum_seq_lens_q=d_cum,
                          sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
-                         out_lse=lse, kernel=args.kernel, num_splits=args.num_splits, error_word=err_word)
+                         out_lse=lse, kernel=args.kernel, num_splits=args.num_splits, error_word=err_word,
+                         swa_topk_lens=d_win, comp_block_tables=d_bt, comp_page_size=w.comp_page_size,
+                         hca_seq_lens=d_hca, width=w.width if w.paged else None)
     plan = B.smla_plan_decode(args_c, local)
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
@@ -339,8 +356,9 @@ def run_gpu(args):
             d_seq.copy_(h_seq, non_blocking=True)
             if d_lens is not None:
                 d_lens.copy_(h_lens, non_blocking=True)
-            if d_cum is not None:
-                d_cum.copy_(h_cum, non_blocking=True)
+            for d_t, h_t in ((d_cum, h_cum), (d_bt, h_bt), (d_hca, h_hca), (d_win, h_win)):
+                if d_t is not None:
+                    d_t.copy_(h_t, non_blocking=True)
             step()
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
@@ -352,7 +370,8 @@ def run_gpu(args):
     total_s = max_over_ranks(sum(step_ms) / 1e3, ws_, dev)
     value = w.sum_q * K * ws_ / total_s                 # all replicas' tokens over the slowest replica's time
     e2e_value = replica_throughput(w.sum_q * K, sum(e2e_ms) / 1e3, ws_, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_seq, h_lens, h_cum) if t is not None)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_seq, h_lens, h_cum, h_bt, h_hca, h_win)
+              if t is not None)
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
     hbm_gbs, bf16_tf, peak_src = peaks()
@@ -405,7 +424,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
+                    help="workload (3 = FP8 decode, 128 tokens, H=128; 6 = the same with page-table "
+                         "compressed segments)")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     ap.add_argument("--num-splits", type=int, default=0, help="0 = the planner's choice")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle timing")

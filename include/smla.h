@@ -18,7 +18,11 @@
  * j < clamp(sparse_topk_lens[t], 0, W) whose index is not -1 and, for SWA
  * columns, j < min(128, pos + 1) where pos = seq_lens[b] - q_len_b + i is the
  * right-aligned position of token i of request b (msa_sparse_decode_attention
- * page, description).  A token with no slot gets O = 0 and LSE2 = -inf.
+ * page, description), or j < clamp(swa_topk_lens[t], 0, 128) when per-row
+ * window lengths are given.  A token with no slot gets O = 0 and LSE2 = -inf.
+ *
+ * The compressed columns come either from the index table (index form) or
+ * from per-token page tables (page-table form, see comp_block_tables below).
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers on the current CUDA device unless
@@ -40,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 1
+#define SMLA_ABI_VERSION 2
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -128,6 +132,32 @@ typedef struct smla_args {
    * programmatic dependent of the split kernel).  For profiling. */
   void* profile_event_begin;
   void* profile_event_end;
+
+  /* Page-table form of the compressed segment (trtllm_batch_decode_sparse_mla_dsv4
+   * page, Parameters: hca_compressed_block_tables, hca_seq_lens,
+   * hca_sparse_indices_format).  With comp_block_tables != NULL the index
+   * table holds only the 128 SWA columns (indices_row_stride >= 128, default
+   * 128) and compressed slot c of token t -- logical column 128 + c, c < W - 128
+   * -- is row  comp_block_tables[t * block_table_stride + c / comp_page_size]
+   * * comp_page_size + c % comp_page_size  of compressed_kv.  Request b backs
+   * hca_seq_lens[b] - 128 compressed slots (the count includes the 128 window
+   * slots); slots past it are never read and their table entries may hold
+   * anything; sparse_topk_lens (logical columns) may cut further.  Requires
+   * W - 128 <= comp_max_pages * comp_page_size.  A row at or past comp_rows
+   * is treated as masked and flagged with SMLA_DEVERR_INDEX_OUT_OF_RANGE.
+   * Runs of consecutive rows (pages of a multiple of 64 rows) are loaded
+   * with whole-tile copies instead of row gathers. */
+  const int32_t* comp_block_tables; /* [T, comp_max_pages] int32 page IDs, or NULL = index form */
+  int64_t block_table_stride;       /* row stride in elements [comp_max_pages] */
+  int32_t comp_max_pages;           /* page-table columns >= 1 */
+  int32_t comp_page_size;           /* rows per compressed page >= 1 */
+  const int32_t* hca_seq_lens;      /* [B] int32, required with comp_block_tables */
+
+  /* Per-row visible sliding-window lengths (same page, Parameters:
+   * swa_topk_lens), either form: SWA column j of token t is visible iff
+   * j < clamp(swa_topk_lens[t], 0, 128); replaces the seq_lens rule.
+   * NULL = the seq_lens rule. */
+  const int32_t* swa_topk_lens;
 } smla_args;
 
 /* The resolved launch plan (shape-based: it never reads device memory). */

@@ -49,6 +49,9 @@ class SmlaArgs(ctypes.Structure):
         ("num_splits", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("error_word", _c_void_p),
         ("profile_event_begin", _c_void_p), ("profile_event_end", _c_void_p),
+        ("comp_block_tables", _c_void_p), ("block_table_stride", ctypes.c_int64),
+        ("comp_max_pages", ctypes.c_int32), ("comp_page_size", ctypes.c_int32),
+        ("hca_seq_lens", _c_void_p), ("swa_topk_lens", _c_void_p),
     ]
 
 
@@ -183,17 +186,28 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
               out_lse: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None,
               num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
-              error_word: Optional[torch.Tensor] = None) -> SmlaArgs:
+              error_word: Optional[torch.Tensor] = None,
+              swa_topk_lens: Optional[torch.Tensor] = None,
+              comp_block_tables: Optional[torch.Tensor] = None,
+              comp_page_size: int = 0, hca_seq_lens: Optional[torch.Tensor] = None,
+              width: Optional[int] = None) -> SmlaArgs:
     """Fill ``smla_args`` from tensors (no copies; wrong layouts raise).  Every
     tensor must live on the CUDA device of ``q`` (the library reads raw device
     pointers; a host pointer would fault the GPU), and the call must then be
-    made with that device current (``sparse_mla_decode`` does both)."""
+    made with that device current (``sparse_mla_decode`` does both).
+
+    Page-table form: ``comp_block_tables`` ``[T, max_pages]`` int32 page IDs,
+    ``comp_page_size`` rows per page and ``hca_seq_lens`` ``[B]``; the index
+    table then holds the 128 SWA columns and ``width`` (logical columns)
+    defaults to ``128 + max_pages * comp_page_size``."""
     dev = q.device
     for name, t in (("q", q), ("swa_kv", swa_kv), ("compressed_kv", compressed_kv),
                     ("sparse_indices", sparse_indices), ("seq_lens", seq_lens), ("out", out),
                     ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
                     ("sinks", sinks), ("out_lse", out_lse), ("workspace", workspace),
-                    ("error_word", error_word), ("bmm1_scale", bmm1_scale), ("bmm2_scale", bmm2_scale)):
+                    ("error_word", error_word), ("bmm1_scale", bmm1_scale), ("bmm2_scale", bmm2_scale),
+                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
+                    ("hca_seq_lens", hca_seq_lens)):
         if isinstance(t, torch.Tensor) and (t.device.type != "cuda" or t.device != dev):
             raise ValueError(f"{name} is on {t.device}; every tensor must be on the CUDA device of q ({dev})")
     if dev.type != "cuda":
@@ -209,9 +223,15 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
                                 or out_lse.numel() != T * H):
         raise ValueError("out_lse must be a contiguous float32 tensor of T*H elements")
     for name, t in (("sparse_indices", sparse_indices), ("seq_lens", seq_lens),
-                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q)):
+                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
+                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
+                    ("hca_seq_lens", hca_seq_lens)):
         if t is not None and t.dtype != torch.int32:
             raise TypeError(f"{name} must be int32")
+    for name, t in (("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
+                    ("swa_topk_lens", swa_topk_lens), ("hca_seq_lens", hca_seq_lens)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
     if sparse_indices.dim() == 3:          # [T, 1, W]
         sparse_indices = sparse_indices[:, 0, :]
     if sparse_indices.stride(-1) != 1:
@@ -220,6 +240,18 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     comp_rows, comp_stride = _rows_and_stride(compressed_kv)
     a = SmlaArgs()
     a.sum_q, a.num_heads, a.width = T, H, sparse_indices.shape[-1]
+    if comp_block_tables is not None:
+        if comp_block_tables.dim() != 2 or comp_block_tables.stride(-1) != 1 or comp_block_tables.shape[0] != T:
+            raise ValueError("comp_block_tables must be [T, max_pages] with a contiguous last dim")
+        if hca_seq_lens is None or comp_page_size < 1:
+            raise ValueError("the page-table form needs hca_seq_lens and comp_page_size >= 1")
+        a.comp_block_tables, a.block_table_stride = comp_block_tables.data_ptr(), comp_block_tables.stride(0)
+        a.comp_max_pages, a.comp_page_size = comp_block_tables.shape[1], int(comp_page_size)
+        a.hca_seq_lens = hca_seq_lens.data_ptr()
+        a.width = SWA_COLS + a.comp_max_pages * a.comp_page_size if width is None else int(width)
+    elif width is not None and width != a.width:
+        raise ValueError("width is the index table's width in the index form")
+    a.swa_topk_lens = _ptr(swa_topk_lens)
     a.batch = seq_lens.numel()
     a.dtype = _dtype_code(q)
     if _dtype_code(swa_kv) != a.dtype or _dtype_code(compressed_kv) != a.dtype:
@@ -259,8 +291,21 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
                       out_lse: Optional[torch.Tensor] = None,
                       num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
                       error_word: Optional[torch.Tensor] = None,
-                      stream: Optional[int] = None):
-    """Decode; returns ``(out, out_lse)``.  ``out`` / ``out_lse`` are allocated when not given."""
+                      stream: Optional[int] = None,
+                      swa_topk_lens: Optional[torch.Tensor] = None,
+                      hca_compressed_block_tables: Optional[torch.Tensor] = None,
+                      hca_seq_lens: Optional[torch.Tensor] = None,
+                      comp_page_size: Optional[int] = None,
+                      width: Optional[int] = None):
+    """Decode; returns ``(out, out_lse)``.  ``out`` / ``out_lse`` are allocated when not given.
+
+    With ``hca_compressed_block_tables`` the compressed segment is given as
+    page tables; ``comp_page_size`` defaults to the compressed cache view's
+    rows per page (``[num_pages, page_size, 512]``)."""
+    if hca_compressed_block_tables is not None and comp_page_size is None:
+        if compressed_kv_cache.dim() < 3:
+            raise ValueError("pass comp_page_size, or a compressed cache view [num_pages, page_size, 512]")
+        comp_page_size = compressed_kv_cache.shape[-2]
     T = query.shape[0] if query.dim() == 3 else query.shape[0] * query.shape[1]
     H = query.shape[-2]
     if out is None:
@@ -272,18 +317,23 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
                      sparse_topk_lens=sparse_topk_lens, cum_seq_lens_q=cum_seq_lens_q,
                      sinks=sinks, bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
                      out_lse=out_lse, workspace=workspace_buffer, num_splits=num_splits,
-                     max_splits=max_splits, kernel=kernel, error_word=error_word)
+                     max_splits=max_splits, kernel=kernel, error_word=error_word,
+                     swa_topk_lens=swa_topk_lens, comp_block_tables=hca_compressed_block_tables,
+                     comp_page_size=comp_page_size or 0, hca_seq_lens=hca_seq_lens, width=width)
     with torch.cuda.device(query.device):   # the library plans and launches on the current device
         smla_decode(args, stream)
     return out, out_lse
 
 
 def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=0,
-                   kernel=KERNEL_AUTO, cum_seq_lens_q=None, device: int = 0) -> int:
-    """Workspace bytes for a call with these shapes (no device memory is read)."""
+                   kernel=KERNEL_AUTO, cum_seq_lens_q=None, device: int = 0,
+                   width: Optional[int] = None) -> int:
+    """Workspace bytes for a call with these shapes (no device memory is read);
+    ``width`` = logical columns in the page-table form."""
     a = SmlaArgs()
     q3 = query if query.dim() == 3 else query.reshape(-1, query.shape[2], query.shape[3])
-    a.sum_q, a.num_heads, a.width = q3.shape[0], q3.shape[1], sparse_indices.shape[-1]
+    a.sum_q, a.num_heads = q3.shape[0], q3.shape[1]
+    a.width = sparse_indices.shape[-1] if width is None else int(width)
     a.batch, a.dtype = seq_lens.numel(), _dtype_code(q3)
     a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
     a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel

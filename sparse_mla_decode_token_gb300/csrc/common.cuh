@@ -43,6 +43,12 @@ struct DecodeParams {
   float* part_o;     // [T, H, S, 512] fp32 normalised split partials (S > 1)
   float* part_lse;   // [T, H, S] fp32 base-2 LSE of each partial (S > 1)
   int32_t* err;
+  // page-table form of the compressed segment (bt == nullptr: index form)
+  const int32_t* bt;       // [T, max_pages] page IDs
+  int64_t bt_stride;
+  int32_t page_size;
+  const int32_t* hca;      // [B] window + compressed slots backing each request
+  const int32_t* swa_lens; // [T] visible window per token, or nullptr (seq_lens rule)
 };
 
 struct TokenInfo {
@@ -51,8 +57,10 @@ struct TokenInfo {
 
 // Step a1: request b(t) (binary search of cum_seq_lens_q, or t / q_len when
 // the query is dense), right-aligned position pos = seq_len - q_len + i, SWA
-// window w_swa = min(128, max(0, pos + 1)) and active columns
-// n_lim = clamp(sparse_topk_lens[t], 0, W).
+// window w_swa = min(128, max(0, pos + 1)) (or clamp(swa_topk_lens[t], 0, 128)
+// when per-row window lengths are given) and active columns
+// n_lim = clamp(sparse_topk_lens[t], 0, W), in the page-table form further
+// capped at max(128, hca_seq_lens[b]) (the request's backed slots).
 __device__ __forceinline__ TokenInfo token_info(const DecodeParams& p, int t) {
   TokenInfo ti;
   if (p.cum != nullptr) {
@@ -70,10 +78,20 @@ __device__ __forceinline__ TokenInfo token_info(const DecodeParams& p, int t) {
     ti.i = t - ti.b * ti.q_len;
   }
   ti.pos = __ldg(p.seq_lens + ti.b) - ti.q_len + ti.i;
-  ti.w_swa = min(kSwaCols, max(0, ti.pos + 1));
+  const int visible = p.swa_lens ? __ldg(p.swa_lens + t) : ti.pos + 1;
+  ti.w_swa = min(kSwaCols, max(0, visible));
   int n = p.topk ? __ldg(p.topk + t) : p.W;
   ti.n_lim = min(max(n, 0), p.W);
+  if (p.bt) ti.n_lim = min(ti.n_lim, max(kSwaCols, __ldg(p.hca + ti.b)));
   return ti;
+}
+
+// Page-table form: row of compressed slot c of token t (c < W - 128, so the
+// table column is in range), or -2 when that row lies outside the pool.
+__device__ __forceinline__ int paged_row(const DecodeParams& p, int t, int c) {
+  const int64_t page = __ldg(p.bt + (int64_t)t * p.bt_stride + c / p.page_size);
+  const int64_t row = page * p.page_size + c % p.page_size;
+  return (row >= 0 && row < p.comp_rows) ? (int)row : -2;
 }
 
 // Step a2 for one column: returns the element offset of the selected row in
@@ -82,9 +100,9 @@ __device__ __forceinline__ TokenInfo token_info(const DecodeParams& p, int t) {
 __device__ __forceinline__ int64_t slot_row_offset(const DecodeParams& p, const TokenInfo& ti,
                                                    int t, int j, bool* from_swa) {
   if (j >= ti.n_lim) return -1;
-  int idx = __ldg(p.ind + (int64_t)t * p.ind_stride + j);
-  if (idx == -1) return -1;
   bool swa = j < kSwaCols;
+  int idx = (!swa && p.bt) ? paged_row(p, t, j - kSwaCols) : __ldg(p.ind + (int64_t)t * p.ind_stride + j);
+  if (idx == -1) return -1;
   *from_swa = swa;
   if (swa && j >= ti.w_swa) return -1;
   int64_t rows = swa ? p.swa_rows : p.comp_rows;

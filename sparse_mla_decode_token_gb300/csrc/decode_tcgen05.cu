@@ -48,6 +48,7 @@
 // waits on an unbounded hardware barrier inside its loop.
 #include <cuda.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -77,6 +78,7 @@ constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
 constexpr uint32_t kSCol = 256;      // S: three buffers of N fp32 columns, then P: two buffers of 16 columns
 constexpr int kSBufs = 3;
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
+constexpr int kExactRefTiles = 8;          // E4M3 P: chains of at most this many tiles follow the exact maximum
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxStages = 8;
 
@@ -133,12 +135,15 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Kernel parameters: the shared decode parameters plus one TMA descriptor per
-// KV pool ([rows, 512] with the pool's row stride; box = 128 bytes x 1 row;
-// 128-byte swizzle), as required by tile::gather4.
+// Kernel parameters: the shared decode parameters plus two TMA descriptors per
+// KV pool ([rows, 512] with the pool's row stride; 128-byte swizzle): box =
+// 128 bytes x 1 row for tile::gather4, and 128 bytes x N rows for whole-tile
+// copies of N consecutive rows.
 struct TcParams {
   CUtensorMap tm_swa;
   CUtensorMap tm_comp;
+  CUtensorMap tm_swa_run;
+  CUtensorMap tm_comp_run;
   DecodeParams p;
 };
 
@@ -219,8 +224,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   const int t = unit / S;
   const int H = p.H;
   // Column range of this split, from the table width only (so that the index
-  // loads need not wait for any device value): [c0, c0 + ceil(W / S)).
-  const int per_split = (p.W + S - 1) / S;
+  // loads need not wait for any device value): [c0, c0 + ceil(W / S)); in the
+  // page-table form rounded up to whole 64-slot runs, so that every full tile
+  // of compressed slots lies on one page when pages hold a multiple of 64 rows.
+  int per_split = (p.W + S - 1) / S;
+  if (p.bt) per_split = (per_split + kMaxN - 1) / kMaxN * kMaxN;
   const int c0 = min(p.W, s * per_split);
   int c1 = min(p.W, c0 + per_split);
   if (c1 - c0 > kMaxCols) {           // the planner prevents this; never read past the staging buffer
@@ -245,10 +253,19 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   const int nchunks = (c1 - c0 + 31) / 32;
   const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
   int32_t rv[kChunksPerWarp];
+  if (p.bt == nullptr) {             // index form (a loop of its own: the FP8 code keeps its registers)
 #pragma unroll
-  for (int q = 0; q < kChunksPerWarp; ++q) {
-    const int col = c0 + (warp + q * kWarps) * 32 + lane;
-    rv[q] = (col < c1) ? __ldg(irow + col) : -1;
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (warp + q * kWarps) * 32 + lane;
+      rv[q] = (col < c1) ? __ldg(irow + col) : -1;
+    }
+  } else {                           // page-table form: compressed rows from the page table
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (warp + q * kWarps) * 32 + lane;
+      rv[q] = -1;
+      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
+    }
   }
   const TokenInfo ti = token_info(p, t);
   c1 = min(c1, max(c0, ti.n_lim));    // active columns of the split
@@ -379,10 +396,14 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // group; two groups take alternate tiles (measured: one group of six
     // sharing every tile reaches ~15 GB/s per SM from HBM, warps owning whole
     // tiles ~24 GB/s but with a long issue time per tile; two groups of three
-    // were fastest in the full kernel).
+    // were fastest in the full kernel).  A full tile of N consecutive rows (a
+    // page run of the page-table form, or a run in the index table) is one
+    // box copy per 128-byte column block instead.
     if (tid == 0) {
       prefetch_tensormap(&P.tm_swa);
       prefetch_tensormap(&P.tm_comp);
+      prefetch_tensormap(&P.tm_swa_run);
+      prefetch_tensormap(&P.tm_comp_run);
     }
     // Producer group pg (kWarpsPerGroup warps) gathers tiles pg, pg + kProducerGroups, ...
     constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
@@ -393,15 +414,31 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       const int start = tile_start(j), n = tile_n(j);
       const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
       if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
-      const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
       const uint32_t stage = kv_addr + st * C::kStageBytes;
       const int32_t* rows = idx_s + start;
-      const int groups = (n4 / 4) * C::kRegions;
-      for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
-        const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
-        tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
-                    rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
-                    bar(sm.kv_full[st]));
+      bool run = false;                      // rows[r] == rows[0] + r for every r < N
+      if (n == kN) {
+        const uint32_t r0 = (uint32_t)rows[0];
+        bool ok = true;
+#pragma unroll
+        for (int r = lane; r < kN; r += 32) ok = ok && (uint32_t)rows[r] == r0 + (uint32_t)r;
+        run = __all_sync(0xffffffffu, ok);
+      }
+      if (run) {
+        // every row of the box was checked against the pool's row count in the set-up
+        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa_run) : static_cast<const void*>(&P.tm_comp_run);
+        if (pw == 0 && lane < C::kRegions)
+          tma_load_2d(stage + lane * C::kRegionKV, tmap, (int)rank * kHalfDims + lane * (128 / C::kElem), rows[0],
+                      bar(sm.kv_full[st]));
+      } else {
+        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
+        const int groups = (n4 / 4) * C::kRegions;
+        for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
+          const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
+          tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
+                      rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
+                      bar(sm.kv_full[st]));
+        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -512,6 +549,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     };
 
     float m_last = -INFINITY, l_run = 0.f;            // reference and row sum of my warpgroup's tiles
+    // E4M3 P keeps 3 mantissa bits: under a lagging reference a row's largest P
+    // (up to 2^8) is rounded by up to 1/16, which shows when few slots carry the
+    // mass, so short tile chains move the reference on every new maximum (the
+    // same choice in both CTAs: ntiles is the pair's).
+    const float thr = (kFp8 && ntiles <= kExactRefTiles) ? 0.f : kRescaleThreshold;
     bool ok = true;
     if (g < ntiles) ok = push(g);
     int j = g;
@@ -568,7 +610,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         if (!(ok = warp_wait(cx, bar(sm.m_ready[g ^ 1]), ((j - 1) >> 1) & 1))) break;
         m_prev = sm.m_buf[g ^ 1][h];
       }
-      const float m_cur = (mt > m_prev + kRescaleThreshold) ? mt : m_prev;
+      const float m_cur = (mt > m_prev + thr) ? mt : m_prev;
       sm.m_buf[g][h] = m_cur;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
@@ -774,15 +816,16 @@ cudaError_t encode_fn(EncodeTiledFn* out) {
   return cudaSuccess;
 }
 
-// [rows, 512] pool view; box 128 bytes x 1 row; 128-byte swizzle.
-cudaError_t encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_stride, int dtype) {
+// [rows, 512] pool view; box 128 bytes x box_rows rows; 128-byte swizzle.
+cudaError_t encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_stride, int dtype,
+                            int box_rows) {
   EncodeTiledFn fn = nullptr;
   cudaError_t e = encode_fn(&fn);
   if (e != cudaSuccess) return e;
   const int elem = dtype == SMLA_BF16 ? 2 : 1;
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(rows > 0 ? rows : 1)};
   const cuuint64_t strides[1] = {(cuuint64_t)(row_stride * elem)};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), 1};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dtype == SMLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -799,9 +842,14 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
   TcParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
-  cudaError_t e = encode_pool_map(&P.tm_swa, p.swa, p.swa_rows, p.swa_stride, p.dtype);
-  if (e != cudaSuccess) return e;
-  e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype);
+  // a pool of fewer than N rows holds no run of N rows: its run map is never used
+  const int64_t run_rows = p.dtype == SMLA_BF16 ? Cfg<false>::kN : Cfg<true>::kN;
+  const int swa_run = (int)std::max<int64_t>(1, std::min(run_rows, p.swa_rows));
+  const int comp_run = (int)std::max<int64_t>(1, std::min(run_rows, p.comp_rows));
+  cudaError_t e = encode_pool_map(&P.tm_swa, p.swa, p.swa_rows, p.swa_stride, p.dtype, 1);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype, 1);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_swa_run, p.swa, p.swa_rows, p.swa_stride, p.dtype, swa_run);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp_run, p.comp, p.comp_rows, p.comp_stride, p.dtype, comp_run);
   if (e != cudaSuccess) return e;
   const int smem = tc_smem_bytes(p.dtype);
   auto launch = [&](auto kernel) -> cudaError_t {

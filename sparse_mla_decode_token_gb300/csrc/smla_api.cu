@@ -72,9 +72,24 @@ smla_status check_shapes(const smla_args* a) {
   if (ss < kHeadDim || (ss * eb) % 16 != 0 || cs < kHeadDim || (cs * eb) % 16 != 0)
     return fail(SMLA_ERR_INVALID_ARG, "pool row strides (%lld, %lld) must be >= 512 and multiples of 16 bytes",
                 (long long)ss, (long long)cs);
-  const int64_t is = a->indices_row_stride ? a->indices_row_stride : a->width;
-  if (is < a->width)
-    return fail(SMLA_ERR_INVALID_ARG, "indices_row_stride %lld < width %d", (long long)is, a->width);
+  const int index_cols = a->comp_block_tables ? kSwaCols : a->width;   // columns the index table holds
+  const int64_t is = a->indices_row_stride ? a->indices_row_stride : index_cols;
+  if (is < index_cols)
+    return fail(SMLA_ERR_INVALID_ARG, "indices_row_stride %lld < %d index columns", (long long)is, index_cols);
+  if (a->comp_block_tables) {
+    if (a->comp_page_size < 1 || a->comp_max_pages < 1)
+      return fail(SMLA_ERR_INVALID_ARG, "comp_page_size %d and comp_max_pages %d must be >= 1",
+                  a->comp_page_size, a->comp_max_pages);
+    const int64_t bts = a->block_table_stride ? a->block_table_stride : a->comp_max_pages;
+    if (bts < a->comp_max_pages)
+      return fail(SMLA_ERR_INVALID_ARG, "block_table_stride %lld < comp_max_pages %d", (long long)bts,
+                  a->comp_max_pages);
+    if ((int64_t)(a->width - kSwaCols) > (int64_t)a->comp_max_pages * a->comp_page_size)
+      return fail(SMLA_ERR_INVALID_ARG, "width %d: %d compressed columns exceed comp_max_pages * comp_page_size = %lld",
+                  a->width, a->width - kSwaCols, (long long)a->comp_max_pages * a->comp_page_size);
+    if (a->comp_rows > 0x7fffffffLL)
+      return fail(SMLA_ERR_UNSUPPORTED, "comp_rows %lld: page-table rows must fit in int32", (long long)a->comp_rows);
+  }
   return SMLA_OK;
 }
 
@@ -195,6 +210,11 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   if (a->sum_q == 0) return SMLA_OK;
   if (!a->q || !a->swa_kv || !a->compressed_kv || !a->sparse_indices || !a->seq_lens || !a->out)
     return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv, sparse_indices, seq_lens and out are required");
+  if (a->comp_block_tables && !a->hca_seq_lens)
+    return fail(SMLA_ERR_INVALID_ARG, "hca_seq_lens is required with comp_block_tables");
+  if ((a->comp_block_tables && !aligned(a->comp_block_tables, 4)) || (a->hca_seq_lens && !aligned(a->hca_seq_lens, 4)) ||
+      (a->swa_topk_lens && !aligned(a->swa_topk_lens, 4)))
+    return fail(SMLA_ERR_INVALID_ARG, "comp_block_tables, hca_seq_lens and swa_topk_lens must be 4-byte aligned");
   if (!aligned(a->q, 16) || !aligned(a->swa_kv, 16) || !aligned(a->compressed_kv, 16) || !aligned(a->out, 16))
     return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv and out must be 16-byte aligned");
   if (!aligned(a->sparse_indices, 4) || (a->out_lse && !aligned(a->out_lse, 4)))
@@ -223,7 +243,14 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   p.comp_rows = a->comp_rows;
   p.comp_stride = a->comp_row_stride ? a->comp_row_stride : kHeadDim;
   p.ind = a->sparse_indices;
-  p.ind_stride = a->indices_row_stride ? a->indices_row_stride : a->width;
+  p.ind_stride = a->indices_row_stride ? a->indices_row_stride : (a->comp_block_tables ? kSwaCols : a->width);
+  if (a->comp_block_tables) {
+    p.bt = a->comp_block_tables;
+    p.bt_stride = a->block_table_stride ? a->block_table_stride : a->comp_max_pages;
+    p.page_size = a->comp_page_size;
+    p.hca = a->hca_seq_lens;
+  }
+  p.swa_lens = a->swa_topk_lens;
   p.topk = a->sparse_topk_lens;
   p.seq_lens = a->seq_lens;
   p.cum = a->cum_seq_lens_q;

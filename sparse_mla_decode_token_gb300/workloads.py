@@ -305,11 +305,13 @@ CONFIG_NAMES = {
     3: "fp8_decode_b128_h128",
     4: "varlen_spec_bf16_h64",
     5: "long_splitk_fp8_b4_h128",
+    6: "paged_fp8_b128_h128",
 }
 
 
 def config_workload(n: int) -> Workload:
-    """Workload ``n`` (1..5); seed 1000 + n."""
+    """Workload ``n`` (1..6); seed 1000 + n.  Workload 6 is workload 3's shape
+    with the compressed segment given as page tables."""
     seed = 1000 + n
     rng = np.random.default_rng(seed + 7919)
     if n == 1:
@@ -351,5 +353,13 @@ def config_workload(n: int) -> Workload:
                              comp_rows=1 << 20, width=128 + 16384,
                              seq_lens=1 << 20, ring_len=128, topk_lens=128 + 16384,
                              sinks=True)
+    if n == 6:
+        # 128 tokens, H=128, FP8 E4M3; 128 SWA + 2048 compressed slots per token on
+        # 16 pages of 128 rows (each request its own random pages of a 262,144-row pool).
+        return make_paged_workload(name=CONFIG_NAMES[6], seed=seed, dtype="e4m3", batch=128,
+                                   q_lens=1, num_heads=128, swa_rows=128 * 128, comp_pages=2048,
+                                   page_size=128, max_pages=16, hca_seq_lens=128 + 2048,
+                                   seq_lens=rng.integers(8192, 65537, size=128), ring_len=128,
+                                   topk_lens=2176)
     raise ValueError(f"no workload {n}")
 

@@ -26,6 +26,9 @@ def device_inputs(w, device="cuda"):
         q=kv(w.q), swa=kv(w.swa_kv), comp=kv(w.comp_kv), indices=i32(w.indices),
         topk_lens=i32(w.topk_lens), seq_lens=i32(w.seq_lens), cum=i32(w.cum_seq_lens_q),
         sinks=None if w.sinks is None else torch.from_numpy(w.sinks).to(device),
+        swa_topk_lens=i32(getattr(w, "swa_topk_lens", None)),
+        block_tables=i32(getattr(w, "comp_block_tables", None)),
+        hca_seq_lens=i32(getattr(w, "hca_seq_lens", None)),
     )
 
 
@@ -55,7 +58,10 @@ def run_gpu(w, d=None, *, num_splits=0, max_splits=0, kernel=B.KERNEL_AUTO, bmm_
                        sparse_indices=d["indices"], seq_lens=d["seq_lens"], out=out,
                        sparse_topk_lens=d["topk_lens"], cum_seq_lens_q=d["cum"], sinks=d["sinks"],
                        bmm1_scale=bmm1, bmm2_scale=bmm2, out_lse=lse, num_splits=num_splits,
-                       max_splits=max_splits, kernel=kernel, error_word=error_word)
+                       max_splits=max_splits, kernel=kernel, error_word=error_word,
+                       swa_topk_lens=d.get("swa_topk_lens"), comp_block_tables=d.get("block_tables"),
+                       comp_page_size=getattr(w, "comp_page_size", 0), hca_seq_lens=d.get("hca_seq_lens"),
+                       width=w.width if getattr(w, "comp_block_tables", None) is not None else None)
     plan = B.smla_plan_decode(args, torch.cuda.current_device()) if T > 0 else None
     ws = None
     if plan is not None and plan.workspace_bytes:

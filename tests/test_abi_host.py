@@ -33,7 +33,7 @@ def test_library_exports_every_declared_function(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(B.EXPORTS)
-    assert B.smla_abi_version() == 1
+    assert B.smla_abi_version() == 2
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -98,6 +98,40 @@ def test_host_argument_errors(lib, mutate, code, needle):
     mutate(a)
     assert status(lib, a) == code
     assert needle in B.smla_last_error()
+
+
+def paged_args():
+    """Page-table form: 4 pages of 128 rows cover the 512 compressed columns of
+    width 640; the pointers are markers only (host checks never read them)."""
+    a = good_args()
+    a.comp_block_tables, a.comp_max_pages, a.comp_page_size = 64, 4, 128
+    a.hca_seq_lens = 64
+    return a
+
+
+@pytest.mark.parametrize("mutate,code,needle", [
+    (lambda a: setattr(a, "comp_page_size", 0), B.SMLA_ERR_INVALID_ARG, "comp_page_size"),
+    (lambda a: setattr(a, "comp_max_pages", 3), B.SMLA_ERR_INVALID_ARG, "exceed"),
+    (lambda a: setattr(a, "block_table_stride", 2), B.SMLA_ERR_INVALID_ARG, "block_table_stride"),
+    (lambda a: setattr(a, "indices_row_stride", 100), B.SMLA_ERR_INVALID_ARG, "indices_row_stride"),
+    (lambda a: setattr(a, "comp_rows", 1 << 31), B.SMLA_ERR_UNSUPPORTED, "int32"),
+])
+def test_page_table_argument_errors(lib, mutate, code, needle):
+    a = paged_args()
+    mutate(a)
+    assert status(lib, a) == code
+    assert needle in B.smla_last_error()
+
+
+def test_page_table_index_table_holds_swa_columns_only(lib):
+    a = paged_args()
+    a.sum_q = 0
+    a.indices_row_stride = 128                     # the index form would need >= width (640)
+    assert status(lib, a) == B.SMLA_OK
+    b = good_args()
+    b.sum_q = 0
+    b.indices_row_stride = 128
+    assert status(lib, b) == B.SMLA_ERR_INVALID_ARG
 
 
 def test_null_args_and_empty_batch(lib):
