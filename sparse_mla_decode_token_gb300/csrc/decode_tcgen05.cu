@@ -25,7 +25,8 @@
 //   softmax warps 8-15  two warpgroups taking whole tiles in turn (warpgroup
 //                       g takes tiles j with j % 2 == g), one thread per head:
 //                       read S_r from TMEM, push it to the peer CTA with
-//                       st.async (completing bytes on the peer's mbarrier), add
+//                       st.async (completing bytes on the peer's mbarrier) as
+//                       24-bit floats (four values in three words), add
 //                       the peer's partial (S = S_0 + S_1, identical in both
 //                       CTAs), settle the running reference maximum m(j) from
 //                       m(j-1) (handed over by the other warpgroup through
@@ -108,7 +109,7 @@ struct Cfg {
   static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
   static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
   static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
-  static constexpr int kStages = 6;
+  static constexpr int kStages = kFp8 ? 7 : 6;                 // KV ring (FP8: the smaller exchange buffers make room for a 7th)
   static constexpr int kKStep = 32 / kElem;                    // MMA K per instruction
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
   static constexpr int kK2 = kN / kKStep;                      // PV K steps
@@ -118,7 +119,10 @@ struct Cfg {
   static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
   static constexpr int kQBytes = kRegions * kRegionQ;
   static constexpr int kStageBytes = kRegions * kRegionKV;
-  static constexpr int kXBytes = 128 * kN * 4;                 // one exchange buffer (fp32 S rows)
+  // one exchange buffer: 128 rows of N 24-bit logits (BF16 keeps 4 bytes per
+  // logit of room: its split-partial epilogue stages 128 KB over the KV ring
+  // and the exchange buffers)
+  static constexpr int kXBytes = 128 * kN * (kFp8 ? 3 : 4);
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffX = kOffKV + kStages * kStageBytes;
@@ -509,7 +513,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     const bool leader = (warp - kSoftmaxWarp0) % 4 == 0 && lane == 0;   // one thread per warpgroup
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
-    const uint32_t xbytes = (uint32_t)(H * kN * 4);    // bytes the peer pushes per tile
+    const uint32_t xbytes = (uint32_t)(H * kN * 3);    // bytes the peer pushes per tile (24-bit logits)
     constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
     const uint32_t x_mine = x_addr + g * C::kXBytes;
     const uint32_t x_peer = map_to_rank(x_mine, peer);
@@ -538,10 +542,20 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           uint32_t v[16];
           tmem_ld16(tl + kSCol + sb * kN + hb * 16, v);
           tmem_wait_ld();
+          // 24-bit logits: the low mantissa byte is dropped after rounding;
+          // values a, b, c, d travel as [a1 a2 a3 d1] [b1 b2 b3 d2] [c1 c2 c3 d3]
+          uint32_t w[12];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_async_v4(xb + (uint32_t)((hb * 4 + q) * 128 * 16), __uint_as_float(v[4 * q]),
-                        __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]),
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint32_t d = v[4 * gq + 3] + 0x80u;
+            w[3 * gq] = __byte_perm(v[4 * gq] + 0x80u, d, 0x5321);
+            w[3 * gq + 1] = __byte_perm(v[4 * gq + 1] + 0x80u, d, 0x6321);
+            w[3 * gq + 2] = __byte_perm(v[4 * gq + 2] + 0x80u, d, 0x7321);
+          }
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            st_async_v4(xb + (uint32_t)((hb * 3 + q) * 128 * 16), __uint_as_float(w[4 * q]),
+                        __uint_as_float(w[4 * q + 1]), __uint_as_float(w[4 * q + 2]), __uint_as_float(w[4 * q + 3]),
                         xin_full_peer);
         }
       }
@@ -577,14 +591,27 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       float mt = -INFINITY;
       if (active) {
         tmem_wait_ld();
-        const float4* xp = reinterpret_cast<const float4*>(base + C::kOffX + g * C::kXBytes) + h;
+        const uint4* xp = reinterpret_cast<const uint4*>(base + C::kOffX + g * C::kXBytes) + h;
 #pragma unroll
-        for (int q = 0; q < kN / 4; ++q) {
-          const float4 x = xp[q * 128];
-          f2_unpack(f2_mul(f2_add(f2_pack(sv[4 * q], sv[4 * q + 1]), f2_pack(x.x, x.y)), c2), sv[4 * q],
-                    sv[4 * q + 1]);
-          f2_unpack(f2_mul(f2_add(f2_pack(sv[4 * q + 2], sv[4 * q + 3]), f2_pack(x.z, x.w)), c2), sv[4 * q + 2],
-                    sv[4 * q + 3]);
+        for (int hb = 0; hb < kN / 16; ++hb) {
+          uint32_t w[12];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const uint4 x = xp[(hb * 3 + q) * 128];
+            w[4 * q] = x.x;
+            w[4 * q + 1] = x.y;
+            w[4 * q + 2] = x.z;
+            w[4 * q + 3] = x.w;
+          }
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint32_t w0 = w[3 * gq], w1 = w[3 * gq + 1], w2 = w[3 * gq + 2];
+            const float pa = __uint_as_float(w0 << 8), pb = __uint_as_float(w1 << 8), pc = __uint_as_float(w2 << 8);
+            const float pd = __uint_as_float(__byte_perm(__byte_perm(w0, w1, 0x7373), w2, 0x7103));
+            const int i = hb * 16 + 4 * gq;
+            f2_unpack(f2_mul(f2_add(f2_pack(sv[i], sv[i + 1]), f2_pack(pa, pb)), c2), sv[i], sv[i + 1]);
+            f2_unpack(f2_mul(f2_add(f2_pack(sv[i + 2], sv[i + 3]), f2_pack(pc, pd)), c2), sv[i + 2], sv[i + 3]);
+          }
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (n_cur >= kN) {
