@@ -317,10 +317,65 @@ def run_gpu(args):
     def step():
         B.smla_decode(args_c, sptr)
 
+    # two buffer sets of the per-step tensors for the end-to-end leg
+    per_step = [("q", h_q), ("idx", h_idx), ("seq", h_seq), ("lens", h_lens), ("cum", h_cum),
+                ("bt", h_bt), ("hca", h_hca), ("win", h_win)]
+    e2e_sets = []
+    for _b in range(2):
+        dd = {k_: (None if h_ is None else torch.empty(h_.shape, dtype=h_.dtype, device=dev)) for k_, h_ in per_step}
+        o_b = torch.empty_like(out)
+        l_b = torch.empty_like(lse)
+        a_b = B.make_args(q=dd["q"], swa_kv=d_swa, compressed_kv=d_comp, sparse_indices=dd["idx"],
+                          seq_lens=dd["seq"], out=o_b, sparse_topk_lens=dd["lens"], cum_seq_lens_q=dd["cum"],
+                          sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                          out_lse=l_b, kernel=args.kernel, num_splits=args.num_splits, error_word=err_word,
+                          swa_topk_lens=dd["win"], comp_block_tables=dd["bt"], comp_page_size=w.comp_page_size,
+                          hca_seq_lens=dd["hca"], width=w.width if w.paged else None)
+        a_b.workspace, a_b.workspace_bytes = workspace.data_ptr(), workspace.numel()   # decodes are serial
+        e2e_sets.append(dict(d=dd, out=o_b, lse=l_b, args=a_b,
+                             h_out=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                             h_lse=torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                             ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event()))
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+
+    def e2e_pipelined(steps):
+        """Seconds for `steps` pipelined end-to-end steps, and whether the last
+        step's copied-back output equals the device-resident leg's."""
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(s_in)
+        for k_ in range(steps):
+            st_ = e2e_sets[k_ & 1]
+            if k_ >= 2:
+                s_in.wait_event(st_["ev_done"])           # step k - 2 has read this set's inputs
+            with torch.cuda.stream(s_in):
+                for name_, h_ in per_step:
+                    if h_ is not None:
+                        st_["d"][name_].copy_(h_, non_blocking=True)
+                st_["ev_in"].record(s_in)
+            stream.wait_event(st_["ev_in"])
+            if k_ >= 2:
+                stream.wait_event(st_["ev_out"])          # step k - 2's outputs are copied out
+            B.smla_decode(st_["args"], sptr)
+            st_["ev_done"].record(stream)
+            s_out.wait_event(st_["ev_done"])
+            with torch.cuda.stream(s_out):
+                st_["h_out"].copy_(st_["out"], non_blocking=True)
+                st_["h_lse"].copy_(st_["lse"], non_blocking=True)
+                st_["ev_out"].record(s_out)
+        ev1.record(s_out)
+        torch.cuda.synchronize()
+        last = e2e_sets[(steps - 1) & 1]
+        same = bool(torch.equal(last["h_out"], out.cpu())) and bool(torch.equal(last["h_lse"], lse.cpu()))
+        return ev0.elapsed_time(ev1) / 1e3, same
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
+    e2e_pipelined(max(2, args.warmup))                 # warm the end-to-end path (streams, pinned copies)
 
     K = args.steps
     ev_step = [(new_event(), new_event()) for _ in range(K)]
@@ -345,31 +400,18 @@ def run_gpu(args):
         torch.cuda.synchronize()
         barrier()
         args_c.profile_event_begin = args_c.profile_event_end = None
-        # end-to-end leg: pinned host inputs -> device, decode, outputs -> pinned host
-        ev_e2e = [(new_event(), new_event()) for _ in range(K)]
-        torch.cuda.synchronize()
-        for k in range(K):
-            flush.zero_()
-            ev_e2e[k][0].record(stream)
-            d_q.copy_(h_q, non_blocking=True)
-            d_idx.copy_(h_idx, non_blocking=True)
-            d_seq.copy_(h_seq, non_blocking=True)
-            if d_lens is not None:
-                d_lens.copy_(h_lens, non_blocking=True)
-            for d_t, h_t in ((d_cum, h_cum), (d_bt, h_bt), (d_hca, h_hca), (d_win, h_win)):
-                if d_t is not None:
-                    d_t.copy_(h_t, non_blocking=True)
-            step()
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
-            ev_e2e[k][1].record(stream)
-        torch.cuda.synchronize()
+        # end-to-end leg through the public call: every step copies its inputs
+        # from pinned host memory, decodes and copies out and LSE back to pinned
+        # host memory.  Copies in, decodes and copies out run on three streams
+        # with two buffer sets, so step k's copies overlap the decodes of steps
+        # k - 1 and k + 1 (a serving loop's pipeline); the timed region spans
+        # all K steps, every copy included.
+        e2e_s, e2e_ok = e2e_pipelined(K)
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     main_ms = [a.elapsed_time(b) for a, b in ev_main]
-    e2e_ms = [a.elapsed_time(b) for a, b in ev_e2e]
     total_s = max_over_ranks(sum(step_ms) / 1e3, ws_, dev)
     value = w.sum_q * K * ws_ / total_s                 # all replicas' tokens over the slowest replica's time
-    e2e_value = replica_throughput(w.sum_q * K, sum(e2e_ms) / 1e3, ws_, dev)
+    e2e_value = replica_throughput(w.sum_q * K, e2e_s, ws_, dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_seq, h_lens, h_cum, h_bt, h_hca, h_win)
               if t is not None)
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
@@ -410,7 +452,9 @@ def run_gpu(args):
         "roofline": roof,
         "plan": plan.as_dict(),
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipeline": "copies in, decode and copies out on three streams, two buffer sets",
+                "output_matches_device_leg": e2e_ok},
         "gpu_launches": K * launches_per_step,
         "device_error_word": int(err_word.item()),
         "clocks": clocks.summary(),
