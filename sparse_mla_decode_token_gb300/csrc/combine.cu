@@ -1,6 +1,6 @@
 // Split-K combine: merges S normalised partials of every (token, head).
 //
-// The partial layout [T, H, S, 512] plus [T, H, S] base-2 LSEs follows the
+// The partial layout [T, H, S, 512] (BF16) plus [T, H, S] (fp32) base-2 LSEs follows the
 // split partials of the FlashInfer cake_sparse_mla_sm120_dsv4_nvfp4_decode page
 // (Parameters: mid_out, mid_lse).  With LSE_s the base-2 log-sum-exp of split s:
 //   LSE = log2 sum_s 2^{LSE_s},   O = sum_s 2^{LSE_s - LSE} O_s,
@@ -25,7 +25,7 @@ combine_kernel(const DecodeParams p) {
   if (th >= (int64_t)p.sum_q * p.H) return;
   const int h = (int)(th % p.H);
   const float* lse_s = p.part_lse + th * S;
-  const float4* o_s = reinterpret_cast<const float4*>(p.part_o + th * S * kHeadDim + d);
+  const uint2* o_s = reinterpret_cast<const uint2*>(p.part_o + th * S * kHeadDim + d);   // 4 BF16 dims
   // the split kernel's partials become visible here (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -44,20 +44,22 @@ combine_kernel(const DecodeParams p) {
   if (mx != -INFINITY) {
     for (int s0 = 0; s0 < S; s0 += kBatch) {
       float w[kBatch];
-      float4 o[kBatch];
+      uint2 o[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const bool in = s0 + k < S;
         const float ls = in ? __ldg(lse_s + s0 + k) : -INFINITY;
         w[k] = ls == -INFINITY ? 0.f : fast_exp2(ls - mx);   // an empty split's partial is all zero
-        o[k] = in ? __ldg(o_s + (int64_t)(s0 + k) * (kHeadDim / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[k] = in ? __ldg(o_s + (int64_t)(s0 + k) * (kHeadDim / 4)) : make_uint2(0u, 0u);
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        acc.x = fmaf(w[k], o[k].x, acc.x);
-        acc.y = fmaf(w[k], o[k].y, acc.y);
-        acc.z = fmaf(w[k], o[k].z, acc.z);
-        acc.w = fmaf(w[k], o[k].w, acc.w);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o[k].x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o[k].y));
+        acc.x = fmaf(w[k], a.x, acc.x);
+        acc.y = fmaf(w[k], a.y, acc.y);
+        acc.z = fmaf(w[k], b.x, acc.z);
+        acc.w = fmaf(w[k], b.y, acc.w);
         wsum += w[k];
       }
     }

@@ -40,7 +40,7 @@ struct DecodeParams {
   const float* bmm2_dev;
   __nv_bfloat16* out;
   float* out_lse;
-  float* part_o;     // [T, H, S, 512] fp32 normalised split partials (S > 1)
+  __nv_bfloat16* part_o;   // [T, H, S, 512] BF16 normalised split partials (S > 1)
   float* part_lse;   // [T, H, S] fp32 base-2 LSE of each partial (S > 1)
   int32_t* err;
   // page-table form of the compressed segment (bt == nullptr: index form)

@@ -209,9 +209,9 @@ decode_cuda_core_kernel(const DecodeParams p) {
       if (tid == 0 && p.out_lse) p.out_lse[(int64_t)t * p.H + hh] = lse;
     } else {
       const int64_t row = ((int64_t)t * p.H + hh) * p.num_splits + s;
-      float* o = p.part_o + row * kHeadDim;
-      o[tid] = acc[h][0] * inv;
-      o[tid + 256] = acc[h][1] * inv;
+      __nv_bfloat16* o = p.part_o + row * kHeadDim;
+      o[tid] = __float2bfloat16_rn(acc[h][0] * inv);
+      o[tid + 256] = __float2bfloat16_rn(acc[h][1] * inv);
       if (tid == 0) p.part_lse[row] = lse;
     }
   }

@@ -119,10 +119,7 @@ struct Cfg {
   static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
   static constexpr int kQBytes = kRegions * kRegionQ;
   static constexpr int kStageBytes = kRegions * kRegionKV;
-  // one exchange buffer: 128 rows of N 24-bit logits (BF16 keeps 4 bytes per
-  // logit of room: its split-partial epilogue stages 128 KB over the KV ring
-  // and the exchange buffers)
-  static constexpr int kXBytes = 128 * kN * (kFp8 ? 3 : 4);
+  static constexpr int kXBytes = 128 * kN * 3;                 // one exchange buffer: 128 rows of N 24-bit logits
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffX = kOffKV + kStages * kStageBytes;
@@ -135,7 +132,7 @@ struct Cfg {
   static_assert(kPCols == 16, "P buffer width");
   static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
   static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
-  static_assert(kStages * kStageBytes + 2 * kXBytes >= 2 * 128 * 512, "partial staging fits in the KV stages and exchange buffers");
+  static_assert(kStages * kStageBytes >= 2 * 128 * 256, "BF16 partial staging fits in the KV stages");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -749,17 +746,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
         const int d0 = (int)rank * kHalfDims + col;
-        if (S == 1) {
-          uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
+        uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        } else {
-          float4* o = reinterpret_cast<float4*>(p.part_o + (row_th * S + s) * kHeadDim + d0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       if (rank == 0 && g == 0) {
         if (S == 1) {
@@ -769,12 +760,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         }
       }
       } else {
-        // fp32 partial rows go through shared memory (the KV stages and
-        // exchange buffers are free once every PV is done), so that the global
-        // stores below are whole 512-byte row segments rather than one 16-byte
-        // piece per row per warp instruction.  Warpgroup g stages its 128
-        // columns; 16-byte chunks are XOR-swizzled by the row to spread banks.
-        unsigned char* row = base + C::kOffKV + g * (128 * 512) + h * 512;
+        // BF16 partial rows go through shared memory (the KV stages are free
+        // once every PV is done), so that the global stores below are whole
+        // 256-byte row segments rather than one 16-byte piece per row per warp
+        // instruction.  Warpgroup g stages its 128 columns; 16-byte chunks are
+        // XOR-swizzled by the row to spread banks.
+        unsigned char* row = base + C::kOffKV + g * (128 * 256) + h * 256;
 #pragma unroll 1
         for (int cc = 0; cc < kHalfDims / 64; ++cc) {
           const int col = g * (kHalfDims / 2) + cc * 32;
@@ -790,22 +781,25 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(row + (((cc * 8 + q) ^ (h & 7)) << 4)) =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         }
         if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
       }
     }
-    // copy-out of this warpgroup's staged partial columns, 512 contiguous bytes per row
+    // copy-out of this warpgroup's staged partial columns, 256 contiguous bytes
+    // per row (half a warp per row)
     if constexpr (kPartial) {
       asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(128) : "memory");
-      const unsigned char* stg = base + C::kOffKV + g * (128 * 512);
+      const unsigned char* stg = base + C::kOffKV + g * (128 * 256);
       const int w4 = (warp - kSoftmaxWarp0) & 3;
       const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
-      for (int r = w4; r < H; r += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(stg + r * 512 + ((lane ^ (r & 7)) << 4));
-        *reinterpret_cast<float4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + lane * 4) = x;
+      const int c = lane & 15;
+      for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
+        const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((c ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + c * 8) = x;
       }
     }
   }

@@ -165,7 +165,8 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
   plan->grid = (int32_t)grid;
   if (S > 1) {
     const size_t rows = (size_t)a->sum_q * a->num_heads * S;
-    plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
+    // BF16 normalised partials, then fp32 base-2 LSEs
+    plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256) + align_up(rows * sizeof(float), 256);
   }
   return SMLA_OK;
 }
@@ -264,9 +265,9 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   p.err = a->error_word;
   if (plan.num_splits > 1) {
     const size_t rows = (size_t)a->sum_q * a->num_heads * plan.num_splits;
-    p.part_o = reinterpret_cast<float*>(a->workspace);
+    p.part_o = reinterpret_cast<__nv_bfloat16*>(a->workspace);
     p.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(a->workspace) +
-                                          align_up(rows * kHeadDim * sizeof(float), 256));
+                                          align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256));
   }
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
