@@ -18,6 +18,7 @@ os.environ.setdefault("OMP_NUM_THREADS", str(_NCPU))
 
 import argparse  # noqa: E402
 import hashlib  # noqa: E402
+import re  # noqa: E402
 import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
@@ -74,13 +75,21 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed (a
+    comment edit leaves the compiled kernel, and so its counters, unchanged)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sources_sha() -> str:
     csrc = os.path.join(ROOT, "sparse_mla_decode_token_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
             h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,9 +13,11 @@
 //   producer warps 0-5  the pair's half of every selected row (256 dims) with
 //                       TMA tile::gather4 (four rows of 128 bytes per request)
 //                       into a 128-byte-swizzled, UMMA-canonical shared-memory
-//                       tile; a warp's TMA requests are served one after
-//                       another, so a tile's 32 requests are spread over the
-//                       three warps of one of two groups taking alternate tiles
+//                       tile of a 7-stage (E4M3) or 6-stage (BF16) ring; a
+//                       warp's TMA requests are served one after another, so a
+//                       tile's 32 requests are spread over the three warps of
+//                       one of two groups taking alternate tiles; a tile of N
+//                       consecutive rows is one box copy per 128-byte block
 //   QK warp 6           S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
 //                       into one of three TMEM S buffers; also allocates and
 //                       frees TMEM
@@ -27,12 +29,12 @@
 //                       read S_r from TMEM, push it to the peer CTA with
 //                       st.async (completing bytes on the peer's mbarrier) as
 //                       24-bit floats (four values in three words), add
-//                       the peer's partial (S = S_0 + S_1, identical in both
-//                       CTAs), settle the running reference maximum m(j) from
+//                       the peer's partial (S = S_0 + S_1; each CTA adds its
+//                       own exact half), settle the running reference maximum m(j) from
 //                       m(j-1) (handed over by the other warpgroup through
 //                       shared memory), exponentials in base 2 with lazy
 //                       rescaling of O, write P (BF16 or E4M3) into TMEM;
-//                       finally normalise O and store it (BF16 output, or fp32
+//                       finally normalise O and store it (BF16 output, or BF16
 //                       split partials staged through shared memory) plus the
 //                       LSE.  Each warpgroup pushes its next tile's partial S
 //                       before its exponentials; one warpgroup's exponentials
@@ -197,7 +199,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// kPartial: the launch has num_splits > 1 and writes fp32 split partials; its
+// kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
 // epilogue stages the partial rows in shared memory for contiguous stores (a
 // separate instantiation, so that the single-split code is compiled alone).
 template <bool kFp8, bool kPartial>
