@@ -368,13 +368,8 @@ def run_gpu(args):
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
 
-    def e2e_pipelined(steps):
-        """Seconds for `steps` pipelined end-to-end steps, and whether the last
-        step's copied-back output equals the device-resident leg's."""
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        ev0.record(s_in)
+    def e2e_enqueue(steps, comp):
+        """Enqueue `steps` pipelined end-to-end steps; decodes on stream `comp`."""
         for k_ in range(steps):
             st_ = e2e_sets[k_ & 1]
             if k_ >= 2:
@@ -382,22 +377,55 @@ def run_gpu(args):
             with torch.cuda.stream(s_in):
                 st_["d_in"].copy_(h_in, non_blocking=True)
                 st_["ev_in"].record(s_in)
-            stream.wait_event(st_["ev_in"])
+            comp.wait_event(st_["ev_in"])
             if k_ >= 2:
-                stream.wait_event(st_["ev_out"])          # step k - 2's outputs are copied out
-            B.smla_decode(st_["args"], sptr)
-            st_["ev_done"].record(stream)
+                comp.wait_event(st_["ev_out"])            # step k - 2's outputs are copied out
+            B.smla_decode(st_["args"], comp.cuda_stream)
+            st_["ev_done"].record(comp)
             s_out.wait_event(st_["ev_done"])
             with torch.cuda.stream(s_out):
                 st_["h_res"].copy_(st_["d_res"], non_blocking=True)
                 st_["ev_out"].record(s_out)
-        ev1.record(s_out)
-        torch.cuda.synchronize()
+
+    def e2e_check(steps):
         last = e2e_sets[(steps - 1) & 1]
         n_out = out.numel() * out.element_size()
-        same = bool(torch.equal(last["h_res"][:n_out], last["d_res"][:n_out].cpu())) and \
+        return bool(torch.equal(last["h_res"][:n_out], last["d_res"][:n_out].cpu())) and \
             bool(torch.equal(last["res"]["out"].cpu(), out.cpu())) and bool(torch.equal(last["res"]["lse"].cpu(), lse.cpu()))
-        return ev0.elapsed_time(ev1) / 1e3, same
+
+    def e2e_pipelined(steps):
+        """Host-loop form: seconds for `steps` pipelined end-to-end steps, and
+        whether the last step's copied-back output equals the device-resident leg's."""
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(s_in)
+        e2e_enqueue(steps, stream)
+        ev1.record(s_out)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3, e2e_check(steps)
+
+    def e2e_graphed(steps):
+        """The same `steps` captured once in a CUDA graph (the public call
+        captured with its copies), then one replay timed: no host time inside."""
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            s_in.wait_stream(cap)
+            s_out.wait_stream(cap)
+            e2e_enqueue(steps, cap)
+            cap.wait_stream(s_in)
+            cap.wait_stream(s_out)
+        g.replay()                                        # warm
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / 1e3, e2e_check(steps)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -434,7 +462,14 @@ def run_gpu(args):
         # with two buffer sets, so step k's copies overlap the decodes of steps
         # k - 1 and k + 1 (a serving loop's pipeline); the timed region spans
         # all K steps, every copy included.
-        e2e_s, e2e_ok = e2e_pipelined(K)
+        try:
+            e2e_s, e2e_ok = e2e_graphed(K)
+            e2e_how = "one CUDA graph of the K steps (captured once, replayed once)"
+        except RuntimeError as exc:                      # capture refused: time the host loop instead
+            print(f"e2e graph capture failed ({exc}); timing the host loop", file=sys.stderr)
+            torch.cuda.synchronize()
+            e2e_s, e2e_ok = e2e_pipelined(K)
+            e2e_how = "host loop"
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     main_ms = [a.elapsed_time(b) for a, b in ev_main]
     total_s = max_over_ranks(sum(step_ms) / 1e3, ws_, dev)
@@ -481,7 +516,7 @@ def run_gpu(args):
         "plan": plan.as_dict(),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": "copy in, decode and copy out on three streams, two buffer sets",
+                "pipeline": "copy in, decode and copy out on three streams, two buffer sets; " + e2e_how,
                 "l2": ("not flushed: the KV pools (%d MB) are larger than L2 (%d MB)" if pool_mb > l2 // 2**20
                        else "warm: the KV pools (%d MB) fit in L2 (%d MB)") % (pool_mb, l2 // 2**20),
                 "output_matches_device_leg": e2e_ok},
