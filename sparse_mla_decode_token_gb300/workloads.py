@@ -240,12 +240,15 @@ def make_paged_workload(*, name: str = "paged", seed: int, dtype: str, batch: in
                         ring_len: Optional[int] = None, topk_lens=None,
                         swa_topk_lens=None, sinks: bool = False,
                         varlen: Optional[bool] = None, fill_unused: int = -1,
-                        width: Optional[int] = None,
+                        width: Optional[int] = None, per_token_pages: bool = False,
                         softmax_scale: float = 1.0 / math.sqrt(HEAD_DIM)) -> Workload:
     """Draw a workload whose compressed segment is a page table.
 
     Every request owns ``max_pages`` distinct random pages of the compressed
-    pool (``comp_pages * page_size`` rows); its tokens share that page list.
+    pool (``comp_pages * page_size`` rows); its tokens share that page list,
+    unless ``per_token_pages``, where every token draws a list of its own (the
+    table has one row per token, so a token must read its own row, not its
+    request's).
     Table entries past the request's footprint ``ceil((hca_seq_lens[b] - 128)
     / page_size)`` hold ``fill_unused`` (never read as rows).  All 128 SWA
     columns hold legal ring rows; the visible window is ``swa_topk_lens`` when
@@ -274,12 +277,15 @@ def make_paged_workload(*, name: str = "paged", seed: int, dtype: str, batch: in
     indices = np.empty((sum_q, SWA_COLS), dtype=np.int32)
     tables = np.full((sum_q, max_pages), fill_unused, dtype=np.int32)
     pages_of = [rng.choice(comp_pages, size=max_pages, replace=False).astype(np.int32) for _ in range(batch)]
+    if per_token_pages:            # drawn after the shared lists: the default stream is unchanged
+        token_pages = [rng.choice(comp_pages, size=max_pages, replace=False).astype(np.int32)
+                       for _ in range(sum_q)]
     for t in range(sum_q):
         b = int(req_of_token[t])
         p = int(pos[t]) - (SWA_COLS - 1) + np.arange(SWA_COLS)       # every column a legal ring row
         indices[t] = b * ring_len + (p % ring_len)
         used = -(-max(0, int(hca[b]) - SWA_COLS) // page_size)
-        tables[t, :used] = pages_of[b][:used]
+        tables[t, :used] = (token_pages[t] if per_token_pages else pages_of[b])[:used]
     if topk_lens is not None:
         topk_lens = np.broadcast_to(np.asarray(topk_lens, dtype=np.int64), (sum_q,)).astype(np.int32)
     if swa_topk_lens is not None:

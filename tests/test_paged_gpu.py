@@ -26,7 +26,7 @@ def built():
 
 def paged_case(seed, *, dtype="bf16", H=128, page_size=64, hca=(128 + 300, 128 + 64, 100),
                q_lens=(1, 2, 1), topk="random", swa_topk=(128, 17, 0, 64), sinks=True,
-               fill_unused=-1, comp_pages=64):
+               fill_unused=-1, comp_pages=64, per_token_pages=False):
     rng = np.random.default_rng(seed)
     batch = len(hca)
     max_pages = -(-max(h - 128 for h in hca) // page_size)
@@ -38,7 +38,7 @@ def paged_case(seed, *, dtype="bf16", H=128, page_size=64, hca=(128 + 300, 128 +
                                  max_pages=max_pages, hca_seq_lens=list(hca),
                                  seq_lens=[5000, 90, 3000, 7000][:batch], ring_len=130,
                                  topk_lens=topk_lens, swa_topk_lens=swa_topk, sinks=sinks,
-                                 varlen=True, fill_unused=fill_unused)
+                                 varlen=True, fill_unused=fill_unused, per_token_pages=per_token_pages)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -63,6 +63,19 @@ def test_paged_page_sizes_off_the_tile_grid(kernel, dtype, page_size):
     w = paged_case(500 + page_size, dtype=dtype, page_size=page_size, hca=(128 + 300, 128 + 200, 128 + 1),
                    topk=None, swa_topk=None, comp_pages=max(64, 3 * 300 // page_size + 8))
     out, lse, _ = run_gpu(w, kernel=kernel)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("splits", [1, 0])
+def test_paged_per_token_tables(kernel, dtype, splits):
+    """Tokens of one request list different pages: each reads its own table row."""
+    w = paged_case(700 + splits, dtype=dtype, q_lens=(3, 2, 1), hca=(128 + 300, 128 + 64, 128 + 9),
+                   swa_topk=None, per_token_pages=True)
+    bt = w.comp_block_tables
+    assert not np.array_equal(bt[0], bt[1]) and not np.array_equal(bt[3], bt[4])
+    out, lse, _ = run_gpu(w, kernel=kernel, num_splits=splits)
     compare(w, out, lse)
 
 
