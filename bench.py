@@ -83,19 +83,28 @@ def code_only(text: str) -> str:
     return " ".join(text.split())
 
 
+# Sources with no device code: argument checks, the planner and parameter
+# packing.  What they decide about a launch (kernel, splits, grid, block, shared
+# memory) is matched through the plan stored with each traffic record instead.
+HOST_ONLY_SOURCES = ("smla_api.cu",)
+PLAN_KEYS = ("kernel", "num_splits", "ctas_per_split", "grid", "threads", "smem_bytes")
+
+
 def kernel_sources_sha() -> str:
+    """Hash of the device-code sources (comments and whitespace ignored)."""
     csrc = os.path.join(ROOT, "sparse_mla_decode_token_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cu", ".cuh", ".h")) and f not in HOST_ONLY_SOURCES:
             h.update(f.encode())
             h.update(code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, plan: dict):
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
-    if it was taken on the current kernel sources; else None."""
+    if it was taken on the current device code with this run's launch plan;
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -104,6 +113,9 @@ def recorded_traffic(workload: str):
         return None
     ent = rec.get(workload)
     if not ent or ent.get("kernel_sources_sha") != kernel_sources_sha():
+        return None
+    want = ent.get("plan")
+    if not want or any(want.get(k) != plan.get(k) for k in PLAN_KEYS):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -492,7 +504,7 @@ def run_gpu(args):
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["traffic"] = recorded_traffic(W.CONFIG_NAMES[args.config])
+    roof["traffic"] = recorded_traffic(W.CONFIG_NAMES[args.config], plan.as_dict())
     roof["algorithmic_bytes_per_launch"] = gathered_bytes
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
     roof["main_kernel_us"] = 1e6 * main_s

@@ -185,7 +185,12 @@ smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes
  * Run the decode on `stream` (a cudaStream_t, NULL = legacy default stream) on
  * the current device.  Asynchronous; allocation- and synchronisation-free.
  * Writes out (and out_lse if given).  Returns SMLA_ERR_* without launching on
- * a host-detectable problem, SMLA_ERR_CUDA if a launch fails.
+ * a host-detectable problem, SMLA_ERR_CUDA if a launch fails.  Shapes and
+ * pointers are checked before any CUDA call: a missing required pointer (q,
+ * swa_kv, compressed_kv, sparse_indices, seq_lens, out; hca_seq_lens with
+ * comp_block_tables), a row pointer (q, swa_kv, compressed_kv, out) not
+ * 16-byte aligned, or an int32 / float32 array not 4-byte aligned is
+ * SMLA_ERR_INVALID_ARG.  Pointed-to values are never read on the host.
  */
 smla_status smla_decode(const smla_args* args, void* stream);
 

@@ -93,6 +93,34 @@ smla_status check_shapes(const smla_args* a) {
   return SMLA_OK;
 }
 
+// Pointer checks of a call with sum_q > 0.  Every array the kernels read or
+// write must be present where required and aligned to its access width: the
+// 16-byte rows (q, pools, out) for TMA and vector accesses, every int32 or
+// float32 array to 4 bytes.  A misaligned pointer would otherwise reach the
+// device as a misaligned access.
+smla_status check_pointers(const smla_args* a) {
+  if (!a->q || !a->swa_kv || !a->compressed_kv || !a->sparse_indices || !a->seq_lens || !a->out)
+    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv, sparse_indices, seq_lens and out are required");
+  if (a->comp_block_tables && !a->hca_seq_lens)
+    return fail(SMLA_ERR_INVALID_ARG, "hca_seq_lens is required with comp_block_tables");
+  if (!aligned(a->q, 16) || !aligned(a->swa_kv, 16) || !aligned(a->compressed_kv, 16) || !aligned(a->out, 16))
+    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv and out must be 16-byte aligned");
+  const struct {
+    const void* ptr;
+    const char* name;
+  } words[] = {
+      {a->sparse_indices, "sparse_indices"}, {a->sparse_topk_lens, "sparse_topk_lens"},
+      {a->seq_lens, "seq_lens"},             {a->cum_seq_lens_q, "cum_seq_lens_q"},
+      {a->sinks, "sinks"},                   {a->bmm1_scale_dev, "bmm1_scale_dev"},
+      {a->bmm2_scale_dev, "bmm2_scale_dev"}, {a->out_lse, "out_lse"},
+      {a->error_word, "error_word"},         {a->comp_block_tables, "comp_block_tables"},
+      {a->hca_seq_lens, "hca_seq_lens"},     {a->swa_topk_lens, "swa_topk_lens"},
+  };
+  for (const auto& w : words)
+    if (w.ptr && !aligned(w.ptr, 4)) return fail(SMLA_ERR_INVALID_ARG, "%s must be 4-byte aligned", w.name);
+  return SMLA_OK;
+}
+
 // Kernel that SMLA_KERNEL_AUTO selects.
 constexpr int kAutoKernel = SMLA_KERNEL_TCGEN05;
 
@@ -199,27 +227,18 @@ smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes
 }
 
 smla_status smla_decode(const smla_args* a, void* stream_ptr) {
-  smla_status st = check_shapes(a);   // host-only checks come before any CUDA call
+  // host-only checks (shapes, then pointers) come before any CUDA call
+  smla_status st = check_shapes(a);
   if (st != SMLA_OK) return st;
   if (a->sum_q == 0) return SMLA_OK;   // empty batch: nothing to launch
+  st = check_pointers(a);
+  if (st != SMLA_OK) return st;
   int device = 0;
   cudaError_t ce = cudaGetDevice(&device);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
   smla_plan plan;
   st = make_plan(a, device, &plan);
   if (st != SMLA_OK) return st;
-  if (a->sum_q == 0) return SMLA_OK;
-  if (!a->q || !a->swa_kv || !a->compressed_kv || !a->sparse_indices || !a->seq_lens || !a->out)
-    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv, sparse_indices, seq_lens and out are required");
-  if (a->comp_block_tables && !a->hca_seq_lens)
-    return fail(SMLA_ERR_INVALID_ARG, "hca_seq_lens is required with comp_block_tables");
-  if ((a->comp_block_tables && !aligned(a->comp_block_tables, 4)) || (a->hca_seq_lens && !aligned(a->hca_seq_lens, 4)) ||
-      (a->swa_topk_lens && !aligned(a->swa_topk_lens, 4)))
-    return fail(SMLA_ERR_INVALID_ARG, "comp_block_tables, hca_seq_lens and swa_topk_lens must be 4-byte aligned");
-  if (!aligned(a->q, 16) || !aligned(a->swa_kv, 16) || !aligned(a->compressed_kv, 16) || !aligned(a->out, 16))
-    return fail(SMLA_ERR_INVALID_ARG, "q, swa_kv, compressed_kv and out must be 16-byte aligned");
-  if (!aligned(a->sparse_indices, 4) || (a->out_lse && !aligned(a->out_lse, 4)))
-    return fail(SMLA_ERR_INVALID_ARG, "sparse_indices and out_lse must be 4-byte aligned");
   if (plan.workspace_bytes > 0) {
     if (a->workspace == nullptr || a->workspace_bytes < plan.workspace_bytes)
       return fail(SMLA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes given, %zu needed",

@@ -100,6 +100,54 @@ def test_host_argument_errors(lib, mutate, code, needle):
     assert needle in B.smla_last_error()
 
 
+def pointer_args():
+    """Every pointer a 256-byte-aligned marker (host checks never dereference)."""
+    a = good_args()
+    for i, f in enumerate(("q", "swa_kv", "compressed_kv", "sparse_indices", "seq_lens", "out")):
+        setattr(a, f, 0x10000 * (i + 1))
+    return a
+
+
+WORD_ARRAYS = ("sparse_indices", "sparse_topk_lens", "seq_lens", "cum_seq_lens_q", "sinks",
+               "bmm1_scale_dev", "bmm2_scale_dev", "out_lse", "error_word", "comp_block_tables",
+               "hca_seq_lens", "swa_topk_lens")
+
+
+@pytest.mark.parametrize("field", WORD_ARRAYS)
+def test_misaligned_word_arrays_are_rejected_on_the_host(lib, field):
+    """int32 / float32 arrays must be 4-byte aligned; the check runs before
+    any CUDA call, so it answers here without a GPU."""
+    a = pointer_args()
+    if field in ("comp_block_tables", "hca_seq_lens"):
+        a.comp_block_tables, a.comp_max_pages, a.comp_page_size, a.hca_seq_lens = 0x90000, 4, 128, 0xa0000
+    setattr(a, field, 0x80002)
+    assert status(lib, a) == B.SMLA_ERR_INVALID_ARG
+    assert f"{field} must be 4-byte aligned" in B.smla_last_error()
+
+
+@pytest.mark.parametrize("field", ["q", "swa_kv", "compressed_kv", "out"])
+def test_misaligned_rows_are_rejected_on_the_host(lib, field):
+    a = pointer_args()
+    setattr(a, field, 0x80008)
+    assert status(lib, a) == B.SMLA_ERR_INVALID_ARG
+    assert "16-byte aligned" in B.smla_last_error()
+
+
+@pytest.mark.parametrize("field", ["q", "swa_kv", "compressed_kv", "sparse_indices", "seq_lens", "out"])
+def test_missing_required_pointer_is_rejected_on_the_host(lib, field):
+    a = pointer_args()
+    setattr(a, field, None)
+    assert status(lib, a) == B.SMLA_ERR_INVALID_ARG
+    assert "required" in B.smla_last_error()
+
+
+def test_page_table_without_hca_seq_lens_is_rejected_on_the_host(lib):
+    a = pointer_args()
+    a.comp_block_tables, a.comp_max_pages, a.comp_page_size = 0x90000, 4, 128
+    assert status(lib, a) == B.SMLA_ERR_INVALID_ARG
+    assert "hca_seq_lens is required" in B.smla_last_error()
+
+
 def paged_args():
     """Page-table form: 4 pages of 128 rows cover the 512 compressed columns of
     width 640; the pointers are markers only (host checks never read them)."""

@@ -47,3 +47,29 @@ def test_workload_config_names_the_page_table_form():
     assert cfg["workload"] == "paged_fp8_b128_h128"
     assert cfg["page_size"] == 128 and cfg["pages_per_token"] == 16 and cfg["index_width"] == 2176
     assert "page_size" not in bench.workload_config(W.config_workload(1), 1)
+
+
+def test_recorded_traffic_needs_the_same_device_code_and_plan(monkeypatch):
+    """A stored ncu traffic figure is reported only for the device code and
+    launch plan it was captured on."""
+    import json
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    name = "fp8_decode_b128_h128"
+    plan = dict(rec[name]["plan"], workspace_bytes=0)
+    want = rec[name]["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: rec[name]["kernel_sources_sha"])
+    assert bench.recorded_traffic(name, plan) == want
+    assert bench.recorded_traffic(name, dict(plan, num_splits=2)) is None
+    assert bench.recorded_traffic(name, dict(plan, grid=plan["grid"] + 2)) is None
+    assert bench.recorded_traffic("no_such_workload", plan) is None
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "0" * 16)
+    assert bench.recorded_traffic(name, plan) is None
+
+
+def test_host_only_sources_hold_no_device_code():
+    """Files left out of the device-code hash must not define device code."""
+    csrc = os.path.join(ROOT, "sparse_mla_decode_token_gb300", "csrc")
+    for f in bench.HOST_ONLY_SOURCES:
+        code = bench.code_only(open(os.path.join(csrc, f)).read())
+        for word in ("__global__", "__device__", "__constant__", "__shared__", "asm(", "asm volatile"):
+            assert word not in code, (f, word)
