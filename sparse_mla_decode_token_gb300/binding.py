@@ -200,6 +200,58 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     ``comp_page_size`` rows per page and ``hca_seq_lens`` ``[B]``; the index
     table then holds the 128 SWA columns and ``width`` (logical columns)
     defaults to ``128 + max_pages * comp_page_size``."""
+    # layout first (tensor metadata only), so that a wrong shape, dtype or
+    # length answers the same on any device; placement after
+    if q.dim() == 4:                       # dense [B, q_len, H, 512]
+        try:
+            q = q.view(-1, q.shape[2], q.shape[3])     # a copy would leave the library a dangling pointer
+        except RuntimeError as exc:
+            raise ValueError(f"dense query [B, q_len, H, {HEAD_DIM}] must flatten to [T, H, {HEAD_DIM}] "
+                             f"without a copy: {exc}") from None
+    if q.dim() != 3 or q.shape[-1] != HEAD_DIM or q.stride(-1) != 1 or q.stride(1) != HEAD_DIM:
+        raise ValueError(f"query must be [T, H, {HEAD_DIM}] with contiguous heads; got {tuple(q.shape)}")
+    T, H = q.shape[0], q.shape[1]
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.numel() != T * H * HEAD_DIM:
+        raise ValueError("out must be a contiguous bfloat16 tensor of T*H*512 elements")
+    if out_lse is not None and (out_lse.dtype != torch.float32 or not out_lse.is_contiguous()
+                                or out_lse.numel() != T * H):
+        raise ValueError("out_lse must be a contiguous float32 tensor of T*H elements")
+    for name, t in (("sparse_indices", sparse_indices), ("seq_lens", seq_lens),
+                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
+                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
+                    ("hca_seq_lens", hca_seq_lens), ("error_word", error_word)):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    B = seq_lens.numel()
+    # arrays the kernels index by token, request or head: contiguous and long
+    # enough (a short one would be read past its end on the device)
+    for name, t, need in (("seq_lens", seq_lens, B), ("sparse_topk_lens", sparse_topk_lens, T),
+                          ("cum_seq_lens_q", cum_seq_lens_q, B + 1), ("swa_topk_lens", swa_topk_lens, T),
+                          ("hca_seq_lens", hca_seq_lens, B), ("sinks", sinks, H),
+                          ("error_word", error_word, 1)):
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.numel() < need:
+            raise ValueError(f"{name} has {t.numel()} entries; the call reads {need}")
+    if sinks is not None and sinks.dtype != torch.float32:
+        raise ValueError("sinks must be float32 with at least H entries")
+    for name, val in (("bmm1", bmm1_scale), ("bmm2", bmm2_scale)):
+        if isinstance(val, torch.Tensor):
+            if val.dtype != torch.float32:
+                raise TypeError(f"{name}_scale tensor must be float32")
+            if val.numel() < 1:
+                raise ValueError(f"{name}_scale tensor is empty")
+    if sparse_indices.dim() == 3:          # [T, 1, W]
+        if sparse_indices.shape[1] != 1:
+            raise ValueError(f"sparse_indices [T, 1, W] must have 1 in dim 1; got {tuple(sparse_indices.shape)}")
+        sparse_indices = sparse_indices[:, 0, :]
+    if sparse_indices.dim() != 2 or sparse_indices.stride(-1) != 1:
+        raise ValueError("sparse_indices must be [T, W] with a contiguous last dim")
+    if sparse_indices.shape[0] < T:
+        raise ValueError(f"sparse_indices has {sparse_indices.shape[0]} rows for {T} query tokens")
+
     dev = q.device
     for name, t in (("q", q), ("swa_kv", swa_kv), ("compressed_kv", compressed_kv),
                     ("sparse_indices", sparse_indices), ("seq_lens", seq_lens), ("out", out),
@@ -212,30 +264,6 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
             raise ValueError(f"{name} is on {t.device}; every tensor must be on the CUDA device of q ({dev})")
     if dev.type != "cuda":
         raise ValueError(f"q is on {dev}; the decode runs on a CUDA device")
-    if q.dim() == 4:                       # dense [B, q_len, H, 512]
-        q = q.reshape(-1, q.shape[2], q.shape[3])
-    if q.dim() != 3 or q.shape[-1] != HEAD_DIM or q.stride(-1) != 1 or q.stride(1) != HEAD_DIM:
-        raise ValueError(f"query must be [T, H, {HEAD_DIM}] with contiguous heads; got {tuple(q.shape)}")
-    T, H = q.shape[0], q.shape[1]
-    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.numel() != T * H * HEAD_DIM:
-        raise ValueError("out must be a contiguous bfloat16 tensor of T*H*512 elements")
-    if out_lse is not None and (out_lse.dtype != torch.float32 or not out_lse.is_contiguous()
-                                or out_lse.numel() != T * H):
-        raise ValueError("out_lse must be a contiguous float32 tensor of T*H elements")
-    for name, t in (("sparse_indices", sparse_indices), ("seq_lens", seq_lens),
-                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
-                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
-                    ("hca_seq_lens", hca_seq_lens)):
-        if t is not None and t.dtype != torch.int32:
-            raise TypeError(f"{name} must be int32")
-    for name, t in (("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
-                    ("swa_topk_lens", swa_topk_lens), ("hca_seq_lens", hca_seq_lens)):
-        if t is not None and not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if sparse_indices.dim() == 3:          # [T, 1, W]
-        sparse_indices = sparse_indices[:, 0, :]
-    if sparse_indices.stride(-1) != 1:
-        raise ValueError("sparse_indices must have a contiguous last dim")
     swa_rows, swa_stride = _rows_and_stride(swa_kv)
     comp_rows, comp_stride = _rows_and_stride(compressed_kv)
     a = SmlaArgs()
@@ -252,7 +280,7 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     elif width is not None and width != a.width:
         raise ValueError("width is the index table's width in the index form")
     a.swa_topk_lens = _ptr(swa_topk_lens)
-    a.batch = seq_lens.numel()
+    a.batch = B
     a.dtype = _dtype_code(q)
     if _dtype_code(swa_kv) != a.dtype or _dtype_code(compressed_kv) != a.dtype:
         raise TypeError("query, swa_kv and compressed_kv must share one dtype")
@@ -263,13 +291,9 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     a.sparse_topk_lens = _ptr(sparse_topk_lens)
     a.seq_lens = seq_lens.data_ptr()
     a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
-    if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() < H):
-        raise ValueError("sinks must be float32 with at least H entries")
     a.sinks = _ptr(sinks)
     for name, val in (("bmm1", bmm1_scale), ("bmm2", bmm2_scale)):
         if isinstance(val, torch.Tensor):
-            if val.dtype != torch.float32:
-                raise TypeError(f"{name}_scale tensor must be float32")
             setattr(a, f"{name}_scale_dev", val.data_ptr())
             setattr(a, f"{name}_scale", 1.0)
         else:
@@ -331,7 +355,7 @@ def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=
     """Workspace bytes for a call with these shapes (no device memory is read);
     ``width`` = logical columns in the page-table form."""
     a = SmlaArgs()
-    q3 = query if query.dim() == 3 else query.reshape(-1, query.shape[2], query.shape[3])
+    q3 = query if query.dim() == 3 else query.view(-1, query.shape[2], query.shape[3])
     a.sum_q, a.num_heads = q3.shape[0], q3.shape[1]
     a.width = sparse_indices.shape[-1] if width is None else int(width)
     a.batch, a.dtype = seq_lens.numel(), _dtype_code(q3)

@@ -224,3 +224,62 @@ def test_binding_rejects_host_tensors():
     out = torch.empty(2, 64, 512, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA device"):
         B.make_args(q=q, swa_kv=kv, compressed_kv=kv, sparse_indices=idx, seq_lens=seq, out=out)
+
+
+def _host_call(**over):
+    """A well-formed call's tensors, on the host (layout checks precede the
+    device check, so every layout error below answers without a GPU)."""
+    import torch
+    T, H, B = 4, 64, 2
+    kw = dict(q=torch.zeros(T, H, 512, dtype=torch.bfloat16),
+              swa_kv=torch.zeros(256, 512, dtype=torch.bfloat16),
+              compressed_kv=torch.zeros(256, 512, dtype=torch.bfloat16),
+              sparse_indices=torch.zeros(T, 256, dtype=torch.int32),
+              seq_lens=torch.full((B,), 300, dtype=torch.int32),
+              out=torch.empty(T, H, 512, dtype=torch.bfloat16),
+              sparse_topk_lens=torch.full((T,), 200, dtype=torch.int32),
+              cum_seq_lens_q=torch.tensor([0, 1, 4], dtype=torch.int32),
+              sinks=torch.zeros(H, dtype=torch.float32),
+              error_word=torch.zeros(1, dtype=torch.int32))
+    kw.update(over)
+    return kw
+
+
+def _bad_layouts():
+    import torch
+    i32 = torch.int32
+    return [
+        ("short_topk_lens", dict(sparse_topk_lens=torch.zeros(3, dtype=i32)), ValueError, "sparse_topk_lens has 3"),
+        ("short_cum", dict(cum_seq_lens_q=torch.tensor([0, 4], dtype=i32)), ValueError, "cum_seq_lens_q has 2"),
+        ("short_sinks", dict(sinks=torch.zeros(63)), ValueError, "sinks has 63"),
+        ("strided_sinks", dict(sinks=torch.zeros(128)[::2]), ValueError, "sinks must be contiguous"),
+        ("f64_sinks", dict(sinks=torch.zeros(64, dtype=torch.float64)), ValueError, "float32"),
+        ("strided_seq_lens", dict(seq_lens=torch.zeros(4, dtype=i32)[::2]), ValueError, "seq_lens must be contiguous"),
+        ("short_swa_topk_lens", dict(swa_topk_lens=torch.zeros(2, dtype=i32)), ValueError, "swa_topk_lens has 2"),
+        ("i64_error_word", dict(error_word=torch.zeros(1, dtype=torch.int64)), TypeError, "error_word must be int32"),
+        ("empty_error_word", dict(error_word=torch.zeros(0, dtype=i32)), ValueError, "error_word has 0"),
+        ("i64_seq_lens", dict(seq_lens=torch.zeros(2, dtype=torch.int64)), TypeError, "seq_lens must be int32"),
+        ("f16_scale", dict(bmm1_scale=torch.ones(1, dtype=torch.float16)), TypeError, "bmm1_scale"),
+        ("empty_scale", dict(bmm2_scale=torch.ones(0)), ValueError, "bmm2_scale tensor is empty"),
+        ("few_index_rows", dict(sparse_indices=torch.zeros(3, 256, dtype=i32)), ValueError, "3 rows for 4"),
+        ("index_dim1_not_1", dict(sparse_indices=torch.zeros(4, 2, 256, dtype=i32)), ValueError, "1 in dim 1"),
+        ("strided_index_cols", dict(sparse_indices=torch.zeros(4, 512, dtype=i32)[:, ::2]), ValueError, "contiguous last dim"),
+        ("dense_query_needs_copy", dict(q=torch.zeros(2, 64, 2, 512, dtype=torch.bfloat16).transpose(1, 2)),
+         ValueError, "without a copy"),
+    ]
+
+
+@pytest.mark.parametrize("case", _bad_layouts(), ids=lambda c: c[0])
+def test_binding_rejects_bad_layouts_before_the_device_check(case):
+    _, over, exc, match = case
+    with pytest.raises(exc, match=match):
+        B.make_args(**_host_call(**over))
+
+
+def test_binding_well_formed_host_call_fails_only_on_placement():
+    with pytest.raises(ValueError, match="CUDA device"):
+        B.make_args(**_host_call())
+    import torch
+    # a dense [B, q_len, H, 512] query that flattens without a copy passes layout
+    with pytest.raises(ValueError, match="CUDA device"):
+        B.make_args(**_host_call(q=torch.zeros(2, 2, 64, 512, dtype=torch.bfloat16)))
