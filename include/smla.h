@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 2
+#define SMLA_ABI_VERSION 3
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -177,6 +177,16 @@ typedef struct smla_plan {
  * The plan depends only on shapes, the device and num_splits/max_splits/kernel.
  */
 smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan);
+
+/*
+ * The same plan for a device with `sm_count` streaming multiprocessors,
+ * without querying any device: a pure function of the shapes, the split
+ * controls and sm_count (smla_plan_decode is this with the device's SM count).
+ * For planning ahead of time, or for another device than the current one.
+ * SMLA_ERR_INVALID_ARG if sm_count < 1 or plan is NULL; shape errors as
+ * smla_plan_decode.
+ */
+smla_status smla_plan_decode_for_sm_count(const smla_args* args, int sm_count, smla_plan* plan);
 
 /* Workspace bytes smla_decode will need for these args on `device`. */
 smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes);

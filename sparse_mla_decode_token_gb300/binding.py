@@ -78,6 +78,8 @@ _lib = None
 # (symbol, restype, argtypes) of every entry point the header declares
 EXPORTS = {
     "smla_plan_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(SmlaPlan)]),
+    "smla_plan_decode_for_sm_count": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int,
+                                                     ctypes.POINTER(SmlaPlan)]),
     "smla_workspace_size": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "smla_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
     "smla_decode_static_workspace": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
@@ -125,6 +127,13 @@ def _check(status: int) -> None:
 def smla_plan_decode(args: SmlaArgs, device: int = 0) -> SmlaPlan:
     plan = SmlaPlan()
     _check(lib().smla_plan_decode(ctypes.byref(args), device, ctypes.byref(plan)))
+    return plan
+
+
+def smla_plan_decode_for_sm_count(args: SmlaArgs, sm_count: int) -> SmlaPlan:
+    """The plan for a device with ``sm_count`` SMs; queries no device."""
+    plan = SmlaPlan()
+    _check(lib().smla_plan_decode_for_sm_count(ctypes.byref(args), sm_count, ctypes.byref(plan)))
     return plan
 
 

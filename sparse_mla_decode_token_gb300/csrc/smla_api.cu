@@ -138,12 +138,12 @@ smla_status sm_count(int device, int* out) {
   return SMLA_OK;
 }
 
-smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
+// The plan as a pure function of the shapes, the split controls and the SM
+// count (no device is queried).
+smla_status make_plan_for(const smla_args* a, int sms, smla_plan* plan) {
   smla_status st = check_shapes(a);
   if (st != SMLA_OK) return st;
-  int sms = 0;
-  st = sm_count(device, &sms);
-  if (st != SMLA_OK) return st;
+  if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
   const int kernel = a->kernel == SMLA_KERNEL_AUTO ? kAutoKernel : a->kernel;
@@ -199,6 +199,15 @@ smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
   return SMLA_OK;
 }
 
+smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
+  smla_status st = check_shapes(a);   // shape errors come before the device query
+  if (st != SMLA_OK) return st;
+  int sms = 0;
+  st = sm_count(device, &sms);
+  if (st != SMLA_OK) return st;
+  return make_plan_for(a, sms, plan);
+}
+
 }  // namespace
 
 smla_status record_error(smla_status st, const char* msg) {
@@ -215,6 +224,11 @@ extern "C" {
 smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan) {
   if (plan == nullptr) return fail(SMLA_ERR_INVALID_ARG, "plan is NULL");
   return make_plan(args, device, plan);
+}
+
+smla_status smla_plan_decode_for_sm_count(const smla_args* args, int sm_count, smla_plan* plan) {
+  if (plan == nullptr) return fail(SMLA_ERR_INVALID_ARG, "plan is NULL");
+  return make_plan_for(args, sm_count, plan);
 }
 
 smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes) {

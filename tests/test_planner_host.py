@@ -1,0 +1,147 @@
+"""The split planner, called through the C ABI as a pure function of shapes
+and the SM count (no GPU): its documented rules, and the plans the committed
+measurements were taken with.
+
+Rules (tcgen05 kernel; one 2-CTA cluster per (token, split), 152 SMs = 76
+pairs on GB300): S = floor(pairs / T) so that every cluster runs in one wave,
+at least 1, capped by max_splits (default 32) and by ceil(W / 64) (at least 64
+columns per split), then raised to ceil(W / 2304) (the columns one CTA stages).
+A forced num_splits below that minimum is an error.  The CUDA-core kernel
+targets 2 resident CTAs per SM with at least 256 columns per split.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from sparse_mla_decode_token_gb300 import binding as B
+from sparse_mla_decode_token_gb300 import build as smla_build
+from sparse_mla_decode_token_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GB300_SMS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    smla_build.build()
+    return B.lib()
+
+
+def args(T, W_, *, H=128, dtype=B.SMLA_E4M3, batch=None, varlen=False, num_splits=0, max_splits=0,
+         kernel=B.KERNEL_AUTO):
+    a = B.SmlaArgs()
+    a.sum_q, a.batch, a.num_heads, a.width, a.dtype = T, batch or max(T, 1), H, W_, dtype
+    if varlen:
+        a.cum_seq_lens_q = 16                 # marks varlen; never read by the planner
+    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    return a
+
+
+def plan(a, sms=GB300_SMS):
+    return B.smla_plan_decode_for_sm_count(a, sms).as_dict()
+
+
+def expected_tc_splits(T, W_, max_splits=0, sms=GB300_SMS):
+    pairs = sms // 2
+    want = pairs // T if T > 0 else 1
+    want = min(want, math.ceil(W_ / 64), max_splits or 32)
+    want = max(want, math.ceil(W_ / 2304))
+    return max(want, 1)
+
+
+def workload_args(n):
+    w = W.config_workload(n)
+    dt = B.SMLA_BF16 if w.dtype == "bf16" else B.SMLA_E4M3
+    return args(w.sum_q, w.width, H=w.num_heads, dtype=dt, batch=w.batch,
+                varlen=w.cum_seq_lens_q is not None)
+
+
+def test_plans_of_the_committed_traffic_records():
+    """traffic.json stores the launch plan of each ncu capture; the planner
+    still produces exactly that plan for the workload on a GB300."""
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    by_name = {name: n for n, name in W.CONFIG_NAMES.items()}
+    checked = 0
+    for name, ent in rec.items():
+        if name.startswith("_"):
+            continue
+        got = plan(workload_args(by_name[name]))
+        for k, v in ent["plan"].items():
+            assert got[k] == v, (name, k, got[k], v)
+        checked += 1
+    assert checked == 4
+
+
+@pytest.mark.parametrize("n,splits,grid", [(1, 4, 16), (2, 2, 128), (3, 1, 256), (4, 1, 324),
+                                           (5, 19, 152), (6, 1, 256)])
+def test_named_workload_plans(n, splits, grid):
+    p = plan(workload_args(n))
+    assert (p["kernel"], p["num_splits"], p["grid"], p["ctas_per_split"]) == (B.KERNEL_TCGEN05, splits, grid, 2)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 7, 19, 38, 75, 76, 77, 128, 1000])
+@pytest.mark.parametrize("W_", [128, 129, 256, 640, 2176, 2304, 2305, 4608, 16512, 65536])
+@pytest.mark.parametrize("max_splits", [0, 1, 8])
+def test_tc_split_rule(T, W_, max_splits):
+    p = plan(args(T, W_, max_splits=max_splits))
+    S = p["num_splits"]
+    assert S == expected_tc_splits(T, W_, max_splits)
+    assert p["grid"] == T * S * 2
+    assert S >= math.ceil(W_ / 2304)                       # no split stages more than 2304 columns
+    if S > math.ceil(W_ / 2304):
+        assert T * S <= GB300_SMS // 2                      # extra splits only while one wave holds
+    # workspace: BF16 partials + fp32 LSEs, each 256-byte aligned; none for S = 1
+    rows = T * 128 * S
+    want_ws = 0 if S == 1 else (-(-rows * 512 * 2 // 256) * 256 + -(-rows * 4 // 256) * 256)
+    assert p["workspace_bytes"] == want_ws
+
+
+def test_sm_count_scales_the_split():
+    a = args(4, 16512)
+    assert plan(a, 152)["num_splits"] == 19
+    assert plan(a, 304)["num_splits"] == 32                  # capped by the default max_splits
+    assert plan(a, 16)["num_splits"] == 8                    # ceil(16512 / 2304) = 8 is the floor
+
+
+def test_forced_splits():
+    assert plan(args(3, 2176, num_splits=5))["num_splits"] == 5
+    with pytest.raises(B.SmlaError) as e:
+        plan(args(3, 4608 + 1, num_splits=2))                 # needs >= 3 splits of <= 2304 columns
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG and "num_splits 2 < 3" in str(e.value)
+
+
+def test_cuda_core_rule():
+    for T, W_, H in ((1, 2176, 128), (32, 640, 128), (128, 2176, 64), (4, 16512, 128)):
+        p = plan(args(T, W_, H=H, kernel=B.KERNEL_CUDA_CORE))
+        units = T * p["ctas_per_split"]
+        want = min(math.ceil(GB300_SMS * 2 / units), math.ceil(W_ / 256), 32)
+        assert p["kernel"] == B.KERNEL_CUDA_CORE and p["num_splits"] == max(want, 1)
+        assert p["grid"] == T * p["num_splits"] * p["ctas_per_split"]
+
+
+def test_bad_sm_count_and_null_plan():
+    with pytest.raises(B.SmlaError) as e:
+        plan(args(1, 256), sms=0)
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG and "sm_count" in str(e.value)
+    assert B.lib().smla_plan_decode_for_sm_count(None, 152, None) == B.SMLA_ERR_INVALID_ARG
+
+
+def test_shape_errors_match_the_decode_call():
+    a = args(1, 100)                                         # width < 128 SWA columns
+    with pytest.raises(B.SmlaError) as e:
+        plan(a)
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG and "width" in str(e.value)
+
+
+@pytest.mark.gpu
+def test_device_plan_equals_the_sm_count_plan():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for n in (1, 2, 3, 5):
+        a = workload_args(n)
+        assert B.smla_plan_decode(a, 0).as_dict() == B.smla_plan_decode_for_sm_count(a, sms).as_dict()
