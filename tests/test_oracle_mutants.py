@@ -106,6 +106,14 @@ MUTANTS = [
      pins.test_single_valid_slot_returns_row_times_bmm2),
     ("lse_natural_log", "attend", "* LOG2E", "* 1.0", pins.test_two_slot_worked_example),
     ("lse_missing_max", "attend", "lse2 = (m + np.log(", "lse2 = (np.log(", pins.test_two_slot_worked_example),
+    ("max_not_subtracted", "attend", "e = np.exp(logits - m[:, None])", "e = np.exp(logits)",
+     pins.test_dominant_logit_selects_its_row_without_overflow),
+    ("sink_dropped_from_normaliser", "attend", "o = bmm2 * (e @ kv) / denom[:, None]",
+     "o = bmm2 * (e @ kv) / z[:, None]", pins.test_sink_limits),
+    ("bmm2_applied_twice", "attend", "o = bmm2 * (e @ kv)", "o = bmm2 * bmm2 * (e @ kv)",
+     pins.test_output_is_linear_in_bmm2_and_lse_ignores_it),
+    ("bmm1_squared", "attend", "logits = bmm1 * (q_t @ kv.T)", "logits = bmm1 * bmm1 * 8.0 * (q_t @ kv.T)",
+     pins.test_power_of_two_query_scale_trades_with_bmm1),
     ("pv_rows_reversed", "attend", "(e @ kv)", "(e @ kv[::-1])", pins.test_two_slot_worked_example),
     ("softmax_over_heads", "attend", "m = logits.max(axis=1)", "m = logits.max(axis=1).max()",
      pins.test_zero_query_gives_mean_and_log2_n),

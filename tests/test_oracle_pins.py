@@ -229,6 +229,60 @@ def test_duplicate_index_counts_twice():
     assert lse[0, 0] == pytest.approx(math.log2(2 * e + 1), abs=1e-15)
 
 
+def test_dominant_logit_selects_its_row_without_overflow():
+    """Logits near 1e3 (e^1000 overflows float64): the largest logit's row
+    takes all the weight; O = that row * bmm2, LSE2 = its logit in base 2."""
+    q = np.zeros((1, 1, 512)); q[0, 0, 0] = 64.0
+    comp = np.zeros((8, 512))
+    comp[2, 0], comp[5, 0], comp[6, 0] = 16.0, 15.0, 14.0          # logits 1024, 960, 896 (bmm1 = 1)
+    comp[2, 1], comp[5, 2] = 3.0, 5.0
+    o, lse = case(H=1, q=q, comp=comp, indices=table([], [5, 2, 6]), bmm1=1.0, bmm2=0.5)
+    assert np.all(np.isfinite(o)) and np.isfinite(lse[0, 0])
+    np.testing.assert_allclose(o[0, 0], 0.5 * comp[2], rtol=0, atol=1e-25)
+    assert lse[0, 0] == pytest.approx(1024.0 * LOG2E, rel=1e-15)
+
+
+def test_sink_limits():
+    """A very negative sink is no sink; a very large one sends O to 0 while
+    the LSE (sink excluded) stays.  Sinks of +-600 keep e^{sink - max logit}
+    inside float64's range, so no step relies on overflow."""
+    rng = np.random.default_rng(12)
+    q, swa, comp, idx = _random_case(rng, T=1)
+    kw = dict(H=4, q=q, swa=swa, comp=comp, indices=idx)
+    o0, l0 = case(**kw)
+    o1, l1 = case(sinks=np.full(4, -600.0, np.float32), **kw)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+    o2, l2 = case(sinks=np.full(4, 600.0, np.float32), **kw)
+    assert 0 < np.abs(o2).max() < 1e-240
+    np.testing.assert_array_equal(l0, l2)
+
+
+def test_output_is_linear_in_bmm2_and_lse_ignores_it():
+    rng = np.random.default_rng(13)
+    q, swa, comp, idx = _random_case(rng, T=2)
+    kw = dict(H=4, q=q, swa=swa, comp=comp, indices=idx, seq_lens=[10 ** 6] * 2,
+              sinks=np.array([0.3, -1.0, 2.0, 0.0], np.float32))
+    o1, l1 = case(bmm2=1.0, **kw)
+    o3, l3 = case(bmm2=3.0, **kw)
+    np.testing.assert_allclose(o3, 3.0 * o1, rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(l1, l3)
+
+
+def test_power_of_two_query_scale_trades_with_bmm1():
+    """BF16 q * 2 is exact, so (2q, bmm1 / 2) gives bit-identical logits."""
+    rng = np.random.default_rng(14)
+    q, swa, comp, idx = _random_case(rng, T=1)
+    kw = dict(H=4, swa=swa, comp=comp, indices=idx, sinks=np.array([0.5, 0.0, -0.5, 1.0], np.float32))
+    qb = bf16_round(q)
+    o1, l1 = case(q=qb, bmm1=0.125, **kw)
+    o2, l2 = case(q=2.0 * qb, bmm1=0.0625, **kw)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    o3, _ = case(q=qb, bmm1=0.0625, **kw)                 # and bmm1 does matter
+    assert np.abs(o3 - o1).max() > 1e-6
+
+
 # ------------------------------------------------------------ invariants
 
 def _random_case(rng, T=3, H=4, n_comp=40, width=128 + 64, comp_rows=100):
