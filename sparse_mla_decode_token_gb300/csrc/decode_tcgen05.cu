@@ -411,7 +411,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // Producer group pg (kWarpsPerGroup warps) gathers tiles pg, pg + kProducerGroups, ...
     constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
     const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
-    for (int j = pg; j < ntiles; j += kProducerGroups) {
+    int j = pg;                              // after the loop: past the last tile this group issued
+    for (; j < ntiles; j += kProducerGroups) {
       const int st = j % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
       const int start = tile_start(j), n = tile_n(j);
@@ -445,9 +446,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    // leave no TMA write of this warp in flight (normally the consumers have waited for all of them)
-    for (int j = max(0, ntiles - C::kStages); j < ntiles; ++j)
-      warp_wait(cx, bar(sm.kv_full[j % C::kStages]), (j / C::kStages) & 1);
+    // Leave no TMA write of this group in flight, also after an abort: wait
+    // (bounded, not cut short by the abort flag) for the last tiles it issued,
+    // at most one per stage.  Normally the consumers have waited for them.
+    for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
+      if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
   } else if (warp == kMmaWarp) {
     // ============================================================ QK issue
     // QK and PV are issued by different warps so that a QK never waits behind
