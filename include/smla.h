@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 3
+#define SMLA_ABI_VERSION 4
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -187,6 +187,28 @@ smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan)
  * smla_plan_decode.
  */
 smla_status smla_plan_decode_for_sm_count(const smla_args* args, int sm_count, smla_plan* plan);
+
+/*
+ * Opt-in validation of a call's index data on HOST copies: sparse_indices,
+ * sparse_topk_lens, seq_lens, cum_seq_lens_q, comp_block_tables,
+ * hca_seq_lens and swa_topk_lens must point to host memory here; q, the
+ * pools, out and the other device pointers are ignored.  After the shape
+ * checks of smla_decode it reports what the contract calls an error or leaves
+ * undefined, by location:
+ *   - a cum_seq_lens_q that does not start at 0, decreases or does not end
+ *     at sum_q;
+ *   - an index the kernels would read that is neither -1 nor a row of its
+ *     pool;
+ *   - a page-table slot the kernels would read whose row lies outside the
+ *     compressed pool.
+ * Lengths are clamped as the kernels clamp them (sparse_topk_lens to
+ * [0, width], the window to [0, 128], the footprint by hca_seq_lens), and
+ * entries the kernels never read are not checked.  Returns
+ * SMLA_ERR_INVALID_ARG with the first bad entry's location in
+ * smla_last_error().  smla_decode does not call it: the kernels mask and flag
+ * bad indices instead (SMLA_DEVERR_INDEX_OUT_OF_RANGE).
+ */
+smla_status smla_validate_host(const smla_args* args);
 
 /* Workspace bytes smla_decode will need for these args on `device`. */
 smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes);

@@ -80,6 +80,7 @@ EXPORTS = {
     "smla_plan_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(SmlaPlan)]),
     "smla_plan_decode_for_sm_count": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int,
                                                      ctypes.POINTER(SmlaPlan)]),
+    "smla_validate_host": (ctypes.c_int, [ctypes.POINTER(SmlaArgs)]),
     "smla_workspace_size": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "smla_decode": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
     "smla_decode_static_workspace": (ctypes.c_int, [ctypes.POINTER(SmlaArgs), _c_void_p]),
@@ -135,6 +136,36 @@ def smla_plan_decode_for_sm_count(args: SmlaArgs, sm_count: int) -> SmlaPlan:
     plan = SmlaPlan()
     _check(lib().smla_plan_decode_for_sm_count(ctypes.byref(args), sm_count, ctypes.byref(plan)))
     return plan
+
+
+def smla_validate_host(args: SmlaArgs) -> None:
+    """Check a call's index data; its index-data pointers must be HOST memory
+    (raises ``SmlaError`` naming the first bad entry)."""
+    _check(lib().smla_validate_host(ctypes.byref(args)))
+
+
+def _validate_on_host(a: SmlaArgs, **tensors) -> None:
+    """``smla_validate_host`` on host copies of the call's index data (one
+    device-to-host copy each: a debugging aid, enabled by SMLA_VALIDATE=1)."""
+    h = SmlaArgs.from_buffer_copy(a)
+    keep = []
+
+    def host(t):
+        c = t.detach().to("cpu").contiguous()
+        keep.append(c)
+        return c
+
+    si = host(tensors["sparse_indices"])
+    h.sparse_indices, h.indices_row_stride = si.data_ptr(), si.stride(0)
+    h.seq_lens = host(tensors["seq_lens"]).data_ptr()
+    for name in ("sparse_topk_lens", "cum_seq_lens_q", "hca_seq_lens", "swa_topk_lens"):
+        t = tensors.get(name)
+        setattr(h, name, None if t is None else host(t).data_ptr())
+    bt = tensors.get("comp_block_tables")
+    if bt is not None:
+        bt = host(bt)
+        h.comp_block_tables, h.block_table_stride = bt.data_ptr(), bt.stride(0)
+    smla_validate_host(h)
 
 
 def smla_workspace_size(args: SmlaArgs, device: int = 0) -> int:
@@ -261,18 +292,6 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     if sparse_indices.shape[0] < T:
         raise ValueError(f"sparse_indices has {sparse_indices.shape[0]} rows for {T} query tokens")
 
-    dev = q.device
-    for name, t in (("q", q), ("swa_kv", swa_kv), ("compressed_kv", compressed_kv),
-                    ("sparse_indices", sparse_indices), ("seq_lens", seq_lens), ("out", out),
-                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
-                    ("sinks", sinks), ("out_lse", out_lse), ("workspace", workspace),
-                    ("error_word", error_word), ("bmm1_scale", bmm1_scale), ("bmm2_scale", bmm2_scale),
-                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
-                    ("hca_seq_lens", hca_seq_lens)):
-        if isinstance(t, torch.Tensor) and (t.device.type != "cuda" or t.device != dev):
-            raise ValueError(f"{name} is on {t.device}; every tensor must be on the CUDA device of q ({dev})")
-    if dev.type != "cuda":
-        raise ValueError(f"q is on {dev}; the decode runs on a CUDA device")
     swa_rows, swa_stride = _rows_and_stride(swa_kv)
     comp_rows, comp_stride = _rows_and_stride(compressed_kv)
     a = SmlaArgs()
@@ -312,6 +331,23 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
         a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
     a.error_word = _ptr(error_word)
+    if os.environ.get("SMLA_VALIDATE") == "1":
+        _validate_on_host(a, sparse_indices=sparse_indices, seq_lens=seq_lens, sparse_topk_lens=sparse_topk_lens,
+                          cum_seq_lens_q=cum_seq_lens_q, hca_seq_lens=hca_seq_lens, swa_topk_lens=swa_topk_lens,
+                          comp_block_tables=comp_block_tables)
+
+    dev = q.device
+    for name, t in (("q", q), ("swa_kv", swa_kv), ("compressed_kv", compressed_kv),
+                    ("sparse_indices", sparse_indices), ("seq_lens", seq_lens), ("out", out),
+                    ("sparse_topk_lens", sparse_topk_lens), ("cum_seq_lens_q", cum_seq_lens_q),
+                    ("sinks", sinks), ("out_lse", out_lse), ("workspace", workspace),
+                    ("error_word", error_word), ("bmm1_scale", bmm1_scale), ("bmm2_scale", bmm2_scale),
+                    ("swa_topk_lens", swa_topk_lens), ("comp_block_tables", comp_block_tables),
+                    ("hca_seq_lens", hca_seq_lens)):
+        if isinstance(t, torch.Tensor) and (t.device.type != "cuda" or t.device != dev):
+            raise ValueError(f"{name} is on {t.device}; every tensor must be on the CUDA device of q ({dev})")
+    if dev.type != "cuda":
+        raise ValueError(f"q is on {dev}; the decode runs on a CUDA device")
     return a
 
 

@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <string>
 
@@ -118,6 +119,80 @@ smla_status check_pointers(const smla_args* a) {
   };
   for (const auto& w : words)
     if (w.ptr && !aligned(w.ptr, 4)) return fail(SMLA_ERR_INVALID_ARG, "%s must be 4-byte aligned", w.name);
+  return SMLA_OK;
+}
+
+// Opt-in host validation of a call's index data (host copies).  It reports
+// what the operation's contract calls an error -- a read index or page-table
+// row outside its pool, which the kernels mask and flag -- and what it leaves
+// undefined: a cum_seq_lens_q that does not start at 0, decreases or does not
+// end at sum_q.  Lengths the contract clamps (sparse_topk_lens,
+// swa_topk_lens, hca_seq_lens, a seq_len shorter than its query) are clamped
+// here as in the kernels: token t of request b sits at position
+// seq_lens[b] - q_len + i; SWA column j < 128 is read when j < n_lim and
+// j < the window; compressed column j >= 128 when j < n_lim; in the
+// page-table form slot c when c < n_lim - 128, n_lim being capped at
+// max(128, hca_seq_lens[b]).  The first bad entry is reported by location.
+smla_status validate_host(const smla_args* a) {
+  smla_status st = check_shapes(a);
+  if (st != SMLA_OK) return st;
+  if (a->sum_q == 0) return SMLA_OK;
+  if (!a->sparse_indices || !a->seq_lens)
+    return fail(SMLA_ERR_INVALID_ARG, "sparse_indices and seq_lens are required");
+  const bool paged = a->comp_block_tables != nullptr;
+  if (paged && !a->hca_seq_lens) return fail(SMLA_ERR_INVALID_ARG, "hca_seq_lens is required with comp_block_tables");
+  const int T = a->sum_q, B = a->batch, W = a->width;
+  const int32_t* cum = a->cum_seq_lens_q;
+  if (cum) {
+    if (cum[0] != 0) return fail(SMLA_ERR_INVALID_ARG, "cum_seq_lens_q[0] = %d, not 0", cum[0]);
+    for (int b = 0; b < B; ++b)
+      if (cum[b + 1] < cum[b])
+        return fail(SMLA_ERR_INVALID_ARG, "cum_seq_lens_q gives request %d a negative length (%d -> %d)", b,
+                    cum[b], cum[b + 1]);
+    if (cum[B] != T) return fail(SMLA_ERR_INVALID_ARG, "cum_seq_lens_q[%d] = %d, not sum_q = %d", B, cum[B], T);
+  }
+  const int64_t is = a->indices_row_stride ? a->indices_row_stride : (paged ? kSwaCols : W);
+  const int64_t bts = paged ? (a->block_table_stride ? a->block_table_stride : a->comp_max_pages) : 0;
+  int b = 0;
+  for (int t = 0; t < T; ++t) {
+    int i, q_len;
+    if (cum) {
+      while (cum[b + 1] <= t) ++b;         // cum[B] == T > t: ends at a request that holds t
+      i = t - cum[b];
+      q_len = cum[b + 1] - cum[b];
+    } else {
+      q_len = T / B;
+      b = t / q_len;
+      i = t - b * q_len;
+    }
+    const int64_t visible = a->swa_topk_lens ? (int64_t)a->swa_topk_lens[t] : (int64_t)a->seq_lens[b] - q_len + i + 1;
+    const int w = (int)std::min<int64_t>(kSwaCols, std::max<int64_t>(0, visible));
+    int n_lim = std::min(std::max(a->sparse_topk_lens ? a->sparse_topk_lens[t] : W, 0), W);
+    if (paged) n_lim = std::min(n_lim, std::max(kSwaCols, a->hca_seq_lens[b]));
+    const int32_t* row = a->sparse_indices + (int64_t)t * is;
+    for (int j = 0; j < std::min(n_lim, w); ++j)
+      if (row[j] != -1 && (row[j] < -1 || row[j] >= a->swa_rows))
+        return fail(SMLA_ERR_INVALID_ARG, "token %d (request %d) column %d: index %d outside the SWA pool of %lld rows",
+                    t, b, j, row[j], (long long)a->swa_rows);
+    if (!paged) {
+      for (int j = kSwaCols; j < n_lim; ++j)
+        if (row[j] != -1 && (row[j] < -1 || row[j] >= a->comp_rows))
+          return fail(SMLA_ERR_INVALID_ARG,
+                      "token %d (request %d) column %d: index %d outside the compressed pool of %lld rows", t, b, j,
+                      row[j], (long long)a->comp_rows);
+    } else {
+      const int32_t* bt = a->comp_block_tables + (int64_t)t * bts;
+      for (int c = 0; c < n_lim - kSwaCols; ++c) {
+        const int64_t page = bt[c / a->comp_page_size];
+        const int64_t r = page * a->comp_page_size + c % a->comp_page_size;
+        if (page < 0 || r >= a->comp_rows)
+          return fail(SMLA_ERR_INVALID_ARG,
+                      "token %d (request %d) compressed slot %d: page %lld (table column %d) gives row %lld, outside "
+                      "the compressed pool of %lld rows",
+                      t, b, c, (long long)page, c / a->comp_page_size, (long long)r, (long long)a->comp_rows);
+      }
+    }
+  }
   return SMLA_OK;
 }
 
@@ -230,6 +305,8 @@ smla_status smla_plan_decode_for_sm_count(const smla_args* args, int sm_count, s
   if (plan == nullptr) return fail(SMLA_ERR_INVALID_ARG, "plan is NULL");
   return make_plan_for(args, sm_count, plan);
 }
+
+smla_status smla_validate_host(const smla_args* args) { return validate_host(args); }
 
 smla_status smla_workspace_size(const smla_args* args, int device, size_t* bytes) {
   if (bytes == nullptr) return fail(SMLA_ERR_INVALID_ARG, "bytes is NULL");
