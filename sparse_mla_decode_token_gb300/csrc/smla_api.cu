@@ -214,10 +214,8 @@ smla_status sm_count(int device, int* out) {
 }
 
 // The plan as a pure function of the shapes, the split controls and the SM
-// count (no device is queried).
-smla_status make_plan_for(const smla_args* a, int sms, smla_plan* plan) {
-  smla_status st = check_shapes(a);
-  if (st != SMLA_OK) return st;
+// count (no device is queried).  The caller has checked the shapes.
+smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
@@ -274,13 +272,14 @@ smla_status make_plan_for(const smla_args* a, int sms, smla_plan* plan) {
   return SMLA_OK;
 }
 
+// Plan for a device ordinal: shapes are checked before the device is queried.
 smla_status make_plan(const smla_args* a, int device, smla_plan* plan) {
-  smla_status st = check_shapes(a);   // shape errors come before the device query
+  smla_status st = check_shapes(a);
   if (st != SMLA_OK) return st;
   int sms = 0;
   st = sm_count(device, &sms);
   if (st != SMLA_OK) return st;
-  return make_plan_for(a, sms, plan);
+  return plan_checked(a, sms, plan);
 }
 
 }  // namespace
@@ -303,7 +302,9 @@ smla_status smla_plan_decode(const smla_args* args, int device, smla_plan* plan)
 
 smla_status smla_plan_decode_for_sm_count(const smla_args* args, int sm_count, smla_plan* plan) {
   if (plan == nullptr) return fail(SMLA_ERR_INVALID_ARG, "plan is NULL");
-  return make_plan_for(args, sm_count, plan);
+  smla_status st = check_shapes(args);
+  if (st != SMLA_OK) return st;
+  return plan_checked(args, sm_count, plan);
 }
 
 smla_status smla_validate_host(const smla_args* args) { return validate_host(args); }
@@ -327,8 +328,11 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   int device = 0;
   cudaError_t ce = cudaGetDevice(&device);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  int sms = 0;
+  st = sm_count(device, &sms);
+  if (st != SMLA_OK) return st;
   smla_plan plan;
-  st = make_plan(a, device, &plan);
+  st = plan_checked(a, sms, &plan);
   if (st != SMLA_OK) return st;
   if (plan.workspace_bytes > 0) {
     if (a->workspace == nullptr || a->workspace_bytes < plan.workspace_bytes)
