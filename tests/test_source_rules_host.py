@@ -1,9 +1,8 @@
 """Static rules over the committed sources (CPU): device code never traps,
 every mbarrier wait goes through a bounded wait, nothing uses multi-GPU
-multicast, every ncu
-command in the profile summaries leaves the clocks alone, nothing changes a
-GPU's settings, and code and comments stand on their own (no build notes or
-machine paths)."""
+multicast, every ncu command in the profile summaries leaves the clocks
+alone, nothing changes a GPU's settings, and code and comments stand on their
+own (no build notes or machine paths)."""
 import os
 import re
 
