@@ -105,19 +105,29 @@ def recorded_traffic(workload: str, plan: dict):
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     if it was taken on the current device code with this run's launch plan;
     else None."""
+    return traffic_record(workload, plan)[0]
+
+
+def traffic_record(workload: str, plan: dict):
+    """(DRAM bytes per launch or None, a note saying where it came from or why
+    there is none)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, "no profiles/traffic.json"
     ent = rec.get(workload)
-    if not ent or ent.get("kernel_sources_sha") != kernel_sources_sha():
-        return None
+    if not ent:
+        return None, f"no ncu capture of workload {workload}"
+    sha = kernel_sources_sha()
+    if ent.get("kernel_sources_sha") != sha:
+        return None, (f"the capture was taken on device code {ent.get('kernel_sources_sha')}; "
+                      f"the current device code is {sha}")
     want = ent.get("plan")
     if not want or any(want.get(k) != plan.get(k) for k in PLAN_KEYS):
-        return None
-    return ent.get("dram_bytes_per_launch")
+        return None, f"the capture's launch plan {want} differs from this run's"
+    return ent.get("dram_bytes_per_launch"), f"profiles/traffic.json, device code {sha}, same launch plan"
 
 
 # -------------------------------------------------------------------- clocks
@@ -504,7 +514,7 @@ def run_gpu(args):
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["traffic"] = recorded_traffic(W.CONFIG_NAMES[args.config], plan.as_dict())
+    roof["traffic"], roof["traffic_source"] = traffic_record(W.CONFIG_NAMES[args.config], plan.as_dict())
     roof["algorithmic_bytes_per_launch"] = gathered_bytes
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
     roof["main_kernel_us"] = 1e6 * main_s

@@ -64,6 +64,8 @@ def test_recorded_traffic_needs_the_same_device_code_and_plan(monkeypatch):
     assert bench.recorded_traffic("no_such_workload", plan) is None
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "0" * 16)
     assert bench.recorded_traffic(name, plan) is None
+    value, note = bench.traffic_record(name, plan)
+    assert value is None and rec[name]["kernel_sources_sha"] in note and "0" * 16 in note
 
 
 def test_host_only_sources_hold_no_device_code():
