@@ -75,3 +75,11 @@ def test_host_only_sources_hold_no_device_code():
         code = bench.code_only(open(os.path.join(csrc, f)).read())
         for word in ("__global__", "__device__", "__constant__", "__shared__", "asm(", "asm volatile"):
             assert word not in code, (f, word)
+
+
+def test_cpu_baseline_cycles_the_workload_until_its_budget():
+    w = W.config_workload(1)                                  # 2 tokens: a fraction of a second
+    done, seconds = bench.time_oracle(w, 0.3)
+    assert done > w.sum_q and seconds >= 0.3
+    done, _ = bench.time_oracle(w, 1e9, max_tokens=3)
+    assert done == 3
