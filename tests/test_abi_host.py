@@ -285,14 +285,18 @@ def test_binding_well_formed_host_call_fails_only_on_placement():
         B.make_args(**_host_call(q=torch.zeros(2, 2, 64, 512, dtype=torch.bfloat16)))
 
 
-def test_plain_c_caller_links_and_runs(lib, tmp_path):
-    """A C program (no Python, no CUDA headers) links libsmla.so and gets
-    plans and host-side statuses from it without a GPU."""
+@pytest.mark.parametrize("compiler", [["gcc", "-std=c99"], ["g++", "-std=c++17", "-x", "c++"]],
+                         ids=["c99", "c++17"])
+def test_plain_c_caller_links_and_runs(lib, tmp_path, compiler):
+    """A C program (no Python, no CUDA headers), built as C99 and as C++,
+    links libsmla.so and gets plans and host-side statuses from it without a
+    GPU."""
     src = os.path.join(ROOT, "tests", "c", "abi_from_c.c")
     exe = tmp_path / "abi_from_c"
     libdir = os.path.dirname(B.LIB_PATH)
-    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
-                    src, "-o", str(exe), "-L", libdir, "-lsmla", f"-Wl,-rpath,{libdir}"], check=True)
+    subprocess.run(compiler + ["-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                               src, "-x", "none", "-o", str(exe), "-L", libdir, "-lsmla", f"-Wl,-rpath,{libdir}"],
+                   check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "FAIL" not in r.stdout and r.stdout.count("ok ") == 10
