@@ -115,3 +115,19 @@ def test_code_and_comments_stand_on_their_own():
         text = open(path, errors="ignore").read()
         for n in needles:
             assert n not in text, (os.path.relpath(path, ROOT), n)
+
+
+def test_the_product_never_imports_the_oracle():
+    """The library package and build() leave the oracle unimported (only the
+    tests, smoke() and the benchmark's CPU-baseline leg may run it)."""
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "sparse_mla_decode_token_gb300")
+    for path in files((".py",), pkg):
+        text = open(path).read()
+        assert not re.search(r"^\s*(import oracle|from oracle)", text, flags=re.M), path
+    code = ("import sys; import __graft_entry__ as g; g.build(); "
+            "import sparse_mla_decode_token_gb300.binding, sparse_mla_decode_token_gb300.workloads; "
+            "assert 'oracle' not in sys.modules and 'oracle.oracle' not in sys.modules, sorted(sys.modules)")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
