@@ -83,3 +83,26 @@ def test_cpu_baseline_cycles_the_workload_until_its_budget():
     assert done > w.sum_q and seconds >= 0.3
     done, _ = bench.time_oracle(w, 1e9, max_tokens=3)
     assert done == 3
+
+
+def test_clock_summary_reports_median_max_and_throttle_reasons(tmp_path):
+    """The clocks entry of the JSON line from nvidia-smi's CSV samples
+    (noheader, nounits): the median SM clock under load, the maximum, and
+    every throttle reason seen Active (a run with a slowdown is rejected)."""
+    csv = tmp_path / "clocks.csv"
+    na = "Not Active"
+    csv.write_text("\n".join([
+        f"0, 2070, 2070, 610.5, 0x0000000000000000, {na}, {na}, {na}, {na}",
+        f"0, 1900, 2070, 1395.0, 0x0000000000000004, {na}, {na}, {na}, Active",
+        f"0, 2000, 2070, 700.0, 0x0000000000000008, Active, {na}, {na}, {na}",
+        f"0, 1980, 2070, [N/A], 0x0000000000000000, {na}, {na}, {na}, {na}",   # unparsable: skipped
+        "garbage line",
+    ]) + "\n")
+    s = bench.ClockSampler(0)
+    s.proc, s.path = object(), str(csv)
+    out = s.summary()
+    assert out["sm_mhz"] == 2000 and out["sm_max_mhz"] == 2070 and out["samples"] == 3
+    assert out["power_w_max"] == 1395.0
+    assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    s2 = bench.ClockSampler(0)
+    assert s2.summary()["reasons"] == ["nvidia-smi unavailable"]
