@@ -106,3 +106,11 @@ def test_clock_summary_reports_median_max_and_throttle_reasons(tmp_path):
     assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
     s2 = bench.ClockSampler(0)
     assert s2.summary()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_roofline_peaks_come_from_the_measured_file_else_the_fallback(monkeypatch, tmp_path):
+    import json
+    rec = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    assert bench.peaks() == (rec["hbm_gbs"], rec["bf16_tflops"], "measured")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))                  # no measured file there
+    assert bench.peaks() == (6800.0, 1900.0, "fallback")              # the recipe's fallback figures
