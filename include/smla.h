@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 4
+#define SMLA_ABI_VERSION 5
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -63,11 +63,19 @@ typedef enum smla_dtype {
   SMLA_E4M3 = 1                    /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */
 } smla_dtype;
 
-/* Kernel selection (smla_args.kernel).  AUTO picks the tensor-core kernel. */
+/* Kernel selection (smla_args.kernel).  AUTO picks the tensor-core kernel.
+ * The tensor-core kernels run each (token, split) on a pair of CTAs, CTA r
+ * keeping output dims [256 r, 256 r + 256) of every head; they differ in
+ * where the softmax runs.  TCGEN05: both CTAs add the peer's partial logits
+ * and run the softmax of every head.  TCGEN05_HEAD_OWNED (E4M3 rows; BF16
+ * rows take TCGEN05): each CTA runs the softmax of half the heads and sends
+ * the peer their E4M3 P; it moves fewer bytes between the CTAs but is slower
+ * (a round trip per tile), and is kept as an alternative. */
 typedef enum smla_kernel {
   SMLA_KERNEL_AUTO = 0,
-  SMLA_KERNEL_CUDA_CORE = 1,       /* plain CUDA-core kernel (fp32 FMA) */
-  SMLA_KERNEL_TCGEN05 = 2          /* tcgen05 / TMEM tensor-core kernel */
+  SMLA_KERNEL_CUDA_CORE = 1,          /* plain CUDA-core kernel (fp32 FMA) */
+  SMLA_KERNEL_TCGEN05 = 2,            /* tcgen05 / TMEM tensor-core kernel */
+  SMLA_KERNEL_TCGEN05_HEAD_OWNED = 3  /* tcgen05 kernel, softmax split between the CTAs by head */
 } smla_kernel;
 
 /* Bits the kernels OR into *error_word (device-side detection, no trap). */
@@ -162,7 +170,7 @@ typedef struct smla_args {
 
 /* The resolved launch plan (shape-based: it never reads device memory). */
 typedef struct smla_plan {
-  int32_t kernel;            /* smla_kernel actually used */
+  int32_t kernel;            /* smla_kernel actually used (TCGEN05_HEAD_OWNED on BF16 rows reports TCGEN05) */
   int32_t num_splits;        /* S: column ranges per token; S > 1 adds a combine launch */
   int32_t ctas_per_split;    /* CTAs cooperating on one (token, split) */
   int32_t grid;              /* CTAs of the main decode launch */

@@ -10,16 +10,17 @@
 //                       slots (per-warp ballots and scans) into a list: SWA
 //                       slots, then compressed slots; tiles are runs of N list
 //                       entries of one pool (masked slots are never loaded)
-//   producer warps 0-5  the pair's half of every selected row (256 dims) with
+//   producer warps 0-3  the pair's half of every selected row (256 dims) with
 //                       TMA tile::gather4 (four rows of 128 bytes per request)
 //                       into a 128-byte-swizzled, UMMA-canonical shared-memory
 //                       tile of a 7-stage (E4M3) or 6-stage (BF16) ring; a
 //                       warp's TMA requests are served one after another, so a
-//                       tile's 32 requests are spread over the three warps of
+//                       tile's 32 requests are spread over the two warps of
 //                       one of two groups taking alternate tiles; a tile of N
 //                       consecutive rows is one box copy per 128-byte block
-//   QK warp 6           S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
-//                       into one of three TMEM S buffers; also allocates and
+//   QK warps 4-6        S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
+//                       into one of three TMEM S buffers, warp 4 + b issuing
+//                       the tiles of buffer b; warp 4 also allocates and
 //                       frees TMEM
 //   PV warp 7           O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
 //                       P read from TMEM); a separate issuer so that no QK
@@ -56,19 +57,22 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace smla {
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
 constexpr int kMaxN = 64;            // largest tile (slots per tile)
 constexpr int kHalfDims = 256;       // output dims per CTA
-constexpr int kProducerWarps = 6;    // TMA gathers
-constexpr int kProducerGroups = 2;   // tiles alternate between two groups of three warps that share each tile
-constexpr int kMmaWarp = kProducerWarps;        // QK issue; allocates and frees TMEM
-constexpr int kPvWarp = kMmaWarp + 1;           // PV issue
+constexpr int kProducerWarps = 4;    // TMA gathers
+constexpr int kProducerGroups = 2;   // tiles alternate between two groups of two warps that share each tile
+constexpr int kMmaWarp = kProducerWarps;        // first QK issuer; allocates and frees TMEM
+constexpr int kQkWarps = 3;                     // QK issuers: warp kMmaWarp + i issues the tiles k with k % 3 == i
+constexpr int kPvWarp = kMmaWarp + kQkWarps;    // PV issue
 constexpr int kSoftmaxWarp0 = kPvWarp + 1;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
@@ -80,13 +84,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
 constexpr uint32_t kSCol = 256;      // S: three buffers of N fp32 columns, then P: two buffers of 16 columns
 constexpr int kSBufs = 3;
+static_assert(kQkWarps == kSBufs, "one QK issuer per S buffer");
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr int kExactRefTiles = 8;          // E4M3 P: chains of at most this many tiles follow the exact maximum
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxStages = 8;
 
 struct TcSmall {
-  uint64_t q_full;
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];
   uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[2], p_empty[2];
@@ -94,7 +97,8 @@ struct TcSmall {
   uint64_t m_ready[2];                   // m_buf[g] written by warpgroup g's four warps
   uint64_t lsum_full;
   uint64_t o_full;                       // every PV done (committed by the PV warp)
-  uint64_t qk_done;                      // every QK done (committed by the QK warp)
+  uint64_t qk0_done;                     // the CTA's first QK done (single use)
+  uint64_t qk_done;                      // every QK done (one commit per QK warp)
   float m_end[2][128];                   // final reference maximum per [warpgroup][head]
   float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
   float lsum[2][128];                    // [warpgroup][head]
@@ -149,55 +153,6 @@ struct TcParams {
   CUtensorMap tm_comp_run;
   DecodeParams p;
 };
-
-struct Ctx {
-  int32_t* abort_flag;
-  int32_t* err;
-};
-
-__device__ __forceinline__ bool wait_bar(const Ctx& cx, uint32_t bar, uint32_t parity, bool cluster_scope) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    bool done = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-    if (done) return true;
-    if ((it & 3u) == 3u) {
-      if (*reinterpret_cast<volatile int32_t*>(cx.abort_flag)) return false;
-      uint64_t now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kTimeoutNs) {
-        *reinterpret_cast<volatile int32_t*>(cx.abort_flag) = 1;
-        if (cx.err) atomicOr(cx.err, SMLA_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// Wait for a barrier that completes once already-issued asynchronous work is
-// done; bounded by the same timeout but not cut short by the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kTimeoutNs) return;
-}
-
-// All lanes of the warp wait; the result is warp-uniform.
-__device__ __forceinline__ bool warp_wait(const Ctx& cx, uint32_t bar, uint32_t parity, bool cluster_scope = false) {
-  bool ok = wait_bar(cx, bar, parity, cluster_scope);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
-// K-major region whose 8-row groups are 1024 bytes apart.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int ch) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
 // epilogue stages the partial rows in shared memory for contiguous stores (a
@@ -286,7 +241,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
     }
     if (tid == 0) {
-      mbar_init(bar(sm.q_full), kThreads);
       for (int i = 0; i < C::kStages; ++i) {
         mbar_init(bar(sm.kv_full[i]), 1);
         mbar_init(bar(sm.kv_empty[i]), 1);
@@ -305,13 +259,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
       }
       mbar_init(bar(sm.o_full), 1);
-      mbar_init(bar(sm.qk_done), 1);
+      mbar_init(bar(sm.qk0_done), 1);
+      mbar_init(bar(sm.qk_done), kQkWarps);
       sm.abort_flag = 0;
       sm.nswa = 0;
       fence_mbar_init_cluster();
     }
     __syncthreads();
-    cp_async_arrive_noinc(bar(sm.q_full));   // completes once this thread's Q copies land
     // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
     // slots first, then valid compressed slots, each in column order
 #pragma unroll
@@ -378,6 +332,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    // Q is read by the tensor core (async proxy): every thread waits for its
+    // own Q copies and fences them into the async proxy before the barrier,
+    // so no QK can start on a Q row that is not yet visible to it
+    asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
     tc_fence_before();
     cluster_sync();
@@ -451,14 +409,22 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // at most one per stage.  Normally the consumers have waited for them.
     for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
       if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
-  } else if (warp == kMmaWarp) {
+  } else if (warp < kMmaWarp + kQkWarps) {
     // ============================================================ QK issue
     // QK and PV are issued by different warps so that a QK never waits behind
     // a PV (which waits for the softmax): the QK of tile k depends only on its
-    // data and a free S buffer.
+    // data and a free S buffer.  A thread's chain of dependent MMAs into one
+    // accumulator is issued about one instruction per 150 ns (measured), so
+    // the tiles' QK chains are spread over three warps, one per S buffer,
+    // whose MMAs the tensor core interleaves.
     constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
-    bool ok = warp_wait(cx, bar(sm.q_full), 0);
-    for (int k = 0; ok && k < ntiles; ++k) {
+    const int qi = warp - kMmaWarp;
+    // The other issuers start only once the CTA's first QK has completed:
+    // on a GB300, a QK issued by a second warp before the first one finished
+    // gave wrong logits for some heads in repeated runs (observed, cause
+    // not identified); after that the issuers' chains overlap freely.
+    bool ok = qi == 0 || ntiles <= qi || warp_wait(cx, bar(sm.qk0_done), 0);
+    for (int k = qi; ok && k < ntiles; k += kQkWarps) {
       const int st = k % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) break;
       const int b = k % kSBufs;
@@ -474,6 +440,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(sm.s_full[b]));
+        if (k == 0) mma_commit(bar(sm.qk0_done));
       }
       __syncwarp();
     }
@@ -822,11 +789,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   cluster_sync();                          // the peer is done with this CTA's shared memory
 }
 
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t encode_fn(EncodeTiledFn* out) {
+static cudaError_t encode_fn(EncodeTiledFn* out) {
   static std::atomic<EncodeTiledFn> cached{nullptr};   // looked up once; callers may be on several threads
   EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
@@ -858,8 +827,6 @@ cudaError_t encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, in
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 int tc_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes; }
 int tc_threads() { return kThreads; }

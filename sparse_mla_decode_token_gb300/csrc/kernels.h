@@ -20,6 +20,12 @@ int tc_smem_bytes(int dtype);
 int tc_threads();
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
 
+// tcgen05 decode kernel for E4M3 rows with head-owned softmax
+// (decode_tc_head_owned.cu): a 2-CTA cluster per (token, split), same column limit.
+int tc_head_owned_smem_bytes();
+int tc_head_owned_threads();
+cudaError_t launch_decode_tc_head_owned(const DecodeParams& p, int grid, cudaStream_t stream);
+
 // Split-K log-sum-exp combine (combine.cu)
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
 

@@ -58,7 +58,8 @@ smla_status check_shapes(const smla_args* a) {
     return fail(SMLA_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", a->num_splits, SMLA_MAX_SPLITS);
   if (a->max_splits < 0 || a->max_splits > SMLA_MAX_SPLITS)
     return fail(SMLA_ERR_INVALID_ARG, "max_splits %d outside [0, %d]", a->max_splits, SMLA_MAX_SPLITS);
-  if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05)
+  if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05 &&
+      a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     return fail(SMLA_ERR_INVALID_ARG, "kernel %d is not a smla_kernel", a->kernel);
   if (a->swa_rows < 0 || a->comp_rows < 0)
     return fail(SMLA_ERR_INVALID_ARG, "negative pool row count");
@@ -221,12 +222,13 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
   const int kernel = a->kernel == SMLA_KERNEL_AUTO ? kAutoKernel : a->kernel;
   int S = a->num_splits;
-  if (kernel == SMLA_KERNEL_TCGEN05) {
+  if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED) {
     // One 2-CTA cluster per (token, split), one cluster per pair of SMs.
-    plan->kernel = SMLA_KERNEL_TCGEN05;
+    const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
+    plan->kernel = head_owned ? SMLA_KERNEL_TCGEN05_HEAD_OWNED : SMLA_KERNEL_TCGEN05;
     plan->ctas_per_split = 2;
-    plan->threads = tc_threads();
-    plan->smem_bytes = tc_smem_bytes(a->dtype);
+    plan->threads = head_owned ? tc_head_owned_threads() : tc_threads();
+    plan->smem_bytes = head_owned ? tc_head_owned_smem_bytes() : tc_smem_bytes(a->dtype);
     const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
     if (s_min > SMLA_MAX_SPLITS)
       return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
@@ -389,8 +391,12 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
     ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_begin), stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
   }
-  ce = plan.kernel == SMLA_KERNEL_TCGEN05 ? launch_decode_tc(p, plan.grid, stream)
-                                          : launch_decode_cuda_core(p, plan.grid, stream);
+  if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
+    ce = launch_decode_tc_head_owned(p, plan.grid, stream);
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05)
+    ce = launch_decode_tc(p, plan.grid, stream);
+  else
+    ce = launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
   if (plan.num_splits > 1) {
     ce = launch_combine(p, stream);

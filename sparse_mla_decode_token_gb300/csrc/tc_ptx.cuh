@@ -206,6 +206,12 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Remote arrive that orders this thread's earlier memory accesses before it
+// (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T (A read from tensor memory).
 template <bool kFp8>
 __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -308,6 +314,42 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
+
+}  // namespace ptx
+}  // namespace smla
+
+namespace smla {
+namespace ptx {
+
+// Asynchronous stores into another CTA's shared memory that complete their
+// bytes on that CTA's mbarrier (addresses from map_to_rank).
+__device__ __forceinline__ void st_async_v4u(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
+#define SMLA_W32(i) "r"(r[i])
+// 32 consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      SMLA_W32(0), SMLA_W32(1), SMLA_W32(2), SMLA_W32(3), SMLA_W32(4), SMLA_W32(5), SMLA_W32(6), SMLA_W32(7),
+      SMLA_W32(8), SMLA_W32(9), SMLA_W32(10), SMLA_W32(11), SMLA_W32(12), SMLA_W32(13), SMLA_W32(14),
+      SMLA_W32(15), SMLA_W32(16), SMLA_W32(17), SMLA_W32(18), SMLA_W32(19), SMLA_W32(20), SMLA_W32(21),
+      SMLA_W32(22), SMLA_W32(23), SMLA_W32(24), SMLA_W32(25), SMLA_W32(26), SMLA_W32(27), SMLA_W32(28),
+      SMLA_W32(29), SMLA_W32(30), SMLA_W32(31)
+      : "memory");
+}
+#undef SMLA_W32
 
 }  // namespace ptx
 }  // namespace smla

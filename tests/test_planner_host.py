@@ -82,6 +82,18 @@ def test_named_workload_plans(n, splits, grid):
     assert (p["kernel"], p["num_splits"], p["grid"], p["ctas_per_split"]) == (B.KERNEL_TCGEN05, splits, grid, 2)
 
 
+def test_head_owned_form_is_opt_in_and_e4m3_only():
+    """The head-owned softmax form runs only when asked for and only on E4M3
+    rows; BF16 rows asking for it get the default tensor-core kernel.  Both
+    forms share the split rule."""
+    ref = plan(args(128, 2176))
+    ho = plan(args(128, 2176, kernel=B.KERNEL_TCGEN05_HEAD_OWNED))
+    assert ref["kernel"] == B.KERNEL_TCGEN05 and ho["kernel"] == B.KERNEL_TCGEN05_HEAD_OWNED
+    assert (ho["num_splits"], ho["grid"], ho["ctas_per_split"]) == (ref["num_splits"], ref["grid"], 2)
+    bf = plan(args(32, 640, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05_HEAD_OWNED))
+    assert bf["kernel"] == B.KERNEL_TCGEN05
+
+
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 7, 19, 38, 75, 76, 77, 128, 1000])
 @pytest.mark.parametrize("W_", [128, 129, 256, 640, 2176, 2304, 2305, 4608, 16512, 65536])
 @pytest.mark.parametrize("max_splits", [0, 1, 8])

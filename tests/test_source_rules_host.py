@@ -65,8 +65,9 @@ def function_body(code, name):
 
 def test_every_mbarrier_wait_is_bounded():
     """Raw try-waits are defined in tc_ptx.cuh and called only from the two
-    bounded waits of the tcgen05 kernel: wait_bar (timeout -> abort flag and
-    error word) and drain_wait (timeout, not cut short by the abort flag)."""
+    bounded waits the tcgen05 kernels share (tc_common.cuh): wait_bar
+    (timeout -> abort flag and error word) and drain_wait (timeout, not cut
+    short by the abort flag)."""
     ptx = strip_comments(open(os.path.join(CSRC, "tc_ptx.cuh")).read())
     assert ptx.count("mbarrier.try_wait") == 2 and "mbarrier.test_wait" not in ptx
     for path in DEVICE_SOURCES:
@@ -75,7 +76,7 @@ def test_every_mbarrier_wait_is_bounded():
             continue
         assert "mbarrier.try_wait" not in code and "mbarrier.test_wait" not in code, path
         calls = len(re.findall(r"\bmbar_try_wait(_cluster)?\s*\(", code))
-        if os.path.basename(path) != "decode_tcgen05.cu":
+        if os.path.basename(path) != "tc_common.cuh":
             assert calls == 0, path
             continue
         wait_bar, drain = function_body(code, "wait_bar"), function_body(code, "drain_wait")
