@@ -249,9 +249,10 @@ smla_status smla_decode(const smla_args* args, void* stream);
  * nothing; lower num_splits / max_splits or use smla_decode.  The function
  * calls no allocator.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture.  Every call on a device shares the one array, and each launch
+ * The first call in each CUDA context (normally the device's primary context)
+ * looks up the array's device address in that context and caches it; make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array, and each launch
  * overwrites the scratch it reads, so nothing needs clearing between calls;
  * but calls whose kernels overlap on the GPU (different streams, no ordering)
  * race on the array and give wrong results.  Order them on one stream.

@@ -11,9 +11,12 @@
 // allocator (no cudaMalloc, cudaFree or allocating library routine).
 //
 // Host code never hands the array's name to a kernel: on the host that name is
-// a stand-in symbol, not a device address.  The first call made on a device
-// looks the device address up with cudaGetSymbolAddress (that device being
-// current), checks the result and caches it; later calls reuse it.
+// a stand-in symbol, not a device address.  The runtime loads the module once
+// per CUDA context, so the array has one device address per context.  The
+// first call made in a context looks it up with cudaGetSymbolAddress (the
+// caller's device and context being current), checks the result and caches
+// it keyed by that context; later calls in the same context reuse it.
+#include <cuda.h>
 #include <stdio.h>
 
 #include <mutex>
@@ -25,19 +28,48 @@ namespace {
 
 __device__ __align__(256) unsigned char g_static_workspace[SMLA_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_static_workspace_ptr[kMaxDevices];
-std::mutex g_static_workspace_mutex;
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-cudaError_t static_workspace_address(int device, void** out) {
-  std::lock_guard<std::mutex> lock(g_static_workspace_mutex);
-  if (g_static_workspace_ptr[device] == nullptr) {
+constexpr int kMaxContexts = 64;
+struct CachedAddress {
+  CUcontext ctx;
+  void* ptr;
+};
+CachedAddress g_cache[kMaxContexts];
+int g_cached = 0;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+std::mutex g_mutex;
+
+// The device address of the static array in the current context.
+cudaError_t static_workspace_address(void** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_ctx_get_current == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    // no context current yet: cudaGetSymbolAddress below makes the device's
+    // primary context current, so read it again afterwards
     void* ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
     if (e != cudaSuccess) return e;
-    g_static_workspace_ptr[device] = ptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
   }
-  *out = g_static_workspace_ptr[device];
+  for (int i = 0; i < g_cached; ++i)
+    if (g_cache[i].ctx == ctx) {
+      *out = g_cache[i].ptr;
+      return cudaSuccess;
+    }
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+  if (e != cudaSuccess) return e;
+  if (g_cached < kMaxContexts) g_cache[g_cached++] = CachedAddress{ctx, ptr};   // beyond that: looked up per call
+  *out = ptr;
   return cudaSuccess;
 }
 
@@ -52,10 +84,6 @@ extern "C" smla_status smla_decode_static_workspace(const smla_args* args, void*
     snprintf(msg, sizeof(msg), "cudaGetDevice: %s", cudaGetErrorString(e));
     return smla::record_error(SMLA_ERR_CUDA, msg);
   }
-  if (device < 0 || device >= kMaxDevices) {
-    snprintf(msg, sizeof(msg), "device %d out of range", device);
-    return smla::record_error(SMLA_ERR_INVALID_ARG, msg);
-  }
   size_t need = 0;
   smla_status st = smla_workspace_size(args, device, &need);
   if (st != SMLA_OK) return st;
@@ -67,7 +95,7 @@ extern "C" smla_status smla_decode_static_workspace(const smla_args* args, void*
     return smla::record_error(SMLA_ERR_WORKSPACE_TOO_SMALL, msg);
   }
   void* ptr = nullptr;
-  e = static_workspace_address(device, &ptr);
+  e = static_workspace_address(&ptr);
   if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
     return smla::record_error(SMLA_ERR_CUDA, msg);

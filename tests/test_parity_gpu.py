@@ -30,8 +30,9 @@ def built():
 
 # ------------------------------------------------------- the five workloads
 
-# tokens checked per workload (the oracle evaluates them one by one)
-SAMPLE = {1: None, 2: None, 3: [0, 1, 37, 64, 100, 127], 4: [0, 1, 2, 50, 99, 160, 161], 5: None}
+# tokens checked per workload: every token (the oracle takes about a second
+# for the 128 tokens of the FP8 workload)
+SAMPLE = {1: None, 2: None, 3: None, 4: None, 5: None}
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -88,13 +89,13 @@ def test_varlen_parity(kernel):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype,H,q_lens,width", [("bf16", 64, [1, 150, 40], 128 + 128),
-                                                   ("e4m3", 128, [2, 64, 1], 128 + 448)])
+                                                   ("e4m3", 128, [2, 64, 1], 128 + 448),
+                                                   ("e4m3", 128, [3, 40, 1], 128 + 16)])
 def test_mixed_prefill_and_decode_batch(kernel, dtype, H, q_lens, width):
     """Requests with q_len from 1 to 150 in one call (a mixed prefill/decode
     batch, flattened tokens on the grid, per-token windows shifted by i).
-    The E4M3 case selects >= ~300 slots per token: with ~130 slots the E4M3
-    quantisation of P alone (P relative to the lazily held reference maximum)
-    reaches ~0.04 in max |dO| in an fp32 simulation of the kernel's arithmetic."""
+    The second E4M3 case has at most 144 slots per token, where the E4M3
+    rounding of P weighs most (short chains follow the exact running maximum)."""
     w = small_case(21 + H, dtype=dtype, H=H, width=width, batch=len(q_lens), q_lens=q_lens, seq_len=4000)
     assert w.cum_seq_lens_q is not None and w.sum_q == sum(q_lens)
     out, lse, _ = run_gpu(w, kernel=kernel)

@@ -5,8 +5,10 @@ decode (an inference runtime's plugin enqueue callback that must not allocate,
 a process whose device memory another allocator has fully reserved, a plain C
 caller with no device allocator).  Its split-K scratch is a library-owned
 static device array, so the test checks, through the C ABI, that two calls in
-a row give the same output as smla_decode with a caller workspace, within the
-parity tolerances, and that an over-size call is refused with a clear error.
+a row give bit for bit the output of smla_decode with a caller workspace (the
+same plan runs the same deterministic kernels, so any difference would be a
+misplaced scratch region), and that an over-size call is refused with a clear
+error.
 
 The file is named to be collected last, so a run that stops at the first
 failure has already run every other test.
@@ -18,7 +20,7 @@ import torch
 from sparse_mla_decode_token_gb300 import binding as B
 from sparse_mla_decode_token_gb300 import workloads as W
 
-from gpu_helpers import TOL_LSE, TOL_O, device_inputs
+from gpu_helpers import device_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -63,11 +65,9 @@ def test_static_workspace_matches_caller_workspace(dtype, H, splits):
         B.smla_decode_static_workspace(b)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all()
-        err_o = (out.float() - ref_o.float()).abs().max().item()
-        assert err_o <= TOL_O[dtype]
-        fin = torch.isfinite(ref_l)
-        assert torch.equal(fin, torch.isfinite(lse))
-        assert (lse[fin] - ref_l[fin]).abs().max().item() <= TOL_LSE
+        assert torch.equal(out, ref_o)
+        assert not torch.isnan(lse).any()
+        assert torch.equal(lse, ref_l)                 # -inf == -inf for empty heads
 
 
 def test_static_workspace_rejects_oversize_calls():
