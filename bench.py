@@ -75,6 +75,17 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def fp8_tensor_peak(bf16_tf: float):
+    """FP8 dense tensor peak: the E4M3 tcgen05.mma burst rate measured on a
+    GB300 (profiles/mma_peak.json, written by mma_peak.cu), else twice the
+    BF16 figure (the nominal ratio)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "mma_peak.json")) as f:
+            return float(json.load(f)["e4m3_tflops"]), "measured (profiles/mma_peak.json)"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * bf16_tf, "2x the BF16 peak (nominal ratio)"
+
+
 def code_only(text: str) -> str:
     """C/C++/CUDA source with comments removed and whitespace collapsed (a
     comment edit leaves the compiled kernel, and so its counters, unchanged)."""
@@ -502,7 +513,10 @@ def run_gpu(args):
     d2h = e2e_sets[0]["h_res"].numel()                  # bytes of the one packed copy out per step
 
     hbm_gbs, bf16_tf, peak_src = peaks()
-    dtype_tf = bf16_tf * (2.0 if w.dtype == "e4m3" else 1.0)     # FP8 dense = 2x BF16 (nominal ratio)
+    if w.dtype == "e4m3":
+        dtype_tf, tensor_src = fp8_tensor_peak(bf16_tf)
+    else:
+        dtype_tf, tensor_src = bf16_tf, peak_src
     main_s = statistics.mean(main_ms) / 1e3
     t_hbm = gathered_bytes / (hbm_gbs * 1e9)
     t_tc = flops / (dtype_tf * 1e12)
@@ -514,6 +528,8 @@ def run_gpu(args):
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["tensor_peak_tflops"], roof["tensor_peak_source"] = dtype_tf, tensor_src
+    roof["tensor_time_us"] = 1e6 * t_tc
     roof["traffic"], roof["traffic_source"] = traffic_record(W.CONFIG_NAMES[args.config], plan.as_dict())
     roof["algorithmic_bytes_per_launch"] = gathered_bytes
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)

@@ -114,3 +114,17 @@ def test_roofline_peaks_come_from_the_measured_file_else_the_fallback(monkeypatc
     assert bench.peaks() == (rec["hbm_gbs"], rec["bf16_tflops"], "measured")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))                  # no measured file there
     assert bench.peaks() == (6800.0, 1900.0, "fallback")              # the recipe's fallback figures
+
+
+def test_fp8_tensor_peak_comes_from_the_measured_record(monkeypatch, tmp_path):
+    """The FP8 tensor peak is the E4M3 tcgen05 burst rate recorded in
+    profiles/mma_peak.json; without that record it falls back to twice the
+    BF16 peak."""
+    import json
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "mma_peak.json")))
+    tf, src = bench.fp8_tensor_peak(1000.0)
+    assert tf == rec["e4m3_tflops"] and "measured" in src
+    assert rec["e4m3_tflops"] > rec["bf16_tflops"] > 0
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    tf, src = bench.fp8_tensor_peak(1000.0)
+    assert tf == 2000.0 and "nominal" in src
