@@ -2,8 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
-One step = one whole decode (split kernel, plus the combine kernel when the
-plan splits) over one batch of the synthetic workload.  Default workload:
+One step = one whole decode (the decode kernel, plus the combine kernel when
+the plan has one) over one batch of the synthetic workload.  Default workload:
 FP8 E4M3, 128 tokens, H=128, 128 SWA + 2048 compressed slots per token over a
 256k-row compressed pool.  L2 is flushed (a write of twice the L2 size)
 between timed steps, outside the timed events.  Prints one JSON line.
@@ -98,7 +98,7 @@ def code_only(text: str) -> str:
 # packing.  What they decide about a launch (kernel, splits, grid, block, shared
 # memory) is matched through the plan stored with each traffic record instead.
 HOST_ONLY_SOURCES = ("smla_api.cu",)
-PLAN_KEYS = ("kernel", "num_splits", "ctas_per_split", "grid", "threads", "smem_bytes")
+PLAN_KEYS = ("kernel", "num_splits", "ctas_per_split", "grid", "threads", "smem_bytes", "clusters")
 
 
 def kernel_sources_sha() -> str:
@@ -339,12 +339,14 @@ def run_gpu(args):
                          seq_lens=d_seq, out=out, sparse_topk_lens=d_lens, cum_seq_lens_q=d_cum,
                          sinks=d_sinks, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
                          out_lse=lse, kernel=args.kernel, num_splits=args.num_splits, error_word=err_word,
+                         schedule=args.schedule,
                          swa_topk_lens=d_win, comp_block_tables=d_bt, comp_page_size=w.comp_page_size,
                          hca_seq_lens=d_hca, width=w.width if w.paged else None)
     plan = B.smla_plan_decode(args_c, local)
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
-    launches_per_step = 1 + (1 if plan.num_splits > 1 else 0)
+    has_combine = plan.num_splits > 1 or plan.clusters > 1
+    launches_per_step = 1 + (1 if has_combine else 0)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -393,6 +395,7 @@ def run_gpu(args):
                           cum_seq_lens_q=dd.get("cum"), sinks=d_sinks, bmm1_scale=w.bmm1_scale,
                           bmm2_scale=w.bmm2_scale, out_lse=res["lse"], kernel=args.kernel,
                           num_splits=args.num_splits, error_word=err_word, swa_topk_lens=dd.get("win"),
+                          schedule=args.schedule,
                           comp_block_tables=dd.get("bt"), comp_page_size=w.comp_page_size,
                           hca_seq_lens=dd.get("hca"), width=w.width if w.paged else None)
         a_b.workspace, a_b.workspace_bytes = workspace.data_ptr(), workspace.numel()   # decodes are serial
@@ -534,7 +537,8 @@ def run_gpu(args):
     roof["algorithmic_bytes_per_launch"] = gathered_bytes
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
     roof["main_kernel_us"] = 1e6 * main_s
-    roof["kernels_timed"] = "split kernel" if plan.num_splits == 1 else "split kernel + combine (programmatic dependent launch)"
+    roof["kernels_timed"] = ("decode kernel + combine (programmatic dependent launch)" if has_combine
+                             else "decode kernel")
     roof["roofline_frac_whole_step"] = max(t_hbm, t_tc) / (total_s / (K * 1.0)) if ws_ == 1 else None
 
     if rank != 0:
@@ -577,6 +581,7 @@ def main():
                          "compressed segments)")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     ap.add_argument("--num-splits", type=int, default=0, help="0 = the planner's choice")
+    ap.add_argument("--schedule", type=int, default=0, help="0 = auto, 1 = grid, 2 = balanced (smla_schedule)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle timing")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")

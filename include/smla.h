@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 5
+#define SMLA_ABI_VERSION 6
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -64,13 +64,25 @@ typedef enum smla_dtype {
 } smla_dtype;
 
 /* Kernel selection (smla_args.kernel).  AUTO picks the tensor-core kernel.
- * The tensor-core kernels run each (token, split) on a pair of CTAs, CTA r
- * keeping output dims [256 r, 256 r + 256) of every head; they differ in
- * where the softmax runs.  TCGEN05: both CTAs add the peer's partial logits
+ * The tensor-core kernels run on pairs of CTAs, CTA r keeping output dims
+ * [256 r, 256 r + 256) of every head; they differ in where the softmax runs.  TCGEN05: both CTAs add the peer's partial logits
  * and run the softmax of every head.  TCGEN05_HEAD_OWNED (E4M3 rows; BF16
  * rows take TCGEN05): each CTA runs the softmax of half the heads and sends
  * the peer their E4M3 P; it moves fewer bytes between the CTAs but is slower
  * (a round trip per tile), and is kept as an alternative. */
+/* Work hand-out of the TCGEN05 kernel (smla_args.schedule).  GRID: one CTA
+ * pair per (token, split), the split count from num_splits / max_splits.
+ * BALANCED (with num_splits == 0 and max_splits == 0, W <= 2304 and T <= 14
+ * pairs; else GRID): one pair per two SMs (smla_plan.clusters pairs), pair c
+ * taking the c-th of equal shares of the T x W selected columns: whole
+ * tokens plus the pieces of the tokens cut at its share's ends, which a
+ * second kernel merges.  AUTO is GRID. */
+typedef enum smla_schedule {
+  SMLA_SCHEDULE_AUTO = 0,
+  SMLA_SCHEDULE_GRID = 1,
+  SMLA_SCHEDULE_BALANCED = 2
+} smla_schedule;
+
 typedef enum smla_kernel {
   SMLA_KERNEL_AUTO = 0,
   SMLA_KERNEL_CUDA_CORE = 1,          /* plain CUDA-core kernel (fp32 FMA) */
@@ -131,13 +143,14 @@ typedef struct smla_args {
   int32_t num_splits;               /* 0 = planner; else forced split count in [1, SMLA_MAX_SPLITS] */
   int32_t max_splits;               /* 0 = SMLA_DEFAULT_MAX_SPLITS; planner upper bound */
   int32_t kernel;                   /* smla_kernel */
+  int32_t schedule;                 /* smla_schedule: how TCGEN05 hands out column ranges */
 
   int32_t* error_word;              /* optional device int32; kernels OR SMLA_DEVERR_* bits into it */
 
   /* Optional cudaEvent_t handles recorded on the stream immediately before
-   * the split kernel and after the last kernel of the call (the split kernel
-   * when num_splits == 1, else the combine, which is launched as a
-   * programmatic dependent of the split kernel).  For profiling. */
+   * the decode kernel and after the last kernel of the call (the decode
+   * kernel when the plan has no combine, else the combine, which is launched
+   * as a programmatic dependent of the decode kernel).  For profiling. */
   void* profile_event_begin;
   void* profile_event_end;
 
@@ -171,12 +184,14 @@ typedef struct smla_args {
 /* The resolved launch plan (shape-based: it never reads device memory). */
 typedef struct smla_plan {
   int32_t kernel;            /* smla_kernel actually used (TCGEN05_HEAD_OWNED on BF16 rows reports TCGEN05) */
-  int32_t num_splits;        /* S: column ranges per token; S > 1 adds a combine launch */
-  int32_t ctas_per_split;    /* CTAs cooperating on one (token, split) */
+  int32_t num_splits;        /* S: column ranges per token; S > 1 adds a combine launch (1 in balanced mode) */
+  int32_t ctas_per_split;    /* CTAs cooperating on one unit of work */
   int32_t grid;              /* CTAs of the main decode launch */
   int32_t threads;           /* threads per CTA of the main decode launch */
   int32_t smem_bytes;        /* dynamic shared memory per CTA */
-  size_t workspace_bytes;    /* workspace the call needs (0 when S == 1) */
+  int32_t clusters;          /* balanced mode: P CTA pairs with equal column shares (grid = 2 P; P > 1 adds a
+                                combine launch); 0: one pair per (token, split) */
+  size_t workspace_bytes;    /* workspace the call needs (0 without a combine) */
 } smla_plan;
 
 /*

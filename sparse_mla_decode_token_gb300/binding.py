@@ -27,6 +27,7 @@ MAX_SPLITS = 64
 SMLA_OK, SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE_TOO_SMALL, SMLA_ERR_CUDA = range(5)
 SMLA_BF16, SMLA_E4M3 = 0, 1
 KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED = 0, 1, 2, 3
+SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_BALANCED = 0, 1, 2
 DEVERR_INDEX_OUT_OF_RANGE = 0x1
 
 _c_void_p = ctypes.c_void_p
@@ -47,6 +48,7 @@ class SmlaArgs(ctypes.Structure):
         ("out", _c_void_p), ("out_lse", _c_void_p),
         ("workspace", _c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("num_splits", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("kernel", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
         ("error_word", _c_void_p),
         ("profile_event_begin", _c_void_p), ("profile_event_end", _c_void_p),
         ("comp_block_tables", _c_void_p), ("block_table_stride", ctypes.c_int64),
@@ -60,7 +62,7 @@ class SmlaPlan(ctypes.Structure):
         ("kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
         ("ctas_per_split", ctypes.c_int32), ("grid", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("clusters", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t),
     ]
 
     def as_dict(self) -> dict:
@@ -228,6 +230,7 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
               num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
               error_word: Optional[torch.Tensor] = None,
               swa_topk_lens: Optional[torch.Tensor] = None,
+              schedule: int = 0,
               comp_block_tables: Optional[torch.Tensor] = None,
               comp_page_size: int = 0, hca_seq_lens: Optional[torch.Tensor] = None,
               width: Optional[int] = None) -> SmlaArgs:
@@ -329,7 +332,7 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     a.out, a.out_lse = out.data_ptr(), _ptr(out_lse)
     if workspace is not None:
         a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    a.num_splits, a.max_splits, a.kernel, a.schedule = num_splits, max_splits, kernel, schedule
     a.error_word = _ptr(error_word)
     if os.environ.get("SMLA_VALIDATE") == "1":
         _validate_on_host(a, sparse_indices=sparse_indices, seq_lens=seq_lens, sparse_topk_lens=sparse_topk_lens,
@@ -361,6 +364,7 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
                       num_splits: int = 0, max_splits: int = 0, kernel: int = KERNEL_AUTO,
                       error_word: Optional[torch.Tensor] = None,
                       stream: Optional[int] = None,
+                      schedule: int = 0,
                       swa_topk_lens: Optional[torch.Tensor] = None,
                       hca_compressed_block_tables: Optional[torch.Tensor] = None,
                       hca_seq_lens: Optional[torch.Tensor] = None,
@@ -386,7 +390,7 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
                      sparse_topk_lens=sparse_topk_lens, cum_seq_lens_q=cum_seq_lens_q,
                      sinks=sinks, bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
                      out_lse=out_lse, workspace=workspace_buffer, num_splits=num_splits,
-                     max_splits=max_splits, kernel=kernel, error_word=error_word,
+                     max_splits=max_splits, kernel=kernel, error_word=error_word, schedule=schedule,
                      swa_topk_lens=swa_topk_lens, comp_block_tables=hca_compressed_block_tables,
                      comp_page_size=comp_page_size or 0, hca_seq_lens=hca_seq_lens, width=width)
     with torch.cuda.device(query.device):   # the library plans and launches on the current device
@@ -396,7 +400,7 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
 
 def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=0,
                    kernel=KERNEL_AUTO, cum_seq_lens_q=None, device: int = 0,
-                   width: Optional[int] = None) -> int:
+                   width: Optional[int] = None, schedule: int = 0) -> int:
     """Workspace bytes for a call with these shapes (no device memory is read);
     ``width`` = logical columns in the page-table form."""
     a = SmlaArgs()
@@ -405,5 +409,5 @@ def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=
     a.width = sparse_indices.shape[-1] if width is None else int(width)
     a.batch, a.dtype = seq_lens.numel(), _dtype_code(q3)
     a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
-    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    a.num_splits, a.max_splits, a.kernel, a.schedule = num_splits, max_splits, kernel, schedule
     return smla_workspace_size(a, device)

@@ -1,45 +1,65 @@
 // tcgen05 / TMEM sparse MLA decode kernel for sm_103a.
 //
-// Work unit: one (token, split) runs on a cluster of two CTAs.  CTA r of the
-// pair owns output dims [256 r, 256 r + 256): an fp32 accumulator for 128 heads
-// x 512 dims is 256 KB, the whole tensor memory of one SM, so the output is
-// split across the pair.  Per tile of up to N selected slots (N = 64 for E4M3,
-// 32 for BF16):
+// A cluster of two CTAs works through a list of units; a unit is the columns
+// [c0, c1) of one token's index row.  Units are handed out in one of two ways:
 //
-//   set-up (all warps)  stage the split's index columns and compact the valid
-//                       slots (per-warp ballots and scans) into a list: SWA
-//                       slots, then compressed slots; tiles are runs of N list
-//                       entries of one pool (masked slots are never loaded)
-//   producer warps 0-3  the pair's half of every selected row (256 dims) with
-//                       TMA tile::gather4 (four rows of 128 bytes per request)
-//                       into a 128-byte-swizzled, UMMA-canonical shared-memory
-//                       tile of a 7-stage (E4M3) or 6-stage (BF16) ring; a
-//                       warp's TMA requests are served one after another, so a
-//                       tile's 32 requests are spread over the two warps of
-//                       one of two groups taking alternate tiles; a tile of N
-//                       consecutive rows is one box copy per 128-byte block
-//   QK warps 4-6        S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
-//                       into one of three TMEM S buffers, warp 4 + b issuing
-//                       the tiles of buffer b; warp 4 also allocates and
-//                       frees TMEM
-//   PV warp 7           O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
-//                       P read from TMEM); a separate issuer so that no QK
-//                       waits behind a PV that waits for the softmax
-//   softmax warps 8-15  two warpgroups taking whole tiles in turn (warpgroup
-//                       g takes tiles j with j % 2 == g), one thread per head:
+//   grid mode        one unit per cluster: (token, split s of S)
+//   balanced mode    cluster c of P takes the c-th of P equal, contiguous
+//                    shares of the token-major column space (T tokens x W
+//                    columns): whole tokens, plus the piece of a token cut at
+//                    either end of the share.  Whole tokens write the output;
+//                    pieces write normalised partials that a second kernel
+//                    merges.  Every cluster gets the same number of columns,
+//                    so no SM pair idles through a last, partial wave, and a
+//                    unit's index compaction and first gathers overlap the
+//                    previous unit's last tiles.
+//
+// CTA r of the pair owns output dims [256 r, 256 r + 256): an fp32 accumulator
+// for 128 heads x 512 dims is 256 KB, the whole tensor memory of one SM, so
+// the output is split across the pair.  Per tile of up to N selected slots
+// (N = 64 for E4M3, 32 for BF16):
+//
+//   producer warps 0-3  per unit, the index compaction: the unit's columns are
+//                       loaded, masked and compacted (ballots and scans) into
+//                       a list: SWA slots, then compressed slots; tiles are runs
+//                       of N list entries of one pool (masked slots are never
+//                       loaded); then the pair's half of every selected row
+//                       (256 dims) with TMA tile::gather4 (four rows of 128
+//                       bytes per request) into a 128-byte-swizzled,
+//                       UMMA-canonical shared-memory tile of a 7-stage (E4M3)
+//                       or 6-stage (BF16) ring; two groups of two warps take
+//                       alternate tiles; a tile of N consecutive rows is one box
+//                       copy per 128-byte block
+//   QK warps 4-6        per unit, the token's query half (TMA box loads, issued
+//                       by warp 4 once every QK of the previous unit is done),
+//                       then S_r = Q_r K_r^T (M = 128 heads, N slots, K = 256
+//                       dims) into one of three TMEM S buffers; warp 4 + b
+//                       issues the tiles of buffer b (one thread's chain of
+//                       dependent MMAs runs at about one instruction per
+//                       150 ns, so the chains overlap); warp 4 also allocates
+//                       and frees TMEM
+//   PV warp 7           O_r += P V_r (M = 128 heads, N = 256 dims, K = N slots,
+//                       P read from TMEM); a unit's first PV waits until the
+//                       previous unit's O has been read out
+//   softmax warps 8-15  two warpgroups taking whole tiles in turn (warpgroup g
+//                       takes tiles j with j % 2 == g), one thread per head:
 //                       read S_r from TMEM, push it to the peer CTA with
 //                       st.async (completing bytes on the peer's mbarrier) as
-//                       24-bit floats (four values in three words), add
-//                       the peer's partial (S = S_0 + S_1; each CTA adds its
-//                       own exact half), settle the running reference maximum m(j) from
-//                       m(j-1) (handed over by the other warpgroup through
+//                       24-bit floats (four values in three words), add the
+//                       peer's partial (S = S_0 + S_1; each CTA adds its own
+//                       exact half), settle the running reference maximum m(j)
+//                       from m(j-1) (handed over by the other warpgroup through
 //                       shared memory), exponentials in base 2 with lazy
-//                       rescaling of O, write P (BF16 or E4M3) into TMEM;
-//                       finally normalise O and store it (BF16 output, or BF16
-//                       split partials staged through shared memory) plus the
+//                       rescaling of O, write P (BF16 or E4M3) into TMEM; at a
+//                       unit's end both warpgroups normalise O and store it
+//                       (the BF16 output, or BF16 normalised partials) plus the
 //                       LSE.  Each warpgroup pushes its next tile's partial S
 //                       before its exponentials; one warpgroup's exponentials
 //                       overlap the other's loads and exchange.
+//
+// Tiles are numbered across the units of a cluster, so the rings of KV
+// stages, S / P buffers and exchange buffers run on without a break between
+// units.
 //
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
@@ -68,26 +88,44 @@ using namespace tc;
 
 constexpr int kMaxN = 64;            // largest tile (slots per tile)
 constexpr int kHalfDims = 256;       // output dims per CTA
-constexpr int kProducerWarps = 4;    // TMA gathers
+constexpr int kProducerWarps = 4;    // index compaction and TMA gathers
 constexpr int kProducerGroups = 2;   // tiles alternate between two groups of two warps that share each tile
-constexpr int kMmaWarp = kProducerWarps;        // first QK issuer; allocates and frees TMEM
-constexpr int kQkWarps = 3;                     // QK issuers: warp kMmaWarp + i issues the tiles k with k % 3 == i
+constexpr int kMmaWarp = kProducerWarps;        // first QK issuer; loads Q; allocates and frees TMEM
+constexpr int kQkWarps = 3;                     // QK issuers: warp kMmaWarp + i issues the tiles j with j % 3 == i
 constexpr int kPvWarp = kMmaWarp + kQkWarps;    // PV issue
-constexpr int kSoftmaxWarp0 = kPvWarp + 1;
+constexpr int kSoftmaxWarp0 = 8;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
-constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of a staged index row
-constexpr int kChunksPerWarp = (kMaxChunks + kWarps - 1) / kWarps;
+constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of a unit
+constexpr int kChunksPerProducer = (kMaxChunks + kProducerWarps - 1) / kProducerWarps;
+constexpr int kMaxUnits = SMLA_TC_MAX_UNITS;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
 constexpr uint32_t kSCol = 256;      // S: three buffers of N fp32 columns, then P: two buffers of 16 columns
 constexpr int kSBufs = 3;
+// One QK issuer per S buffer: an issuer then waits on its buffer's phases in
+// order.  An issuer taking tiles of several buffers could wait two phases
+// ahead of a buffer's release, which a parity wait cannot tell from one phase
+// behind.
 static_assert(kQkWarps == kSBufs, "one QK issuer per S buffer");
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr int kExactRefTiles = 8;          // E4M3 P: chains of at most this many tiles follow the exact maximum
 constexpr int kMaxStages = 8;
+static_assert(kPvWarp >= kMmaWarp + kQkWarps && kPvWarp < kSoftmaxWarp0, "warp roles");
+
+// A unit of work: columns [c0, c1) of token t, and where its result goes.
+struct Unit {
+  int32_t t, c0, c1;
+  int32_t partial;           // 0: the output (bmm2, sink, BF16 out, out_lse); 1: a normalised partial
+  int64_t part_row;          // partial: element offset of head 0's row
+  int64_t lse_row;           // partial: offset of head 0's LSE
+  int32_t part_hstride;      // partial: elements between consecutive heads' rows
+  int32_t lse_hstride;       // partial: entries between consecutive heads' LSEs
+  // written by the producers once the unit is compacted
+  int32_t nswa, nvalid, ntiles, tile0;
+  int32_t swa_tail, last_tail;   // slots of the last SWA tile and of the last tile
+};
 
 struct TcSmall {
   uint64_t kv_full[kMaxStages];
@@ -95,16 +133,25 @@ struct TcSmall {
   uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[2], p_empty[2];
   uint64_t xin_full[2], xout_free[2];
   uint64_t m_ready[2];                   // m_buf[g] written by warpgroup g's four warps
-  uint64_t lsum_full;
-  uint64_t o_full;                       // every PV done (committed by the PV warp)
-  uint64_t qk0_done;                     // the CTA's first QK done (single use)
-  uint64_t qk_done;                      // every QK done (one commit per QK warp)
-  float m_end[2][128];                   // final reference maximum per [warpgroup][head]
+  uint64_t unit_ready[kMaxUnits];        // unit u compacted (single use)
+  uint64_t prod_counts;                  // the producer warps' chunk counts of a unit written (one phase per unit)
+  uint64_t prod_list;                    // the producer warps' slot lists of a unit written (one phase per unit)
+  uint64_t q_full;                       // a unit's Q landed (one phase per unit using Q: the first, and those with tiles)
+  uint64_t qk_first;                     // a unit's first QK done (one phase per unit with tiles)
+  uint64_t qk_unit_done;                 // every QK of a unit done (one phase per unit using Q)
+  uint64_t lsum_full;                    // both warpgroups' row sums of a unit written (one phase per unit)
+  uint64_t unit_pv_done;                 // every PV of a unit done (one phase per unit)
+  uint64_t o_free;                       // a unit's O read out (one phase per unit)
+  uint64_t o_full;                       // every PV done (committed by the PV warp at the end)
+  uint64_t qk_done;                      // every QK done (one commit per QK warp at the end)
+  float m_end[2][2][128];                // [unit & 1][warpgroup][head]: final reference maximum
+  float lsum[2][2][128];                 // [unit & 1][warpgroup][head]: row sum at m_end
   float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
-  float lsum[2][128];                    // [warpgroup][head]
-  int32_t chunk_off[kMaxChunks];        // compacted-slot count of each 32-column chunk, then its offset
-  int32_t nswa;                          // valid slots in the SWA columns of the split
-  int32_t nvalid;                        // valid slots of the split
+  float2 epi[2][128];                    // [warpgroup][head]: bmm2 scale, sink x log2(e) (each thread its own)
+  int32_t chunk_cnt[kMaxChunks];         // compacted-slot count of each 32-column chunk
+  int32_t chunk_swa[kMaxChunks];         // of which SWA slots
+  Unit unit[kMaxUnits];
+  int32_t nunits;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -114,7 +161,6 @@ struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
   static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
-  static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
   static constexpr int kStages = kFp8 ? 7 : 6;                 // KV ring (FP8: the smaller exchange buffers make room for a 7th)
   static constexpr int kKStep = 32 / kElem;                    // MMA K per instruction
   static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
@@ -130,7 +176,7 @@ struct Cfg {
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffX = kOffKV + kStages * kStageBytes;
   static constexpr int kOffIdx = kOffX + 2 * kXBytes;
-  static constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
+  static constexpr int kOffSmall = kOffIdx + 2 * kMaxCols * 4;             // two slot lists
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
   static_assert(kStages <= kMaxStages, "barrier arrays");
   static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
@@ -138,26 +184,79 @@ struct Cfg {
   static_assert(kPCols == 16, "P buffer width");
   static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
   static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
-  static_assert(kStages * kStageBytes >= 2 * 128 * 256, "BF16 partial staging fits in the KV stages");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Kernel parameters: the shared decode parameters plus two TMA descriptors per
-// KV pool ([rows, 512] with the pool's row stride; 128-byte swizzle): box =
-// 128 bytes x 1 row for tile::gather4, and 128 bytes x N rows for whole-tile
-// copies of N consecutive rows.
+// Kernel parameters: the shared decode parameters; two TMA descriptors per KV
+// pool ([rows, 512] with the pool's row stride; 128-byte swizzle): box = 128
+// bytes x 1 row for tile::gather4, and 128 bytes x N rows for whole-tile
+// copies of N consecutive rows; the query as [T, H, 512] (box 128 bytes x H
+// heads x 1 token); and the unit hand-out.
 struct TcParams {
   CUtensorMap tm_swa;
   CUtensorMap tm_comp;
   CUtensorMap tm_swa_run;
   CUtensorMap tm_comp_run;
+  CUtensorMap tm_q;
   DecodeParams p;
+  int32_t clusters;            // balanced mode: P shares; 0: grid mode
+  __nv_bfloat16* piece_o;      // balanced mode: [P][2][H][512] BF16 normalised partials of cut tokens
+  float* piece_lse;            // balanced mode: [P][2][H] their base-2 LSEs
 };
 
-// kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
-// epilogue stages the partial rows in shared memory for contiguous stores (a
-// separate instantiation, so that the single-split code is compiled alone).
-template <bool kFp8, bool kPartial>
+// The units of cluster c; returns their count (at most kMaxUnits, which the
+// planner guarantees).  In balanced mode a piece goes to slot 2c if it
+// continues a token begun by an earlier cluster (c0 > 0), else to slot 2c + 1
+// (the head of a token that later clusters continue).
+__device__ int make_units(const TcParams& P, int c, Unit* units) {
+  const DecodeParams& p = P.p;
+  const int H = p.H;
+  if (P.clusters == 0) {
+    // Column range of split s, from the table width only (so that the index
+    // loads need not wait for any device value): [c0, c0 + ceil(W / S)); in
+    // the page-table form rounded up to whole 64-slot runs, so that every full
+    // tile of compressed slots lies on one page when pages hold a multiple of
+    // 64 rows.
+    const int S = p.num_splits;
+    const int s = c % S, t = c / S;
+    int per_split = (p.W + S - 1) / S;
+    if (p.bt) per_split = (per_split + kMaxN - 1) / kMaxN * kMaxN;
+    Unit u = {};
+    u.t = t;
+    u.c0 = min(p.W, s * per_split);
+    u.c1 = min(p.W, u.c0 + per_split);
+    u.partial = S > 1;
+    u.part_row = ((int64_t)t * H * S + s) * kHeadDim;
+    u.part_hstride = S * kHeadDim;
+    u.lse_row = (int64_t)t * H * S + s;
+    u.lse_hstride = S;
+    units[0] = u;
+    return 1;
+  }
+  const int64_t W = p.W;
+  const int64_t total = (int64_t)p.sum_q * W;
+  const int64_t g0 = total * c / P.clusters, g1 = total * (c + 1) / P.clusters;
+  int n = 0;
+  for (int64_t t = g0 / W; t * W < g1 && n < kMaxUnits; ++t) {
+    Unit u = {};
+    u.t = (int32_t)t;
+    const int64_t lo = g0 - t * W, hi = g1 - t * W;
+    u.c0 = (int32_t)(lo > 0 ? lo : 0);
+    u.c1 = (int32_t)(hi < W ? hi : W);
+    if (u.c0 > 0 || u.c1 < W) {
+      const int64_t slot = 2 * (int64_t)c + (u.c0 > 0 ? 0 : 1);
+      u.partial = 1;
+      u.part_row = slot * H * kHeadDim;
+      u.part_hstride = kHeadDim;
+      u.lse_row = slot * H;
+      u.lse_hstride = 1;
+    }
+    units[n++] = u;
+  }
+  return n;
+}
+
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
   using C = Cfg<kFp8>;
@@ -176,60 +275,14 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
   const uint32_t peer = rank ^ 1u;
-  const int S = p.num_splits;
-  const int unit = blockIdx.x >> 1;
-  const int s = unit % S;
-  const int t = unit / S;
   const int H = p.H;
-  // Column range of this split, from the table width only (so that the index
-  // loads need not wait for any device value): [c0, c0 + ceil(W / S)); in the
-  // page-table form rounded up to whole 64-slot runs, so that every full tile
-  // of compressed slots lies on one page when pages hold a multiple of 64 rows.
-  int per_split = (p.W + S - 1) / S;
-  if (p.bt) per_split = (per_split + kMaxN - 1) / kMaxN * kMaxN;
-  const int c0 = min(p.W, s * per_split);
-  int c1 = min(p.W, c0 + per_split);
-  if (c1 - c0 > kMaxCols) {           // the planner prevents this; never read past the staging buffer
-    if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
-    c1 = c0 + kMaxCols;
-  }
 
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
 
   // ---------------------------------------------------------------- set-up
-  // Q first: its copies need nothing but (t, rank)
   {
-    const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
-                              ((int64_t)t * p.q_stride_token + (int64_t)rank * kHalfDims) * C::kElem;
-    for (int c = tid; c < H * C::kChunks; c += kThreads) {
-      const int h = c / C::kChunks, cc = c % C::kChunks;
-      cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7),
-                  qb + (int64_t)h * kHeadDim * C::kElem + cc * 16);
-    }
-  }
-  // the split's index columns, in flight together with the token metadata loads
-  const int nchunks = (c1 - c0 + 31) / 32;
-  const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
-  int32_t rv[kChunksPerWarp];
-  if (p.bt == nullptr) {             // index form (a loop of its own: the FP8 code keeps its registers)
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = (col < c1) ? __ldg(irow + col) : -1;
-    }
-  } else {                           // page-table form: compressed rows from the page table
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = -1;
-      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
-    }
-  }
-  const TokenInfo ti = token_info(p, t);
-  c1 = min(c1, max(c0, ti.n_lim));    // active columns of the split
-  {
-    // zero the KV stages (rows past a tile's slot count then hold finite data)
-    // and the Q rows of absent heads
+    // zero the KV stages (rows past a tile's slot count then hold finite
+    // data) and the Q rows of absent heads (the Q box loads only H rows)
     const uint4 z = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
     const int zn = C::kStages * C::kStageBytes / 16;
@@ -246,96 +299,32 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         mbar_init(bar(sm.kv_empty[i]), 1);
       }
       for (int b = 0; b < 2; ++b) {
-
         mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
         mbar_init(bar(sm.p_empty[b]), 1);
         mbar_init(bar(sm.xin_full[b]), 1);
         mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps / 2);
         mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
       }
-      mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
       for (int b = 0; b < kSBufs; ++b) {
         mbar_init(bar(sm.s_full[b]), 1);
         mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
       }
+      for (int u = 0; u < kMaxUnits; ++u) mbar_init(bar(sm.unit_ready[u]), 1);
+      mbar_init(bar(sm.prod_counts), kProducerWarps);
+      mbar_init(bar(sm.prod_list), kProducerWarps);
+      mbar_init(bar(sm.q_full), 1);
+      mbar_init(bar(sm.qk_first), 1);
+      mbar_init(bar(sm.qk_unit_done), kQkWarps);
+      mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
+      mbar_init(bar(sm.unit_pv_done), 1);
+      mbar_init(bar(sm.o_free), kSoftmaxWarps);
       mbar_init(bar(sm.o_full), 1);
-      mbar_init(bar(sm.qk0_done), 1);
       mbar_init(bar(sm.qk_done), kQkWarps);
       sm.abort_flag = 0;
-      sm.nswa = 0;
+      sm.nunits = make_units(P, blockIdx.x >> 1, sm.unit);
       fence_mbar_init_cluster();
     }
-    __syncthreads();
-    // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
-    // slots first, then valid compressed slots, each in column order
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int k = warp + q * kWarps;
-      if (k < nchunks) {
-        const int col = c0 + k * 32 + lane;
-        const int idx = rv[q];
-        rv[q] = -1;
-        if (col < c1) {
-          const bool swa = col < kSwaCols;
-          bool ok = idx != -1 && (!swa || col < ti.w_swa);
-          if (ok) {
-            const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
-            if (idx < 0 || (int64_t)idx >= nrows) {
-              ok = false;
-              if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
-            }
-          }
-          if (ok) rv[q] = idx;
-        }
-        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
-        if (lane == 0) {
-          sm.chunk_off[k] = __popc(ball);
-          if (ball_swa) atomicAdd(&sm.nswa, __popc(ball_swa));
-        }
-      }
-    }
-    __syncthreads();
-    // every warp scans the chunk counts itself (at most kMaxChunks = 72, three
-    // shuffle scans), which saves a serialised scan and a block barrier
-    int chunk_base[kChunksPerWarp];
-    {
-      int carry = 0;
-#pragma unroll
-      for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
-      for (int base0 = 0; base0 < nchunks; base0 += 32) {
-        const int k = base0 + lane;
-        const int v = k < nchunks ? sm.chunk_off[k] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += u;
-        }
-        // exclusive prefix of this warp's chunks k = warp + q * kWarps in this group of 32
-#pragma unroll
-        for (int q = 0; q < kChunksPerWarp; ++q) {
-          const int kq = warp + q * kWarps;
-          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
-          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
-        }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (warp == 0 && lane == 0) sm.nvalid = carry;
-    }
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int k = warp + q * kWarps;
-      if (k < nchunks) {
-        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
-      }
-    }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
-    // Q is read by the tensor core (async proxy): every thread waits for its
-    // own Q copies and fences them into the async proxy before the barrier,
-    // so no QK can start on a Q row that is not yet visible to it
-    asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
     tc_fence_before();
     cluster_sync();
@@ -343,138 +332,320 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   }
   const uint32_t tmem = sm.tmem_base;
   const Ctx cx{&sm.abort_flag, p.err};
-  // tiles: runs of up to N compacted slots of one pool
-  const int nswa = sm.nswa, nvalid = sm.nvalid;
-  const int tswa = (nswa + kN - 1) / kN;
-  const int ntiles = tswa + (nvalid - nswa + kN - 1) / kN;
-  auto tile_start = [&](int j) { return j < tswa ? j * kN : nswa + (j - tswa) * kN; };
-  auto tile_n = [&](int j) { return min(kN, (j < tswa ? nswa : nvalid) - tile_start(j)); };
+  const int nunits = sm.nunits;
 
   if (warp < kProducerWarps) {
     // ============================================================ producer
-    // A warp's TMA requests are served one after another (about 50 ns per
-    // gather4), so a tile's requests are spread over the three warps of its
-    // group; two groups take alternate tiles (measured: one group of six
-    // sharing every tile reaches ~15 GB/s per SM from HBM, warps owning whole
-    // tiles ~24 GB/s but with a long issue time per tile; two groups of three
-    // were fastest in the full kernel).  A full tile of N consecutive rows (a
-    // page run of the page-table form, or a run in the index table) is one
-    // box copy per 128-byte column block instead.
+    // The four warps compact each unit's index columns together into a list
+    // (two lists alternate), publish the unit, and gather its tiles.  Unit
+    // u + 1 is compacted while unit u's tiles are in flight: for unit 0 after
+    // its first ring of tiles is issued, for later units before their first
+    // tile, when the ring is normally full of the previous unit's tiles.  A
+    // warp's TMA requests are served one after another (about 40 ns per
+    // gather4), so a tile's requests are spread over the two warps of its
+    // group; two groups take alternate tiles.  A full tile of N consecutive
+    // rows (a page run of the page-table form, or a run in the index table) is
+    // one box copy per 128-byte column block instead.
     if (tid == 0) {
       prefetch_tensormap(&P.tm_swa);
       prefetch_tensormap(&P.tm_comp);
       prefetch_tensormap(&P.tm_swa_run);
       prefetch_tensormap(&P.tm_comp_run);
     }
-    // Producer group pg (kWarpsPerGroup warps) gathers tiles pg, pg + kProducerGroups, ...
     constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
     const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
-    int j = pg;                              // after the loop: past the last tile this group issued
-    for (; j < ntiles; j += kProducerGroups) {
-      const int st = j % C::kStages;
-      if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
-      const int start = tile_start(j), n = tile_n(j);
-      const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
-      const uint32_t stage = kv_addr + st * C::kStageBytes;
-      const int32_t* rows = idx_s + start;
-      bool run = false;                      // rows[r] == rows[0] + r for every r < N
-      if (n == kN) {
-        const uint32_t r0 = (uint32_t)rows[0];
-        bool ok = true;
-#pragma unroll
-        for (int r = lane; r < kN; r += 32) ok = ok && (uint32_t)rows[r] == r0 + (uint32_t)r;
-        run = __all_sync(0xffffffffu, ok);
+    // ---- a2 for unit u: index columns, token metadata, masks; compaction of
+    // [c0, c1) into list u & 1: valid SWA slots first, then valid compressed
+    // slots, each in column order; publishes the unit (its first tile tile0).
+    // List u & 1 was last read by the gathers of unit u - 2, all issued before
+    // every producer warp reached this compaction.
+    auto compact = [&](int u, int tile0, int& o_nswa, int& o_nvalid) -> bool {
+      Unit& U = sm.unit[u];
+      const int t = U.t, c0 = U.c0;
+      int c1 = U.c1;
+      if (c1 - c0 > kMaxCols) {              // the planner prevents this; never write past the list
+        if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
+        c1 = c0 + kMaxCols;
       }
-      if (run) {
-        // every row of the box was checked against the pool's row count in the set-up
-        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa_run) : static_cast<const void*>(&P.tm_comp_run);
-        if (pw == 0 && lane < C::kRegions)
-          tma_load_2d(stage + lane * C::kRegionKV, tmap, (int)rank * kHalfDims + lane * (128 / C::kElem), rows[0],
-                      bar(sm.kv_full[st]));
-      } else {
-        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
-        const int groups = (n4 / 4) * C::kRegions;
-        for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
-          const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
-          tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
-                      rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
-                      bar(sm.kv_full[st]));
+      int32_t* list = idx_s + (u & 1) * kMaxCols;
+      const int nchunks = (c1 - c0 + 31) / 32;
+      int32_t rv[kChunksPerProducer];
+      if (p.bt == nullptr) {                 // index form: independent loads, all in flight together
+        const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+#pragma unroll
+        for (int q = 0; q < kChunksPerProducer; ++q) {
+          const int col = c0 + (warp + q * kProducerWarps) * 32 + lane;
+          rv[q] = col < c1 ? __ldg(irow + col) : -1;
+        }
+      } else {                               // page-table form: compressed rows from the page table
+        const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+#pragma unroll
+        for (int q = 0; q < kChunksPerProducer; ++q) {
+          const int col = c0 + (warp + q * kProducerWarps) * 32 + lane;
+          rv[q] = -1;
+          if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
         }
       }
+      const TokenInfo ti = token_info(p, t);
+      c1 = min(c1, max(c0, ti.n_lim));     // active columns of the unit
+#pragma unroll
+      for (int q = 0; q < kChunksPerProducer; ++q) {
+        const int k = warp + q * kProducerWarps;
+        if (k < nchunks) {
+          const int col = c0 + k * 32 + lane;
+          const int idx = rv[q];
+          rv[q] = -1;
+          if (col < c1) {
+            const bool swa = col < kSwaCols;
+            bool valid = idx != -1 && (!swa || col < ti.w_swa);
+            if (valid) {
+              const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+              if (idx < 0 || (int64_t)idx >= nrows) {
+                valid = false;
+                if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+              }
+            }
+            if (valid) rv[q] = idx;
+          }
+          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+          const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
+          if (lane == 0) {
+            sm.chunk_cnt[k] = __popc(ball);
+            sm.chunk_swa[k] = __popc(ball_swa);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.prod_counts));
+      if (!warp_wait(cx, bar(sm.prod_counts), u & 1)) return false;
+      // every producer warp scans the chunk counts itself (at most 72)
+      int chunk_base[kChunksPerProducer];
+      int nvalid = 0, nswa = 0;
+#pragma unroll
+      for (int q = 0; q < kChunksPerProducer; ++q) chunk_base[q] = 0;
+      for (int base0 = 0; base0 < nchunks; base0 += 32) {
+        const int k = base0 + lane;
+        const int v = k < nchunks ? sm.chunk_cnt[k] : 0;
+        int sw = k < nchunks ? sm.chunk_swa[k] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int w = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+#pragma unroll
+        for (int q = 0; q < kChunksPerProducer; ++q) {
+          const int kq = warp + q * kProducerWarps;
+          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
+          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = nvalid + excl;
+        }
+        nvalid += __shfl_sync(0xffffffffu, incl, 31);
+        nswa += sw;
+      }
+#pragma unroll
+      for (int q = 0; q < kChunksPerProducer; ++q) {
+        const int k = warp + q * kProducerWarps;
+        if (k < nchunks) {
+          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+          if (rv[q] >= 0) list[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.prod_list));
+      if (!warp_wait(cx, bar(sm.prod_list), u & 1)) return false;   // the list is complete; the chunk counts are free
+      if (warp == 0 && lane == 0) {
+        U.nswa = nswa;
+        U.nvalid = nvalid;
+        const int tswa = (nswa + kN - 1) / kN, tcomp = (nvalid - nswa + kN - 1) / kN;
+        U.ntiles = tswa + tcomp;
+        U.tile0 = tile0;
+        U.swa_tail = nswa - (tswa - 1) * kN;
+        U.last_tail = tcomp > 0 ? nvalid - nswa - (tcomp - 1) * kN : U.swa_tail;
+        mbar_arrive(bar(sm.unit_ready[u]));
+      }
+      o_nswa = nswa;
+      o_nvalid = nvalid;
+      return true;
+    };
+
+    int next_j = pg;                         // the next tile this group issues (after the loop: past its last one)
+    int nswa = 0, nvalid = 0;                // the current unit's counts
+    bool ok = nunits == 0 || compact(0, 0, nswa, nvalid);
+    int tile0 = 0;                           // the current unit's first tile
+    for (int u = 0; ok && u < nunits; ++u) {
+      const int tswa = (nswa + kN - 1) / kN;
+      const int ntiles = tswa + (nvalid - nswa + kN - 1) / kN;
+      const int32_t* list = idx_s + (u & 1) * kMaxCols;
+      // tiles issued before the next unit's compaction: unit 0's first ring
+      const int k_early = u == 0 ? C::kStages : 0;
+      int nswa_next = 0, nvalid_next = 0;
+      bool compacted = u + 1 >= nunits;
+      // ---- gathers of the unit's tiles (global tile j = tile0 + k)
+      for (;;) {
+        if (!compacted && next_j - tile0 >= min(k_early, ntiles)) {
+          if (!(ok = compact(u + 1, tile0 + ntiles, nswa_next, nvalid_next))) break;
+          compacted = true;
+        }
+        if (next_j >= tile0 + ntiles) break;
+        const int j = next_j, k = j - tile0;
+        const int st = j % C::kStages;
+        if (!(ok = warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1))) break;
+        const int start = k < tswa ? k * kN : nswa + (k - tswa) * kN;
+        const int n = min(kN, (k < tswa ? nswa : nvalid) - start);
+        const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
+        if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
+        const uint32_t stage = kv_addr + st * C::kStageBytes;
+        const int32_t* rows = list + start;
+        bool run = false;                      // rows[r] == rows[0] + r for every r < N
+        if (n == kN) {
+          const uint32_t r0 = (uint32_t)rows[0];
+          bool same = true;
+#pragma unroll
+          for (int r = lane; r < kN; r += 32) same = same && (uint32_t)rows[r] == r0 + (uint32_t)r;
+          run = __all_sync(0xffffffffu, same);
+        }
+        if (run) {
+          // every row of the box was checked against the pool's row count in the compaction
+          const void* tmap = k < tswa ? static_cast<const void*>(&P.tm_swa_run) : static_cast<const void*>(&P.tm_comp_run);
+          if (pw == 0 && lane < C::kRegions)
+            tma_load_2d(stage + lane * C::kRegionKV, tmap, (int)rank * kHalfDims + lane * (128 / C::kElem), rows[0],
+                        bar(sm.kv_full[st]));
+        } else {
+          const void* tmap = k < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
+          const int groups = (n4 / 4) * C::kRegions;
+          for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
+            const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
+            tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
+                        rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
+                        bar(sm.kv_full[st]));
+          }
+        }
+        next_j += kProducerGroups;
+      }
+      tile0 += ntiles;
+      nswa = nswa_next;
+      nvalid = nvalid_next;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     // Leave no TMA write of this group in flight, also after an abort: wait
     // (bounded, not cut short by the abort flag) for the last tiles it issued,
     // at most one per stage.  Normally the consumers have waited for them.
-    for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
+    for (int jj = max(pg, next_j - C::kStages); jj < next_j; ++jj)
       if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
   } else if (warp < kMmaWarp + kQkWarps) {
-    // ============================================================ QK issue
+    // ============================================================ Q load and QK issue
     // QK and PV are issued by different warps so that a QK never waits behind
-    // a PV (which waits for the softmax): the QK of tile k depends only on its
-    // data and a free S buffer.  A thread's chain of dependent MMAs into one
-    // accumulator is issued about one instruction per 150 ns (measured), so
-    // the tiles' QK chains are spread over three warps, one per S buffer,
-    // whose MMAs the tensor core interleaves.
+    // a PV (which waits for the softmax): the QK of tile j depends only on its
+    // data, the unit's Q and a free S buffer.  The issuer of the unit's first
+    // tile goes first and the others start once that QK has
+    // completed (on a GB300 a QK issued by a second warp before the first one
+    // finished gave wrong logits for some heads in repeated runs; observed,
+    // cause not identified).
     constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
     const int qi = warp - kMmaWarp;
-    // The other issuers start only once the CTA's first QK has completed:
-    // on a GB300, a QK issued by a second warp before the first one finished
-    // gave wrong logits for some heads in repeated runs (observed, cause
-    // not identified); after that the issuers' chains overlap freely.
-    bool ok = qi == 0 || ntiles <= qi || warp_wait(cx, bar(sm.qk0_done), 0);
-    for (int k = qi; ok && k < ntiles; k += kQkWarps) {
-      const int st = k % C::kStages;
-      if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) break;
-      const int b = k % kSBufs;
-      if (!warp_wait(cx, bar(sm.s_empty[b]), ((k / kSBufs) & 1) ^ 1)) break;
-      fence_proxy_async_smem();
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t stage = kv_addr + st * C::kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < C::kK1; ++kk) {
-          const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
-          const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
-          mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(sm.s_full[b]));
-        if (k == 0) mma_commit(bar(sm.qk0_done));
+    const uint32_t qbytes = (uint32_t)(C::kRegions * H * 128);
+    // Q of token tq, loaded by warp kMmaWarp: the first unit's at once (before
+    // its index compaction is done), a later unit's once every QK of the
+    // previous unit that used Q is done.  The first unit counts as using Q
+    // even when it has no tile, so that every load is followed by one wait of
+    // every QK warp and one commit of each (no parity wait can fall two
+    // phases behind or ahead).
+    auto load_q = [&](int tq) {
+      if (qi == 0 && lane == 0) {
+        mbar_arrive_expect_tx(bar(sm.q_full), qbytes);
+        for (int kb = 0; kb < C::kRegions; ++kb)
+          tma_load_3d(q_addr + kb * C::kRegionQ, &P.tm_q, (int)rank * kHalfDims + kb * (128 / C::kElem), 0, tq,
+                      bar(sm.q_full));
       }
       __syncwarp();
+    };
+    bool ok = true;
+    int ne = 0;                              // units that used Q so far
+    int nf = 0;                              // units with tiles so far
+    if (nunits > 0) load_q(sm.unit[0].t);
+    for (int u = 0; ok && u < nunits; ++u) {
+      if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
+      const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0, t = sm.unit[u].t;
+      if (ntiles == 0 && u > 0) continue;
+      if (u > 0) {
+        if (qi == 0 && !(ok = warp_wait(cx, bar(sm.qk_unit_done), (ne - 1) & 1))) break;
+        load_q(t);
+      }
+      if (!(ok = warp_wait(cx, bar(sm.q_full), ne & 1))) break;
+      const int first = (qi - tile0 % kSBufs + kSBufs) % kSBufs;   // this warp's first tile of the unit (local index)
+      if (first > 0 && first < ntiles && !(ok = warp_wait(cx, bar(sm.qk_first), nf & 1))) break;
+      for (int k = first; k < ntiles; k += kQkWarps) {
+        const int j = tile0 + k;
+        const int st = j % C::kStages;
+        if (!(ok = warp_wait(cx, bar(sm.kv_full[st]), (j / C::kStages) & 1))) break;
+        const int b = j % kSBufs;
+        if (!(ok = warp_wait(cx, bar(sm.s_empty[b]), ((j / kSBufs) & 1) ^ 1))) break;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t stage = kv_addr + st * C::kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kK1; ++kk) {
+            const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
+            const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
+            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(sm.s_full[b]));
+          if (k == 0) mma_commit(bar(sm.qk_first));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(bar(sm.qk_unit_done));     // completes once every QK above is done
+      __syncwarp();
+      ++ne;
+      if (ntiles > 0) ++nf;
     }
-    if (lane == 0) mma_commit(bar(sm.qk_done));   // completes once every QK issued above is done
+    if (lane == 0) mma_commit(bar(sm.qk_done));
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ============================================================ PV issue
     constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
-    for (int jj = 0; jj < ntiles; ++jj) {
-      const int b = jj & 1, st = jj % C::kStages;
-      if (!warp_wait(cx, bar(sm.p_full[b]), (jj >> 1) & 1)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t stage = kv_addr + st * C::kStageBytes;
+    bool ok = true;
+    for (int u = 0; ok && u < nunits; ++u) {
+      if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
+      // the unit's first PV overwrites O: the previous unit's O must have been
+      // read out (waited for every unit, so that this warp runs at most one
+      // unit ahead of the epilogue)
+      if (u > 0 && !(ok = warp_wait(cx, bar(sm.o_free), (u - 1) & 1))) break;
+      const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0;
+      for (int k = 0; k < ntiles; ++k) {
+        const int j = tile0 + k;
+        const int b = j & 1, st = j % C::kStages;
+        if (!(ok = warp_wait(cx, bar(sm.p_full[b]), (j >> 1) & 1))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t stage = kv_addr + st * C::kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < C::kK2; ++kk) {
-          const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
-          mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
-                           idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < C::kK2; ++kk) {
+            const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
+            mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
+                             idesc_pv, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(sm.p_empty[b]));
+          mma_commit(bar(sm.kv_empty[st]));
         }
-        mma_commit(bar(sm.p_empty[b]));
-        mma_commit(bar(sm.kv_empty[st]));
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) mma_commit(bar(sm.unit_pv_done));     // completes once every PV of the unit is done
       __syncwarp();
     }
     if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every PV issued above is done
     __syncwarp();
-  } else {
+  } else if (warp >= kSoftmaxWarp0) {
     // ============================================================ softmax / epilogue
     // Two warpgroups take turns: warpgroup g handles tiles j with j % 2 == g
     // (all N slots; S, P and exchange buffer g).  The only hand-off between
-    // consecutive tiles is the running reference maximum m(j), published by
-    // the warpgroup of tile j as soon as it is known, so one warpgroup's
-    // exponentials overlap the other's loads and exchange.
+    // consecutive tiles of a unit is the running reference maximum m(j),
+    // published by the warpgroup of tile j as soon as it is known, so one
+    // warpgroup's exponentials overlap the other's loads and exchange.
     const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;
@@ -489,7 +660,9 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer) + g * kBarStride;
     const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[0]), peer) + g * kBarStride;
     const uint32_t p_cols = C::kPCol + g * C::kPCols;  // P buffer g
-    if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
+    // the output scales, loaded now so that their latency hides behind the first tile
+    if (active)
+      sm.epi[g][h] = make_float2(load_scale(p.bmm2, p.bmm2_dev), p.sinks ? __ldg(p.sinks + h) * kLog2e : 0.f);
     if (!active) {
       // rows of absent heads: P = 0, so O stays 0 there
       uint32_t zr[C::kPCols];
@@ -531,213 +704,195 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       return true;
     };
 
-    float m_last = -INFINITY, l_run = 0.f;            // reference and row sum of my warpgroup's tiles
-    // E4M3 P keeps 3 mantissa bits: under a lagging reference a row's largest P
-    // (up to 2^8) is rounded by up to 1/16, which shows when few slots carry the
-    // mass, so short tile chains move the reference on every new maximum (the
-    // same choice in both CTAs: ntiles is the pair's).
-    const float thr = (kFp8 && ntiles <= kExactRefTiles) ? 0.f : kRescaleThreshold;
-    bool ok = true;
-    if (g < ntiles) ok = push(g);
-    int j = g;
     const uint64_t c2 = f2_pack(c, c);
-    for (; ok && j < ntiles; j += 2) {
-      const int n_cur = tile_n(j);
-      const int sb = j % kSBufs;
-      // S(j) is final (this warpgroup pushed it): its TMEM load overlaps the wait for the peer's half
-      float sv[kN];
-      if (active) {
-#pragma unroll
-        for (int hb = 0; hb < kN / 32; ++hb) {
-          uint32_t r[32];
-          tmem_ld32(tl + kSCol + sb * kN + hb * 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
-        }
+    bool ok = true;
+    for (int u = 0; u < nunits; ++u) {
+      if (ok) ok = warp_wait(cx, bar(sm.unit_ready[u]), 0);
+      const Unit& U = sm.unit[u];
+      const int ntiles = ok ? U.ntiles : 0, tile0 = U.tile0;
+      const int jend = tile0 + ntiles, jswa = tile0 + (U.nswa + kN - 1) / kN;   // past the unit's last tile / SWA tile
+      float m_last = -INFINITY, l_run = 0.f;            // reference and row sum of my warpgroup's tiles of the unit
+      // E4M3 P keeps 3 mantissa bits: under a lagging reference a row's largest
+      // P (up to 2^8) is rounded by up to 1/16, which shows when few slots carry
+      // the mass, so short tile chains move the reference on every new maximum
+      // (the same choice in both CTAs: ntiles is the pair's).
+      const float thr = (kFp8 && ntiles <= kExactRefTiles) ? 0.f : kRescaleThreshold;
+      const int first = (tile0 & 1) == g ? 0 : 1;        // my first tile of the unit (local index)
+      if (first < ntiles) {
+        if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
+        ok = push(tile0 + first);
       }
-      if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
-      tc_fence_after();
-      float mt = -INFINITY;
-      if (active) {
-        tmem_wait_ld();
-        const uint4* xp = reinterpret_cast<const uint4*>(base + C::kOffX + g * C::kXBytes) + h;
+      for (int j = tile0 + first; ok && j < jend; j += 2) {   // j: tile number within the cluster's work
+        // slots of tile j: N but for the unit's last SWA tile and its last tile
+        // (read from shared memory where needed, which keeps them out of the
+        // registers of the loop)
+        const int n_cur = j == jswa - 1 ? *reinterpret_cast<volatile const int32_t*>(&U.swa_tail)
+                        : j == jend - 1 ? *reinterpret_cast<volatile const int32_t*>(&U.last_tail) : kN;
+        const int sb = j % kSBufs;
+        // S(j) is final (this warpgroup pushed it): its TMEM load overlaps the wait for the peer's half
+        float sv[kN];
+        if (active) {
 #pragma unroll
-        for (int hb = 0; hb < kN / 16; ++hb) {
-          uint32_t w[12];
+          for (int hb = 0; hb < kN / 32; ++hb) {
+            uint32_t r[32];
+            tmem_ld32(tl + kSCol + sb * kN + hb * 32, r);
 #pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            const uint4 x = xp[(hb * 3 + q) * 128];
-            w[4 * q] = x.x;
-            w[4 * q + 1] = x.y;
-            w[4 * q + 2] = x.z;
-            w[4 * q + 3] = x.w;
-          }
-#pragma unroll
-          for (int gq = 0; gq < 4; ++gq) {
-            const uint32_t w0 = w[3 * gq], w1 = w[3 * gq + 1], w2 = w[3 * gq + 2];
-            const float pa = __uint_as_float(w0 << 8), pb = __uint_as_float(w1 << 8), pc = __uint_as_float(w2 << 8);
-            const float pd = __uint_as_float(__byte_perm(__byte_perm(w0, w1, 0x7373), w2, 0x7103));
-            const int i = hb * 16 + 4 * gq;
-            f2_unpack(f2_mul(f2_add(f2_pack(sv[i], sv[i + 1]), f2_pack(pa, pb)), c2), sv[i], sv[i + 1]);
-            f2_unpack(f2_mul(f2_add(f2_pack(sv[i + 2], sv[i + 3]), f2_pack(pc, pd)), c2), sv[i + 2], sv[i + 3]);
+            for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
           }
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (n_cur >= kN) {
-#pragma unroll
-          for (int i = 0; i < kN; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < kN; ++i)
-            if (i < n_cur) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
-        }
-        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(sm.s_empty[sb]));                         // S buffer sb may be overwritten
-        mbar_arrive_cluster_relaxed(xout_free_peer);               // exchange buffer g read out
-      }
-      // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
-      float m_prev = -INFINITY;
-      if (j > 0) {
-        if (!(ok = warp_wait(cx, bar(sm.m_ready[g ^ 1]), ((j - 1) >> 1) & 1))) break;
-        m_prev = sm.m_buf[g ^ 1][h];
-      }
-      const float m_cur = (mt > m_prev + thr) ? mt : m_prev;
-      sm.m_buf[g][h] = m_cur;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
-      // ---- look ahead: my next tile's partial S to the peer (before this tile's
-      // exponentials, so that the peer has it by the time it gets there)
-      if (j + 2 < ntiles && !(ok = push(j + 2))) break;
-      // ---- P = 2^(x - m(j)); this warpgroup's row sum, rescaled to m(j)
-      if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
-      tc_fence_after();
-      if (active) {
-        l_run *= (m_last == -INFINITY) ? 0.f : fast_exp2(m_last - m_cur);
-        m_last = m_cur;
-        const uint64_t nm2 = f2_pack(-m_cur, -m_cur);
-#pragma unroll
-        for (int i = 0; i < kN; i += 2) {
-          float x0, x1;
-          f2_unpack(f2_add(f2_pack(sv[i], sv[i + 1]), nm2), x0, x1);
-          sv[i] = fast_exp2(x0);
-          sv[i + 1] = fast_exp2(x1);
-        }
-        if (n_cur < kN) {
-#pragma unroll
-          for (int i = 0; i < kN; ++i)
-            if (i >= n_cur) sv[i] = 0.f;
-        }
-        uint64_t s4[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int i = 0; i < kN; i += 2) s4[(i >> 1) & 1] = f2_add(s4[(i >> 1) & 1], f2_pack(sv[i], sv[i + 1]));
-        float s0, s1, s2, s3;
-        f2_unpack(s4[0], s0, s1);
-        f2_unpack(s4[1], s2, s3);
-        l_run += (s0 + s1) + (s2 + s3);
-        uint32_t pr[C::kPCols];
-        if constexpr (kFp8) {
-#pragma unroll
-          for (int i = 0; i < C::kPCols; ++i)
-            pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i], sv[4 * i + 1]), __NV_SATFINITE, __NV_E4M3) |
-                    ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i + 2], sv[4 * i + 3]), __NV_SATFINITE, __NV_E4M3) << 16);
-        } else {
-#pragma unroll
-          for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-        }
-        tmem_st16(tl + p_cols, pr);
-      }
-      // ---- O rescale when the reference moved (O holds tiles < j at m(j-1))
-      const bool rescale = active && j > 0 && m_cur != m_prev;
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!(ok = warp_wait(cx, bar(sm.p_empty[g ^ 1]), ((j - 1) >> 1) & 1))) break;
+        if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
         tc_fence_after();
-        const float alpha = rescale ? fast_exp2(m_prev - m_cur) : 1.f;
-#pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 16; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(tl + kOCol + cc * 16, r);
+        float mt = -INFINITY;
+        if (active) {
           tmem_wait_ld();
+          const uint4* xp = reinterpret_cast<const uint4*>(base + C::kOffX + g * C::kXBytes) + h;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st16(tl + kOCol + cc * 16, r);
+          for (int hb = 0; hb < kN / 16; ++hb) {
+            uint32_t w[12];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              const uint4 x = xp[(hb * 3 + q) * 128];
+              w[4 * q] = x.x;
+              w[4 * q + 1] = x.y;
+              w[4 * q + 2] = x.z;
+              w[4 * q + 3] = x.w;
+            }
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+              const uint32_t w0 = w[3 * gq], w1 = w[3 * gq + 1], w2 = w[3 * gq + 2];
+              const float pa = __uint_as_float(w0 << 8), pb = __uint_as_float(w1 << 8), pc = __uint_as_float(w2 << 8);
+              const float pd = __uint_as_float(__byte_perm(__byte_perm(w0, w1, 0x7373), w2, 0x7103));
+              const int i = hb * 16 + 4 * gq;
+              f2_unpack(f2_mul(f2_add(f2_pack(sv[i], sv[i + 1]), f2_pack(pa, pb)), c2), sv[i], sv[i + 1]);
+              f2_unpack(f2_mul(f2_add(f2_pack(sv[i + 2], sv[i + 3]), f2_pack(pc, pd)), c2), sv[i + 2], sv[i + 3]);
+            }
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (n_cur >= kN) {
+#pragma unroll
+            for (int i = 0; i < kN; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kN; ++i)
+              if (i < n_cur) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+          }
+          mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
+        if (leader && j + 2 < jend) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(sm.s_empty[sb]));                       // S buffer sb may be overwritten
+          mbar_arrive_cluster_relaxed(xout_free_peer);             // exchange buffer g read out
+        }
+        // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
+        float m_prev = -INFINITY;
+        if (j > tile0) {
+          if (!(ok = warp_wait(cx, bar(sm.m_ready[g ^ 1]), ((j - 1) >> 1) & 1))) break;
+          m_prev = sm.m_buf[g ^ 1][h];
+        }
+        const float m_cur = (mt > m_prev + thr) ? mt : m_prev;
+        sm.m_buf[g][h] = m_cur;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
+        // ---- look ahead: my next tile's partial S to the peer (before this tile's
+        // exponentials, so that the peer has it by the time it gets there)
+        if (j + 2 < jend && !(ok = push(j + 2))) break;
+        // ---- P = 2^(x - m(j)); this warpgroup's row sum, rescaled to m(j)
+        if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
+        tc_fence_after();
+        if (active) {
+          l_run *= (m_last == -INFINITY) ? 0.f : fast_exp2(m_last - m_cur);
+          m_last = m_cur;
+          const uint64_t nm2 = f2_pack(-m_cur, -m_cur);
+#pragma unroll
+          for (int i = 0; i < kN; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_add(f2_pack(sv[i], sv[i + 1]), nm2), x0, x1);
+            sv[i] = fast_exp2(x0);
+            sv[i + 1] = fast_exp2(x1);
+          }
+          if (n_cur < kN) {
+#pragma unroll
+            for (int i = 0; i < kN; ++i)
+              if (i >= n_cur) sv[i] = 0.f;
+          }
+          uint64_t s4[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int i = 0; i < kN; i += 2) s4[(i >> 1) & 1] = f2_add(s4[(i >> 1) & 1], f2_pack(sv[i], sv[i + 1]));
+          float s0, s1, s2, s3;
+          f2_unpack(s4[0], s0, s1);
+          f2_unpack(s4[1], s2, s3);
+          l_run += (s0 + s1) + (s2 + s3);
+          uint32_t pr[C::kPCols];
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int i = 0; i < C::kPCols; ++i)
+              pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i], sv[4 * i + 1]), __NV_SATFINITE, __NV_E4M3) |
+                      ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i + 2], sv[4 * i + 3]), __NV_SATFINITE, __NV_E4M3) << 16);
+          } else {
+#pragma unroll
+            for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+          }
+          tmem_st16(tl + p_cols, pr);
+        }
+        // ---- O rescale when the reference moved (O holds the unit's tiles < j at m(j-1))
+        const bool rescale = active && j > tile0 && m_cur != m_prev;
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (!(ok = warp_wait(cx, bar(sm.p_empty[g ^ 1]), ((j - 1) >> 1) & 1))) break;   // PV(j - 1) done
+          tc_fence_after();
+          const float alpha = rescale ? fast_exp2(m_prev - m_cur) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < kHalfDims / 16; ++cc) {
+            uint32_t r[16];
+            tmem_ld16(tl + kOCol + cc * 16, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(tl + kOCol + cc * 16, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.p_full[g]));
       }
-      tmem_wait_st();
-      tc_fence_before();
+
+      // ---- the unit's end: both warpgroups' row sums brought to the final reference
+      const int ub = u & 1;
+      if (active) {
+        sm.lsum[ub][g][h] = l_run;
+        sm.m_end[ub][g][h] = m_last;
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.p_full[g]));
-    }
-    // total row sum: both warpgroups' sums brought to the final reference
-    if (active) {
-      sm.lsum[g][h] = l_run;
-      sm.m_end[g][h] = m_last;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(sm.lsum_full));
-    if (ok) ok = warp_wait(cx, bar(sm.lsum_full), 0);
-    if (ok && ntiles > 0) {
-      ok = warp_wait(cx, bar(sm.o_full), 0);
-      tc_fence_after();
-    }
-    if (active) {
-      float l_tot = 0.f, m_fin = -INFINITY;
+      if (lane == 0) mbar_arrive(bar(sm.lsum_full));
+      if (ok) ok = warp_wait(cx, bar(sm.lsum_full), u & 1);
       if (ok) {
-        const float ma = sm.m_end[0][h], mb = sm.m_end[1][h];
-        m_fin = fmaxf(ma, mb);
-        if (m_fin != -INFINITY) {
-          if (ma != -INFINITY) l_tot += sm.lsum[0][h] * fast_exp2(ma - m_fin);
-          if (mb != -INFINITY) l_tot += sm.lsum[1][h] * fast_exp2(mb - m_fin);
+        ok = warp_wait(cx, bar(sm.unit_pv_done), u & 1);
+        tc_fence_after();
+      }
+      if (active) {
+        float l_tot = 0.f, m_fin = -INFINITY;
+        if (ok) {
+          const float ma = sm.m_end[ub][0][h], mb = sm.m_end[ub][1][h];
+          m_fin = fmaxf(ma, mb);
+          if (m_fin != -INFINITY) {
+            if (ma != -INFINITY) l_tot += sm.lsum[ub][0][h] * fast_exp2(ma - m_fin);
+            if (mb != -INFINITY) l_tot += sm.lsum[ub][1][h] * fast_exp2(mb - m_fin);
+          }
         }
-      }
-      const bool have = ok && ntiles > 0 && l_tot > 0.f;
-      const float lse = have ? m_fin + fast_log2(l_tot) : -INFINITY;
-      float f = have ? 1.f / l_tot : 0.f;
-      if (S == 1) {
-        f *= load_scale(p.bmm2, p.bmm2_dev);
-        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
-      }
-      const int64_t row_th = (int64_t)t * H + h;
-      if constexpr (!kPartial) {
-#pragma unroll 1
-      for (int cc = 0; cc < kHalfDims / 64; ++cc) {
-        const int col = g * (kHalfDims / 2) + cc * 32;
-        float v[32];
-        if (have) {
-          uint32_t r[32];
-          tmem_ld32(tl + kOCol + col, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
+        const bool have = ok && ntiles > 0 && l_tot > 0.f;
+        const float lse = have ? m_fin + fast_log2(l_tot) : -INFINITY;
+        float f = have ? 1.f / l_tot : 0.f;
+        __nv_bfloat16* dst;
+        if (!U.partial) {
+          const float2 e = sm.epi[g][h];
+          f *= e.x;
+          if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(e.y - lse));
+          dst = p.out + ((int64_t)U.t * H + h) * kHeadDim;
         } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          dst = (P.clusters ? P.piece_o : p.part_o) + U.part_row + (int64_t)h * U.part_hstride;
         }
-        const int d0 = (int)rank * kHalfDims + col;
-        uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      }
-      if (rank == 0 && g == 0) {
-        if (S == 1) {
-          if (p.out_lse) p.out_lse[row_th] = lse;
-        } else {
-          p.part_lse[row_th * S + s] = lse;
-        }
-      }
-      } else {
-        // BF16 partial rows go through shared memory (the KV stages are free
-        // once every PV is done), so that the global stores below are whole
-        // 256-byte row segments rather than one 16-byte piece per row per warp
-        // instruction.  Warpgroup g stages its 128 columns; 16-byte chunks are
-        // XOR-swizzled by the row to spread banks.
-        unsigned char* row = base + C::kOffKV + g * (128 * 256) + h * 256;
 #pragma unroll 1
         for (int cc = 0; cc < kHalfDims / 64; ++cc) {
           const int col = g * (kHalfDims / 2) + cc * 32;
@@ -752,27 +907,24 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
+          uint4* o = reinterpret_cast<uint4*>(dst + (int)rank * kHalfDims + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
-                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         }
-        if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
+        if (rank == 0 && g == 0) {
+          if (!U.partial) {
+            if (p.out_lse) p.out_lse[(int64_t)U.t * H + h] = lse;
+          } else {
+            (P.clusters ? P.piece_lse : p.part_lse)[U.lse_row + (int64_t)h * U.lse_hstride] = lse;
+          }
+        }
       }
-    }
-    // copy-out of this warpgroup's staged partial columns, 256 contiguous bytes
-    // per row (half a warp per row)
-    if constexpr (kPartial) {
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(128) : "memory");
-      const unsigned char* stg = base + C::kOffKV + g * (128 * 256);
-      const int w4 = (warp - kSoftmaxWarp0) & 3;
-      const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
-      const int c = lane & 15;
-      for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
-        const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((c ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + c * 8) = x;
-      }
+      // O read out: the next unit's first PV may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.o_free));
     }
   }
 
@@ -828,13 +980,35 @@ cudaError_t encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The query as [T, H, 512] (heads 512 elements apart, tokens q_stride_token
+// apart); box 128 bytes x H heads x 1 token; 128-byte swizzle.  The call's
+// checks make q 16-byte aligned and q_stride_token a multiple of 16 bytes.
+static cudaError_t encode_query_map(CUtensorMap* map, const DecodeParams& p) {
+  EncodeTiledFn fn = nullptr;
+  cudaError_t e = encode_fn(&fn);
+  if (e != cudaSuccess) return e;
+  const int elem = p.dtype == SMLA_BF16 ? 2 : 1;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)p.H, (cuuint64_t)(p.sum_q > 0 ? p.sum_q : 1)};
+  const cuuint64_t strides[2] = {(cuuint64_t)(kHeadDim * elem), (cuuint64_t)(p.q_stride_token * elem)};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem), (cuuint32_t)p.H, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, p.dtype == SMLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                  const_cast<void*>(p.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int tc_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes; }
 int tc_threads() { return kThreads; }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams& p, int grid, int clusters, __nv_bfloat16* piece_o, float* piece_lse,
+                             cudaStream_t stream) {
   TcParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
+  P.clusters = clusters;
+  P.piece_o = piece_o;
+  P.piece_lse = piece_lse;
   // a pool of fewer than N rows holds no run of N rows: its run map is never used
   const int64_t run_rows = p.dtype == SMLA_BF16 ? Cfg<false>::kN : Cfg<true>::kN;
   const int swa_run = (int)std::max<int64_t>(1, std::min(run_rows, p.swa_rows));
@@ -843,6 +1017,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype, 1);
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_swa_run, p.swa, p.swa_rows, p.swa_stride, p.dtype, swa_run);
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp_run, p.comp, p.comp_rows, p.comp_stride, p.dtype, comp_run);
+  if (e == cudaSuccess) e = encode_query_map(&P.tm_q, p);
   if (e != cudaSuccess) return e;
   const int smem = tc_smem_bytes(p.dtype);
   auto launch = [&](auto kernel) -> cudaError_t {
@@ -851,11 +1026,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
     kernel<<<grid, kThreads, smem, stream>>>(P);
     return cudaSuccess;
   };
-  const bool partial = p.num_splits > 1;
-  if (p.dtype == SMLA_BF16)
-    e = partial ? launch(decode_tc_kernel<false, true>) : launch(decode_tc_kernel<false, false>);
-  else
-    e = partial ? launch(decode_tc_kernel<true, true>) : launch(decode_tc_kernel<true, false>);
+  e = p.dtype == SMLA_BF16 ? launch(decode_tc_kernel<false>) : launch(decode_tc_kernel<true>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -58,6 +58,8 @@ smla_status check_shapes(const smla_args* a) {
     return fail(SMLA_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", a->num_splits, SMLA_MAX_SPLITS);
   if (a->max_splits < 0 || a->max_splits > SMLA_MAX_SPLITS)
     return fail(SMLA_ERR_INVALID_ARG, "max_splits %d outside [0, %d]", a->max_splits, SMLA_MAX_SPLITS);
+  if (a->schedule < SMLA_SCHEDULE_AUTO || a->schedule > SMLA_SCHEDULE_BALANCED)
+    return fail(SMLA_ERR_INVALID_ARG, "schedule %d is not an smla_schedule", a->schedule);
   if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05 &&
       a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     return fail(SMLA_ERR_INVALID_ARG, "kernel %d is not a smla_kernel", a->kernel);
@@ -197,8 +199,9 @@ smla_status validate_host(const smla_args* a) {
   return SMLA_OK;
 }
 
-// Kernel that SMLA_KERNEL_AUTO selects.
+// Kernel and schedule that SMLA_KERNEL_AUTO / SMLA_SCHEDULE_AUTO select.
 constexpr int kAutoKernel = SMLA_KERNEL_TCGEN05;
+constexpr int kAutoSchedule = SMLA_SCHEDULE_GRID;
 
 std::atomic<int> g_sm_count[64];   // per device; 0 = not queried yet (callers may be on several threads)
 
@@ -223,7 +226,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   const int kernel = a->kernel == SMLA_KERNEL_AUTO ? kAutoKernel : a->kernel;
   int S = a->num_splits;
   if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED) {
-    // One 2-CTA cluster per (token, split), one cluster per pair of SMs.
+    // 2-CTA clusters: balanced mode, else one cluster per (token, split).
     const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
     plan->kernel = head_owned ? SMLA_KERNEL_TCGEN05_HEAD_OWNED : SMLA_KERNEL_TCGEN05;
     plan->ctas_per_split = 2;
@@ -235,10 +238,34 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     if (S != 0 && S < s_min)
       return fail(SMLA_ERR_INVALID_ARG, "num_splits %d < %d: the tcgen05 kernel takes at most %d columns per split",
                   S, s_min, SMLA_TC_MAX_SPLIT_COLS);
+    const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
+    const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
+    if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned &&
+        a->width <= SMLA_TC_MAX_SPLIT_COLS && a->sum_q <= (int64_t)(SMLA_TC_MAX_UNITS - 2) * pairs) {
+      // Balanced mode: P clusters, one per SM pair, take equal shares of the
+      // T x W columns, each share at least 64 columns.  A share of at most
+      // (SMLA_TC_MAX_UNITS - 2) W columns touches at most SMLA_TC_MAX_UNITS - 1
+      // tokens, and no unit is wider than W.  Wider tables and larger batches
+      // take grid mode (the latter in many waves, where a partial last wave
+      // costs little).
+      const int64_t total = (int64_t)a->sum_q * a->width;
+      int64_t P = total / 64;
+      if (P > pairs) P = pairs;
+      if (P < 1) P = 1;
+      plan->num_splits = 1;
+      plan->clusters = (int32_t)P;
+      plan->grid = (int32_t)(2 * P);
+      if (P > 1) {
+        const size_t rows = (size_t)2 * P * a->num_heads;
+        // BF16 normalised pieces, then their fp32 base-2 LSEs
+        plan->workspace_bytes =
+            align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256) + align_up(rows * sizeof(float), 256);
+      }
+      return SMLA_OK;
+    }
     if (S == 0) {
       // as many splits as keep every cluster in one wave (a second, partial
       // wave costs a whole unit of time for a few clusters)
-      const int64_t pairs = sms / 2;
       int64_t want = a->sum_q > 0 ? pairs / a->sum_q : 1;
       const int64_t by_width = (a->width + 63) / 64;    // keep >= 64 columns per split
       if (want > by_width) want = by_width;
@@ -385,6 +412,14 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
     p.part_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(a->workspace) +
                                           align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256));
   }
+  __nv_bfloat16* piece_o = nullptr;
+  float* piece_lse = nullptr;
+  if (plan.clusters > 1) {
+    const size_t rows = (size_t)2 * plan.clusters * a->num_heads;
+    piece_o = reinterpret_cast<__nv_bfloat16*>(a->workspace);
+    piece_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(a->workspace) +
+                                         align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256));
+  }
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
   if (a->profile_event_begin) {
@@ -394,11 +429,14 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     ce = launch_decode_tc_head_owned(p, plan.grid, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05)
-    ce = launch_decode_tc(p, plan.grid, stream);
+    ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, stream);
   else
     ce = launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
-  if (plan.num_splits > 1) {
+  if (plan.clusters > 1) {
+    ce = launch_combine_pieces(p, plan.clusters, piece_o, piece_lse, stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
+  } else if (plan.num_splits > 1) {
     ce = launch_combine(p, stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
   }

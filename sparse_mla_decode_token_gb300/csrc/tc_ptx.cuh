@@ -353,3 +353,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 }  // namespace ptx
 }  // namespace smla
+
+namespace smla {
+namespace ptx {
+
+// TMA tile load of a 3-D box at (x, y, z) into shared memory at dst (swizzled
+// as the tensor map says); completes its bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+}  // namespace ptx
+}  // namespace smla

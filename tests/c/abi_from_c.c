@@ -44,15 +44,26 @@ int main(void) {
   smla_plan p;
   smla_status st = smla_plan_decode_for_sm_count(&a, 152, &p);
   CHECK(st == SMLA_OK && p.kernel == SMLA_KERNEL_TCGEN05 && p.num_splits == 1 && p.grid == 256 &&
-            p.workspace_bytes == 0,
-        "plan 128 tokens: kernel %d splits %d grid %d threads %d smem %d", p.kernel, p.num_splits, p.grid,
-        p.threads, p.smem_bytes);
+            p.clusters == 0 && p.workspace_bytes == 0,
+        "plan 128 tokens: kernel %d splits %d grid %d clusters %d threads %d smem %d", p.kernel, p.num_splits,
+        p.grid, p.clusters, p.threads, p.smem_bytes);
+
+  /* balanced schedule: 76 pairs with equal column shares; pieces of cut
+     tokens in 2 x 76 x 128 BF16 rows of 512 plus their LSEs */
+  a.schedule = SMLA_SCHEDULE_BALANCED;
+  st = smla_plan_decode_for_sm_count(&a, 152, &p);
+  size_t pieces = (size_t)2 * 76 * 128;
+  size_t want_pieces = (pieces * 512 * 2 + 255) / 256 * 256 + (pieces * 4 + 255) / 256 * 256;
+  CHECK(st == SMLA_OK && p.num_splits == 1 && p.grid == 152 && p.clusters == 76 && p.workspace_bytes == want_pieces,
+        "plan 128 tokens, balanced: splits %d grid %d clusters %d workspace %zu", p.num_splits, p.grid, p.clusters,
+        p.workspace_bytes);
+  a.schedule = SMLA_SCHEDULE_AUTO;
 
   smla_args b = base(4, 128 + 16384);
   st = smla_plan_decode_for_sm_count(&b, 152, &p);
   size_t rows = (size_t)4 * 128 * 19;
   size_t want = (rows * 512 * 2 + 255) / 256 * 256 + (rows * 4 + 255) / 256 * 256;
-  CHECK(st == SMLA_OK && p.num_splits == 19 && p.grid == 152 && p.workspace_bytes == want,
+  CHECK(st == SMLA_OK && p.num_splits == 19 && p.grid == 152 && p.clusters == 0 && p.workspace_bytes == want,
         "plan 4 long tokens: splits %d grid %d workspace %zu", p.num_splits, p.grid, p.workspace_bytes);
 
   /* host-detectable mistakes: statuses, no CUDA call */

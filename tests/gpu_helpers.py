@@ -36,7 +36,7 @@ DEVERR_FATAL = 0x2 | 0x4      # a bounded on-device wait expired / an internal l
 
 
 def run_gpu(w, d=None, *, num_splits=0, max_splits=0, kernel=B.KERNEL_AUTO, bmm_as_tensor=False,
-            error_word=None, sync=True):
+            error_word=None, sync=True, schedule=B.SCHEDULE_AUTO):
     """Run the decode on the GPU; returns (out bf16 tensor, lse tensor, plan dict).
 
     Every run carries a device error word; a timeout or internal-limit bit fails
@@ -58,7 +58,7 @@ def run_gpu(w, d=None, *, num_splits=0, max_splits=0, kernel=B.KERNEL_AUTO, bmm_
                        sparse_indices=d["indices"], seq_lens=d["seq_lens"], out=out,
                        sparse_topk_lens=d["topk_lens"], cum_seq_lens_q=d["cum"], sinks=d["sinks"],
                        bmm1_scale=bmm1, bmm2_scale=bmm2, out_lse=lse, num_splits=num_splits,
-                       max_splits=max_splits, kernel=kernel, error_word=error_word,
+                       max_splits=max_splits, kernel=kernel, error_word=error_word, schedule=schedule,
                        swa_topk_lens=d.get("swa_topk_lens"), comp_block_tables=d.get("block_tables"),
                        comp_page_size=getattr(w, "comp_page_size", 0), hca_seq_lens=d.get("hca_seq_lens"),
                        width=w.width if getattr(w, "comp_block_tables", None) is not None else None)

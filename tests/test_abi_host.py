@@ -33,7 +33,7 @@ def test_library_exports_every_declared_function(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(B.EXPORTS)
-    assert B.smla_abi_version() == 5
+    assert B.smla_abi_version() == 6
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -299,4 +299,4 @@ def test_plain_c_caller_links_and_runs(lib, tmp_path, compiler):
                    check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "FAIL" not in r.stdout and r.stdout.count("ok ") == 10
+    assert "FAIL" not in r.stdout and r.stdout.count("ok ") == 11

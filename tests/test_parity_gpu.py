@@ -55,9 +55,9 @@ def small_case(seed, *, dtype="bf16", H=128, width=128 + 300, batch=3, q_lens=1,
     T = int(q_lens_arr.sum())
     n_comp = width - 128
     comp_valid = rng.integers(n_comp // 2, n_comp + 1, size=T) if holes else None
-    if topk == "random":
+    if isinstance(topk, str) and topk == "random":
         topk_lens = rng.integers(129, width + 1, size=T)
-    elif topk == "none":
+    elif isinstance(topk, str) and topk == "none":
         topk_lens = None
     else:
         topk_lens = topk
@@ -77,6 +77,58 @@ def test_small_parity(kernel, dtype, H, splits):
     if splits:
         assert plan["num_splits"] == splits
     compare(w, out, lse)
+
+
+# ------------------------------------- balanced mode: shares of the columns
+
+def expected_clusters(T, width, sms):
+    """The planner's cluster count under the balanced schedule (see the
+    header's smla_schedule)."""
+    pairs = max(sms // 2, 1)
+    if width > 2304 or T > 14 * pairs:
+        return 0
+    return max(1, min(pairs, T * width // 64))
+
+
+@pytest.mark.parametrize("dtype,H,batch,q_lens,width,topk", [
+    ("e4m3", 128, 1, 1, 128 + 2048, "none"),     # one token in 34 pieces
+    ("bf16", 64, 3, 1, 128 + 512, "random"),     # three tokens in 10 pieces each
+    ("e4m3", 128, 7, 11, 128 + 512, "random"),   # 77 tokens: most shares cut two tokens
+    ("bf16", 128, 8, 25, 256, "random"),         # 200 tokens: 3 to 4 units per share
+    ("e4m3", 64, 8, 133, 128, "none"),           # 1064 tokens: 14 whole tokens per share
+    ("e4m3", 128, 5, 20, 128 + 128, "zeros"),    # every third token has no active column
+])
+def test_balanced_mode_parity(dtype, H, batch, q_lens, width, topk):
+    """The balanced schedule: each CTA pair takes an equal share of the T x W
+    columns, whole tokens plus pieces of tokens cut at the share boundaries,
+    merged by the piece combine."""
+    T = batch * q_lens
+    if isinstance(topk, str) and topk == "zeros":
+        rng = np.random.default_rng(5)
+        topk = rng.integers(129, width + 1, size=T)
+        topk[::3] = 0
+    w = small_case(300 + T, dtype=dtype, H=H, width=width, batch=batch, q_lens=q_lens, topk=topk,
+                   seq_len=4000)
+    out, lse, plan = run_gpu(w, kernel=B.KERNEL_TCGEN05, schedule=B.SCHEDULE_BALANCED)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["clusters"] == expected_clusters(T, width, sms)
+    assert plan["grid"] == 2 * plan["clusters"] and plan["num_splits"] == 1
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_balanced_and_grid_modes_agree(dtype):
+    """The same workload in balanced mode (which cuts some tokens into
+    pieces) and in grid mode (one pair per token): both match the oracle."""
+    w = small_case(41, dtype=dtype, H=128, width=128 + 640, batch=4, q_lens=40, seq_len=4000)
+    out_b, lse_b, plan_b = run_gpu(w, kernel=B.KERNEL_TCGEN05, schedule=B.SCHEDULE_BALANCED)
+    out_g, lse_g, plan_g = run_gpu(w, kernel=B.KERNEL_TCGEN05)
+    assert plan_b["clusters"] > 1 and plan_g["clusters"] == 0
+    compare(w, out_b, lse_b)
+    compare(w, out_g, lse_g)
+    P, Wd = plan_b["clusters"], w.width
+    cut = {(w.sum_q * Wd * c // P) // Wd for c in range(1, P) if (w.sum_q * Wd * c // P) % Wd}
+    assert cut and len(cut) < w.sum_q
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

@@ -1,13 +1,23 @@
-"""The split planner, called through the C ABI as a pure function of shapes
-and the SM count (no GPU): its documented rules, and the plans the committed
+"""The planner, called through the C ABI as a pure function of shapes and the
+SM count (no GPU): its documented rules, and the plans the committed
 measurements were taken with.
 
-Rules (tcgen05 kernel; one 2-CTA cluster per (token, split), 152 SMs = 76
-pairs on GB300): S = floor(pairs / T) so that every cluster runs in one wave,
-at least 1, capped by max_splits (default 32) and by ceil(W / 64) (at least 64
-columns per split), then raised to ceil(W / 2304) (the columns one CTA stages).
-A forced num_splits below that minimum is an error.  The CUDA-core kernel
-targets 2 resident CTAs per SM with at least 256 columns per split.
+Rules (tcgen05 kernel, 2-CTA clusters, 152 SMs = 76 pairs on GB300):
+
+* balanced mode when the schedule is BALANCED, num_splits and max_splits
+  are 0, the kernel is TCGEN05, W <= 2304 and T <= 14 x pairs: P = min(pairs, T W / 64)
+  clusters (at least 1) take equal shares of the T x W columns; grid = 2 P,
+  num_splits = 1; with P > 1 the workspace holds 2 P x H BF16 pieces of 512
+  and their fp32 LSEs (each part 256-byte aligned);
+* otherwise (and under the default schedule) grid mode, one cluster per
+  (token, split): S = floor(pairs / T)
+  so that every cluster runs in one wave, at least 1, capped by max_splits
+  (default 32) and by ceil(W / 64) (at least 64 columns per split), then
+  raised to ceil(W / 2304) (the columns one CTA stages).  A forced num_splits
+  below that minimum is an error.
+
+The CUDA-core kernel targets 2 resident CTAs per SM with at least 256 columns
+per split.
 """
 import json
 import math
@@ -31,17 +41,25 @@ def lib():
 
 
 def args(T, W_, *, H=128, dtype=B.SMLA_E4M3, batch=None, varlen=False, num_splits=0, max_splits=0,
-         kernel=B.KERNEL_AUTO):
+         kernel=B.KERNEL_AUTO, schedule=B.SCHEDULE_AUTO):
     a = B.SmlaArgs()
     a.sum_q, a.batch, a.num_heads, a.width, a.dtype = T, batch or max(T, 1), H, W_, dtype
     if varlen:
         a.cum_seq_lens_q = 16                 # marks varlen; never read by the planner
-    a.num_splits, a.max_splits, a.kernel = num_splits, max_splits, kernel
+    a.num_splits, a.max_splits, a.kernel, a.schedule = num_splits, max_splits, kernel, schedule
     return a
 
 
 def plan(a, sms=GB300_SMS):
     return B.smla_plan_decode_for_sm_count(a, sms).as_dict()
+
+
+def expected_clusters(T, W_, num_splits=0, max_splits=0, sms=GB300_SMS, schedule=B.SCHEDULE_BALANCED):
+    """Balanced-mode cluster count, 0 where grid mode applies."""
+    pairs = sms // 2
+    if schedule != B.SCHEDULE_BALANCED or num_splits or max_splits or W_ > 2304 or T > 14 * pairs:
+        return 0
+    return max(1, min(pairs, T * W_ // 64))
 
 
 def expected_tc_splits(T, W_, max_splits=0, sms=GB300_SMS):
@@ -60,45 +78,76 @@ def workload_args(n):
 
 
 def test_plans_of_the_committed_traffic_records():
-    """traffic.json stores the launch plan of each ncu capture; the planner
-    still produces exactly that plan for the workload on a GB300."""
+    """traffic.json stores the launch plan and device-code hash of each ncu
+    capture.  A record of the current device code must match the planner's
+    plan for its workload on a GB300; a record of older device code is one
+    that bench.py reports as stale (traffic null), never as a measurement of
+    this code."""
+    import bench
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     by_name = {name: n for n, name in W.CONFIG_NAMES.items()}
-    checked = 0
+    sha = bench.kernel_sources_sha()
     for name, ent in rec.items():
         if name.startswith("_"):
             continue
         got = plan(workload_args(by_name[name]))
-        for k, v in ent["plan"].items():
-            assert got[k] == v, (name, k, got[k], v)
-        checked += 1
-    assert checked == 4
+        traffic, note = bench.traffic_record(name, got)
+        if ent.get("kernel_sources_sha") == sha:
+            for k, v in ent["plan"].items():
+                assert got[k] == v, (name, k, got[k], v)
+            assert traffic == ent["dram_bytes_per_launch"]
+        else:
+            assert traffic is None and sha in note
 
 
 @pytest.mark.parametrize("n,splits,grid", [(1, 4, 16), (2, 2, 128), (3, 1, 256), (4, 1, 324),
                                            (5, 19, 152), (6, 1, 256)])
 def test_named_workload_plans(n, splits, grid):
     p = plan(workload_args(n))
-    assert (p["kernel"], p["num_splits"], p["grid"], p["ctas_per_split"]) == (B.KERNEL_TCGEN05, splits, grid, 2)
+    assert (p["kernel"], p["num_splits"], p["grid"], p["ctas_per_split"], p["clusters"]) == \
+        (B.KERNEL_TCGEN05, splits, grid, 2, 0)
+
+
+@pytest.mark.parametrize("n,grid,clusters", [(1, 16, 8), (2, 152, 76), (3, 152, 76), (4, 152, 76),
+                                             (5, 152, 0), (6, 152, 76)])
+def test_named_workload_balanced_plans(n, grid, clusters):
+    a = workload_args(n)
+    a.schedule = B.SCHEDULE_BALANCED
+    p = plan(a)
+    assert (p["kernel"], p["grid"], p["clusters"]) == (B.KERNEL_TCGEN05, grid, clusters)
 
 
 def test_head_owned_form_is_opt_in_and_e4m3_only():
     """The head-owned softmax form runs only when asked for and only on E4M3
-    rows; BF16 rows asking for it get the default tensor-core kernel.  Both
-    forms share the split rule."""
-    ref = plan(args(128, 2176))
-    ho = plan(args(128, 2176, kernel=B.KERNEL_TCGEN05_HEAD_OWNED))
+    rows; BF16 rows asking for it get the default tensor-core kernel.  It has
+    no balanced mode: one cluster per (token, split), by the grid-mode rule."""
+    ref = plan(args(128, 2176, schedule=B.SCHEDULE_BALANCED))
+    ho = plan(args(128, 2176, kernel=B.KERNEL_TCGEN05_HEAD_OWNED, schedule=B.SCHEDULE_BALANCED))
     assert ref["kernel"] == B.KERNEL_TCGEN05 and ho["kernel"] == B.KERNEL_TCGEN05_HEAD_OWNED
-    assert (ho["num_splits"], ho["grid"], ho["ctas_per_split"]) == (ref["num_splits"], ref["grid"], 2)
-    bf = plan(args(32, 640, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05_HEAD_OWNED))
-    assert bf["kernel"] == B.KERNEL_TCGEN05
+    assert ref["clusters"] == 76 and ho["clusters"] == 0
+    assert (ho["num_splits"], ho["grid"], ho["ctas_per_split"]) == (expected_tc_splits(128, 2176), 256, 2)
+    bf = plan(args(32, 640, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05_HEAD_OWNED, schedule=B.SCHEDULE_BALANCED))
+    assert bf["kernel"] == B.KERNEL_TCGEN05 and bf["clusters"] == 76
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4, 7, 19, 38, 75, 76, 77, 128, 1000])
+def workspace(rows):
+    return -(-rows * 512 * 2 // 256) * 256 + -(-rows * 4 // 256) * 256
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 7, 19, 38, 75, 76, 77, 128, 1000, 1064, 1065])
 @pytest.mark.parametrize("W_", [128, 129, 256, 640, 2176, 2304, 2305, 4608, 16512, 65536])
 @pytest.mark.parametrize("max_splits", [0, 1, 8])
-def test_tc_split_rule(T, W_, max_splits):
-    p = plan(args(T, W_, max_splits=max_splits))
+@pytest.mark.parametrize("schedule", [B.SCHEDULE_AUTO, B.SCHEDULE_GRID, B.SCHEDULE_BALANCED])
+def test_tc_plan_rule(T, W_, max_splits, schedule):
+    p = plan(args(T, W_, max_splits=max_splits, schedule=schedule))
+    P = expected_clusters(T, W_, max_splits=max_splits, schedule=schedule)
+    assert p["clusters"] == P
+    if P:
+        # balanced mode: equal shares, pieces of cut tokens in the workspace
+        assert p["num_splits"] == 1 and p["grid"] == 2 * P
+        assert P <= GB300_SMS // 2 and (P == GB300_SMS // 2 or P == max(1, T * W_ // 64))
+        assert p["workspace_bytes"] == (workspace(2 * P * 128) if P > 1 else 0)
+        return
     S = p["num_splits"]
     assert S == expected_tc_splits(T, W_, max_splits)
     assert p["grid"] == T * S * 2
@@ -106,9 +155,19 @@ def test_tc_split_rule(T, W_, max_splits):
     if S > math.ceil(W_ / 2304):
         assert T * S <= GB300_SMS // 2                      # extra splits only while one wave holds
     # workspace: BF16 partials + fp32 LSEs, each 256-byte aligned; none for S = 1
-    rows = T * 128 * S
-    want_ws = 0 if S == 1 else (-(-rows * 512 * 2 // 256) * 256 + -(-rows * 4 // 256) * 256)
-    assert p["workspace_bytes"] == want_ws
+    assert p["workspace_bytes"] == (0 if S == 1 else workspace(T * 128 * S))
+
+
+def test_balanced_shares_are_whole_waves_of_one_cluster_per_pair():
+    """Balanced mode uses every SM pair once the columns allow 64 per share,
+    and never more clusters than pairs."""
+    for sms in (16, 132, 148, 152):
+        pairs = sms // 2
+        bal = B.SCHEDULE_BALANCED
+        assert plan(args(min(128, 14 * pairs), 2176, schedule=bal), sms)["clusters"] == pairs
+        assert plan(args(1, 256, schedule=bal), sms)["clusters"] == min(pairs, 4)
+        assert plan(args(14 * pairs + 1, 128, schedule=bal), sms)["clusters"] == 0   # beyond 14 tokens per pair
+        assert plan(args(128, 2176), sms)["clusters"] == 0                           # the default schedule: grid
 
 
 def test_sm_count_scales_the_split():
@@ -139,6 +198,15 @@ def test_bad_sm_count_and_null_plan():
         plan(args(1, 256), sms=0)
     assert e.value.status == B.SMLA_ERR_INVALID_ARG and "sm_count" in str(e.value)
     assert B.lib().smla_plan_decode_for_sm_count(None, 152, None) == B.SMLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value", [("kernel", 4), ("kernel", -1), ("schedule", 3), ("schedule", -1)])
+def test_unknown_kernel_or_schedule_is_an_error(field, value):
+    a = args(8, 640)
+    setattr(a, field, value)
+    with pytest.raises(B.SmlaError) as e:
+        plan(a)
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG and field in str(e.value)
 
 
 def test_shape_errors_match_the_decode_call():
