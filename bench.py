@@ -345,7 +345,7 @@ def run_gpu(args):
     plan = B.smla_plan_decode(args_c, local)
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
-    has_combine = plan.num_splits > 1 or plan.clusters > 1
+    has_combine = plan.num_splits > 1
     launches_per_step = 1 + (1 if has_combine else 0)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -538,7 +538,7 @@ def run_gpu(args):
     roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
     roof["main_kernel_us"] = 1e6 * main_s
     roof["kernels_timed"] = ("decode kernel + combine (programmatic dependent launch)" if has_combine
-                             else "decode kernel")
+                             else "counter memset + decode kernel" if plan.clusters > 1 else "decode kernel")
     roof["roofline_frac_whole_step"] = max(t_hbm, t_tc) / (total_s / (K * 1.0)) if ws_ == 1 else None
 
     if rank != 0:

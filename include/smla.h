@@ -75,8 +75,10 @@ typedef enum smla_dtype {
  * BALANCED (with num_splits == 0 and max_splits == 0, W <= 2304 and T <= 14
  * pairs; else GRID): one pair per two SMs (smla_plan.clusters pairs), pair c
  * taking the c-th of equal shares of the T x W selected columns: whole
- * tokens plus the pieces of the tokens cut at its share's ends, which a
- * second kernel merges.  AUTO is GRID. */
+ * tokens plus the pieces of the tokens cut at its share's ends.  A piece goes
+ * to the workspace with its LSE and counts itself on its token's counter
+ * (the call zeroes the counters with cudaMemsetAsync before the launch); the
+ * token's last piece to finish merges them into the output.  AUTO is GRID. */
 typedef enum smla_schedule {
   SMLA_SCHEDULE_AUTO = 0,
   SMLA_SCHEDULE_GRID = 1,
@@ -190,7 +192,7 @@ typedef struct smla_plan {
   int32_t threads;           /* threads per CTA of the main decode launch */
   int32_t smem_bytes;        /* dynamic shared memory per CTA */
   int32_t clusters;          /* balanced mode: P CTA pairs with equal column shares (grid = 2 P; P > 1 adds a
-                                combine launch); 0: one pair per (token, split) */
+                                memset of the piece counters); 0: one pair per (token, split) */
   size_t workspace_bytes;    /* workspace the call needs (0 without a combine) */
 } smla_plan;
 

@@ -1,5 +1,4 @@
-// Split-K combine: merges S normalised partials of every (token, head); and
-// the merge of the pieces of tokens that the balanced mode cuts.
+// Split-K combine: merges S normalised partials of every (token, head).
 //
 // The partial layout [T, H, S, 512] (BF16) plus [T, H, S] (fp32) base-2 LSEs follows the
 // split partials of the FlashInfer cake_sparse_mla_sm120_dsv4_nvfp4_decode page
@@ -99,51 +98,6 @@ combine_kernel(const DecodeParams p) {
       p.out + th * kHeadDim, p.out_lse ? p.out_lse + th : nullptr);
 }
 
-// Balanced mode: cluster c of P took the columns [g(c), g(c + 1)) of the
-// token-major column space, g(c) = floor(T W c / P).  A token cut by one or
-// more of these boundaries has a head piece (slot 2c + 1 of the cluster where
-// it starts) and one piece per later cluster that covers part of it (slot 2c'
-// of each).  Block (b, four heads) merges the token cut at g(b + 1) if that is
-// the token's first cut; a thread takes 8 dims of one head.
-constexpr int kPieceHeadsPerCta = 4;
-constexpr int kPieceThreadsPerHead = kHeadDim / 8;
-
-template <class I>
-__device__ __forceinline__ bool piece_merge_of(const DecodeParams& p, I clusters, I b, int* t_out, int* n_out) {
-  const I W = (I)p.W, total = (I)p.sum_q * W;
-  const I cut = total * (b + 1) / clusters;
-  if (cut % W == 0) return false;                 // a token edge: nothing cut here
-  const I t = cut / W;
-  if (total * b / clusters > t * W) return false; // an earlier boundary cuts this token
-  I last = b + 1;                                 // the last cluster that covers part of token t
-  while (last + 1 < clusters && total * (last + 1) / clusters < (t + 1) * W) ++last;
-  *t_out = (int)t;
-  *n_out = (int)(last - b + 1);
-  return true;
-}
-
-__global__ void __launch_bounds__(kPieceHeadsPerCta * kPieceThreadsPerHead)
-combine_pieces_kernel(const DecodeParams p, int clusters, const __nv_bfloat16* piece_o, const float* piece_lse) {
-  const int hblocks = (p.H + kPieceHeadsPerCta - 1) / kPieceHeadsPerCta;
-  const int b = blockIdx.x / hblocks;
-  const int h = (blockIdx.x % hblocks) * kPieceHeadsPerCta + threadIdx.x / kPieceThreadsPerHead;
-  const int d = (threadIdx.x % kPieceThreadsPerHead) * 8;
-  if (h >= p.H) return;
-  int t = 0, n = 0;
-  // 32-bit arithmetic where T W P fits (divisions are the cost here)
-  const bool small = (uint64_t)p.sum_q * (uint64_t)p.W * (uint64_t)clusters < (1ull << 32);
-  const bool merge = small ? piece_merge_of<uint32_t>(p, (uint32_t)clusters, (uint32_t)b, &t, &n)
-                           : piece_merge_of<uint64_t>(p, (uint64_t)clusters, (uint64_t)b, &t, &n);
-  if (!merge) return;
-  const int64_t H = p.H;
-  auto slot = [&](int k) -> int64_t { return k == 0 ? 2 * (int64_t)b + 1 : 2 * ((int64_t)b + k); };
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  merge_partials<8>(
-      p, h, n, d, [&](int k) { return __ldg(piece_lse + slot(k) * H + h); },
-      [&](int k) { return reinterpret_cast<const uint4*>(piece_o + (slot(k) * H + h) * kHeadDim + d); },
-      p.out + ((int64_t)t * H + h) * kHeadDim, p.out_lse ? p.out_lse + (int64_t)t * H + h : nullptr);
-}
-
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
@@ -163,23 +117,6 @@ cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, p);
-}
-
-cudaError_t launch_combine_pieces(const DecodeParams& p, int clusters, const __nv_bfloat16* piece_o,
-                                  const float* piece_lse, cudaStream_t stream) {
-  const int64_t grid = (int64_t)(clusters - 1) * ((p.H + kPieceHeadsPerCta - 1) / kPieceHeadsPerCta);
-  if (grid <= 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kPieceHeadsPerCta * kPieceThreadsPerHead);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_pieces_kernel, p, clusters, piece_o, piece_lse);
 }
 
 }  // namespace smla

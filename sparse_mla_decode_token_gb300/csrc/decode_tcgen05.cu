@@ -8,8 +8,10 @@
 //                    shares of the token-major column space (T tokens x W
 //                    columns): whole tokens, plus the piece of a token cut at
 //                    either end of the share.  Whole tokens write the output;
-//                    pieces write normalised partials that a second kernel
-//                    merges.  Every cluster gets the same number of columns,
+//                    a piece writes its normalised partial and LSE, counts
+//                    itself on its token's counter, and the token's last
+//                    piece to finish merges the others with its own fp32 O
+//                    into the output.  Every cluster gets the same number of columns,
 //                    so no SM pair idles through a last, partial wave, and a
 //                    unit's index compaction and first gathers overlap the
 //                    previous unit's last tiles.
@@ -95,10 +97,22 @@ constexpr int kQkWarps = 3;                     // QK issuers: warp kMmaWarp + i
 constexpr int kPvWarp = kMmaWarp + kQkWarps;    // PV issue
 constexpr int kSoftmaxWarp0 = 8;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
+constexpr int kPushWarp0 = kSoftmaxWarp0 + kSoftmaxWarps;   // partial-S exchange, one warp per TMEM lane quadrant
+constexpr int kPushWarps = 4;
+constexpr int kThreads = (kPushWarp0 + kPushWarps) * 32;
+// Registers per thread of each warpgroup after the role split (setmaxnreg):
+// the launch gives every thread kLaunchRegs; the MMA and push warpgroups hand
+// registers back, the two softmax warpgroups take them, the producers keep
+// theirs (their index compaction holds two 18-entry arrays per lane).
+constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;
+constexpr int kRegsProducer = kLaunchRegs;
+constexpr int kRegsMma = 40;
+constexpr int kRegsSoftmax = 128;
+constexpr int kRegsPush = 80;
+static_assert(128 * (kRegsProducer + kRegsMma + kRegsPush) + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
+              "the warpgroups' registers after the split fit in what the launch holds");
 constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
 constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of a unit
-constexpr int kChunksPerProducer = (kMaxChunks + kProducerWarps - 1) / kProducerWarps;
 constexpr int kMaxUnits = SMLA_TC_MAX_UNITS;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
@@ -113,6 +127,8 @@ constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
 constexpr int kExactRefTiles = 8;          // E4M3 P: chains of at most this many tiles follow the exact maximum
 constexpr int kMaxStages = 8;
 static_assert(kPvWarp >= kMmaWarp + kQkWarps && kPvWarp < kSoftmaxWarp0, "warp roles");
+static_assert(kMmaWarp % 4 == 0 && kPvWarp == kMmaWarp + 3, "the QK and PV warps form one warpgroup");
+static_assert(kSoftmaxWarp0 % 4 == 0 && kPushWarp0 % 4 == 0, "warpgroups start at multiples of four warps");
 
 // A unit of work: columns [c0, c1) of token t, and where its result goes.
 struct Unit {
@@ -122,6 +138,11 @@ struct Unit {
   int64_t lse_row;           // partial: offset of head 0's LSE
   int32_t part_hstride;      // partial: elements between consecutive heads' rows
   int32_t lse_hstride;       // partial: entries between consecutive heads' LSEs
+  // balanced mode, a piece of a cut token: the token's pieces are the head
+  // piece of cluster merge_first (slot 2 merge_first + 1) and the continuing
+  // pieces of the next merge_n - 1 clusters (slot 2 c'); the last of them to
+  // finish merges all into the output
+  int32_t merge_first, merge_n;
   // written by the producers once the unit is compacted
   int32_t nswa, nvalid, ntiles, tile0;
   int32_t swa_tail, last_tail;   // slots of the last SWA tile and of the last tile
@@ -142,6 +163,10 @@ struct TcSmall {
   uint64_t lsum_full;                    // both warpgroups' row sums of a unit written (one phase per unit)
   uint64_t unit_pv_done;                 // every PV of a unit done (one phase per unit)
   uint64_t o_free;                       // a unit's O read out (one phase per unit)
+  uint64_t epi_staged[2];                // warpgroup g's rows of the last unit staged in shared memory (single use)
+  uint64_t piece_sync;                   // balanced mode: the softmax warps wrote a piece (one phase per piece)
+  uint64_t piece_dec;                    // balanced mode: whether this piece is its token's last one is known
+  int32_t piece_last;                    // balanced mode: this CTA merges the token's pieces
   uint64_t o_full;                       // every PV done (committed by the PV warp at the end)
   uint64_t qk_done;                      // every QK done (one commit per QK warp at the end)
   float m_end[2][2][128];                // [unit & 1][warpgroup][head]: final reference maximum
@@ -200,14 +225,16 @@ struct TcParams {
   CUtensorMap tm_q;
   DecodeParams p;
   int32_t clusters;            // balanced mode: P shares; 0: grid mode
-  __nv_bfloat16* piece_o;      // balanced mode: [P][2][H][512] BF16 normalised partials of cut tokens
-  float* piece_lse;            // balanced mode: [P][2][H] their base-2 LSEs
+  __nv_bfloat16* piece_o;      // balanced mode: [P][2][H][512] BF16 normalised pieces of cut tokens
+  float* piece_lse;            // balanced mode: [P][2][2 ranks][H] their base-2 LSEs (each CTA writes its own)
+  uint32_t* piece_cnt;         // balanced mode: [P][2 ranks] pieces finished per cut token (zero at launch)
 };
 
 // The units of cluster c; returns their count (at most kMaxUnits, which the
 // planner guarantees).  In balanced mode a piece goes to slot 2c if it
 // continues a token begun by an earlier cluster (c0 > 0), else to slot 2c + 1
-// (the head of a token that later clusters continue).
+// (the head of a token that later clusters continue); cluster c covers the
+// columns [g(c), g(c + 1)) of the token-major column space, g(c) = floor(T W c / P).
 __device__ int make_units(const TcParams& P, int c, Unit* units) {
   const DecodeParams& p = P.p;
   const int H = p.H;
@@ -248,13 +275,137 @@ __device__ int make_units(const TcParams& P, int c, Unit* units) {
       u.partial = 1;
       u.part_row = slot * H * kHeadDim;
       u.part_hstride = kHeadDim;
-      u.lse_row = slot * H;
+      u.lse_row = slot * 2 * H;             // + rank * H
       u.lse_hstride = 1;
+      auto g = [&](int64_t cc) { return total * cc / P.clusters; };
+      int64_t first = c, last = c;          // the clusters holding the token's first and last column
+      while (first > 0 && g(first) > t * W) --first;
+      while (last + 1 < P.clusters && g(last + 1) < (t + 1) * W) ++last;
+      u.merge_first = (int32_t)first;
+      u.merge_n = (int32_t)(last - first + 1);
     }
     units[n++] = u;
   }
   return n;
 }
+
+// Step a2 for unit u, by kNW warps (warp index wi): index columns, token
+// metadata, masks; compaction of [c0, c1) into list u & 1: valid SWA slots
+// first, then valid compressed slots, each in column order; then publishes
+// the unit (its first tile tile0) on unit_ready[u].  sync(i) joins the kNW
+// warps (i = 0: chunk counts written, 1: list written) and returns false
+// after an abort.  List u & 1 was last read by the gathers of unit u - 2,
+// all issued before any warp reaches this compaction.
+template <int kN, int kNW, class Sync>
+__device__ __forceinline__ bool compact_unit(const DecodeParams& p, TcSmall& sm, int32_t* idx_s, int u, int tile0,
+                                         int wi, int lane, uint32_t rank, Sync sync, int& o_nswa, int& o_nvalid) {
+  constexpr int kChunksPerWarp = (kMaxChunks + kNW - 1) / kNW;
+  Unit& U = sm.unit[u];
+  const int t = U.t, c0 = U.c0;
+  int c1 = U.c1;
+  if (c1 - c0 > kMaxCols) {              // the planner prevents this; never write past the list
+    if (p.err && wi == 0 && lane == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
+    c1 = c0 + kMaxCols;
+  }
+  int32_t* list = idx_s + (u & 1) * kMaxCols;
+  const int nchunks = (c1 - c0 + 31) / 32;
+  int32_t rv[kChunksPerWarp];
+  if (p.bt == nullptr) {                 // index form: independent loads, all in flight together
+    const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (wi + q * kNW) * 32 + lane;
+      rv[q] = col < c1 ? __ldg(irow + col) : -1;
+    }
+  } else {                               // page-table form: compressed rows from the page table
+    const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (wi + q * kNW) * 32 + lane;
+      rv[q] = -1;
+      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
+    }
+  }
+  const TokenInfo ti = token_info(p, t);
+  c1 = min(c1, max(c0, ti.n_lim));     // active columns of the unit
+#pragma unroll
+  for (int q = 0; q < kChunksPerWarp; ++q) {
+    const int k = wi + q * kNW;
+    if (k < nchunks) {
+      const int col = c0 + k * 32 + lane;
+      const int idx = rv[q];
+      rv[q] = -1;
+      if (col < c1) {
+        const bool swa = col < kSwaCols;
+        bool valid = idx != -1 && (!swa || col < ti.w_swa);
+        if (valid) {
+          const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+          if (idx < 0 || (int64_t)idx >= nrows) {
+            valid = false;
+            if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+          }
+        }
+        if (valid) rv[q] = idx;
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+      const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
+      if (lane == 0) {
+        sm.chunk_cnt[k] = __popc(ball);
+        sm.chunk_swa[k] = __popc(ball_swa);
+      }
+    }
+  }
+  if (!sync(0)) return false;
+  // every producer warp scans the chunk counts itself (at most 72)
+  int chunk_base[kChunksPerWarp];
+  int nvalid = 0, nswa = 0;
+#pragma unroll
+  for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
+  for (int base0 = 0; base0 < nchunks; base0 += 32) {
+    const int k = base0 + lane;
+    const int v = k < nchunks ? sm.chunk_cnt[k] : 0;
+    int sw = k < nchunks ? sm.chunk_swa[k] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int kq = wi + q * kNW;
+      const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
+      if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = nvalid + excl;
+    }
+    nvalid += __shfl_sync(0xffffffffu, incl, 31);
+    nswa += sw;
+  }
+#pragma unroll
+  for (int q = 0; q < kChunksPerWarp; ++q) {
+    const int k = wi + q * kNW;
+    if (k < nchunks) {
+      const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+      if (rv[q] >= 0) list[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+    }
+  }
+  if (!sync(1)) return false;   // the list is complete; the chunk counts are free
+  if (wi == 0 && lane == 0) {
+    U.nswa = nswa;
+    U.nvalid = nvalid;
+    const int tswa = (nswa + kN - 1) / kN, tcomp = (nvalid - nswa + kN - 1) / kN;
+    U.ntiles = tswa + tcomp;
+    U.tile0 = tile0;
+    U.swa_tail = nswa - (tswa - 1) * kN;
+    U.last_tail = tcomp > 0 ? nvalid - nswa - (tcomp - 1) * kN : U.swa_tail;
+    mbar_arrive(smem_addr(&sm.unit_ready[u]));
+  }
+  o_nswa = nswa;
+  o_nvalid = nvalid;
+  return true;
+}
+
 
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -307,7 +458,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       }
       for (int b = 0; b < kSBufs; ++b) {
         mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2 + kPushWarps);   // read by one softmax warpgroup and the push warps
       }
       for (int u = 0; u < kMaxUnits; ++u) mbar_init(bar(sm.unit_ready[u]), 1);
       mbar_init(bar(sm.prod_counts), kProducerWarps);
@@ -318,6 +469,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
       mbar_init(bar(sm.unit_pv_done), 1);
       mbar_init(bar(sm.o_free), kSoftmaxWarps);
+      mbar_init(bar(sm.piece_sync), kSoftmaxWarps);
+      mbar_init(bar(sm.epi_staged[0]), kSoftmaxWarps / 2);
+      mbar_init(bar(sm.epi_staged[1]), kSoftmaxWarps / 2);
+      mbar_init(bar(sm.piece_dec), 1);
       mbar_init(bar(sm.o_full), 1);
       mbar_init(bar(sm.qk_done), kQkWarps);
       sm.abort_flag = 0;
@@ -325,6 +480,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    __syncthreads();
+    // unit 0's index compaction by every warp, before the roles split
+    if (sm.nunits > 0) {
+      int n0 = 0, v0 = 0;
+      compact_unit<kN, kThreads / 32>(p, sm, idx_s, 0, 0, warp, lane, rank, [](int) { __syncthreads(); return true; },
+                                      n0, v0);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     cluster_sync();
@@ -354,125 +516,19 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     }
     constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
     const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
-    // ---- a2 for unit u: index columns, token metadata, masks; compaction of
-    // [c0, c1) into list u & 1: valid SWA slots first, then valid compressed
-    // slots, each in column order; publishes the unit (its first tile tile0).
-    // List u & 1 was last read by the gathers of unit u - 2, all issued before
-    // every producer warp reached this compaction.
+    // units 1, 2, ... are compacted here (unit 0 in the set-up, by every warp)
     auto compact = [&](int u, int tile0, int& o_nswa, int& o_nvalid) -> bool {
-      Unit& U = sm.unit[u];
-      const int t = U.t, c0 = U.c0;
-      int c1 = U.c1;
-      if (c1 - c0 > kMaxCols) {              // the planner prevents this; never write past the list
-        if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
-        c1 = c0 + kMaxCols;
-      }
-      int32_t* list = idx_s + (u & 1) * kMaxCols;
-      const int nchunks = (c1 - c0 + 31) / 32;
-      int32_t rv[kChunksPerProducer];
-      if (p.bt == nullptr) {                 // index form: independent loads, all in flight together
-        const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
-#pragma unroll
-        for (int q = 0; q < kChunksPerProducer; ++q) {
-          const int col = c0 + (warp + q * kProducerWarps) * 32 + lane;
-          rv[q] = col < c1 ? __ldg(irow + col) : -1;
-        }
-      } else {                               // page-table form: compressed rows from the page table
-        const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
-#pragma unroll
-        for (int q = 0; q < kChunksPerProducer; ++q) {
-          const int col = c0 + (warp + q * kProducerWarps) * 32 + lane;
-          rv[q] = -1;
-          if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
-        }
-      }
-      const TokenInfo ti = token_info(p, t);
-      c1 = min(c1, max(c0, ti.n_lim));     // active columns of the unit
-#pragma unroll
-      for (int q = 0; q < kChunksPerProducer; ++q) {
-        const int k = warp + q * kProducerWarps;
-        if (k < nchunks) {
-          const int col = c0 + k * 32 + lane;
-          const int idx = rv[q];
-          rv[q] = -1;
-          if (col < c1) {
-            const bool swa = col < kSwaCols;
-            bool valid = idx != -1 && (!swa || col < ti.w_swa);
-            if (valid) {
-              const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
-              if (idx < 0 || (int64_t)idx >= nrows) {
-                valid = false;
-                if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
-              }
-            }
-            if (valid) rv[q] = idx;
-          }
-          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-          const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
-          if (lane == 0) {
-            sm.chunk_cnt[k] = __popc(ball);
-            sm.chunk_swa[k] = __popc(ball_swa);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.prod_counts));
-      if (!warp_wait(cx, bar(sm.prod_counts), u & 1)) return false;
-      // every producer warp scans the chunk counts itself (at most 72)
-      int chunk_base[kChunksPerProducer];
-      int nvalid = 0, nswa = 0;
-#pragma unroll
-      for (int q = 0; q < kChunksPerProducer; ++q) chunk_base[q] = 0;
-      for (int base0 = 0; base0 < nchunks; base0 += 32) {
-        const int k = base0 + lane;
-        const int v = k < nchunks ? sm.chunk_cnt[k] : 0;
-        int sw = k < nchunks ? sm.chunk_swa[k] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int w = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += w;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
-#pragma unroll
-        for (int q = 0; q < kChunksPerProducer; ++q) {
-          const int kq = warp + q * kProducerWarps;
-          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
-          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = nvalid + excl;
-        }
-        nvalid += __shfl_sync(0xffffffffu, incl, 31);
-        nswa += sw;
-      }
-#pragma unroll
-      for (int q = 0; q < kChunksPerProducer; ++q) {
-        const int k = warp + q * kProducerWarps;
-        if (k < nchunks) {
-          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-          if (rv[q] >= 0) list[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.prod_list));
-      if (!warp_wait(cx, bar(sm.prod_list), u & 1)) return false;   // the list is complete; the chunk counts are free
-      if (warp == 0 && lane == 0) {
-        U.nswa = nswa;
-        U.nvalid = nvalid;
-        const int tswa = (nswa + kN - 1) / kN, tcomp = (nvalid - nswa + kN - 1) / kN;
-        U.ntiles = tswa + tcomp;
-        U.tile0 = tile0;
-        U.swa_tail = nswa - (tswa - 1) * kN;
-        U.last_tail = tcomp > 0 ? nvalid - nswa - (tcomp - 1) * kN : U.swa_tail;
-        mbar_arrive(bar(sm.unit_ready[u]));
-      }
-      o_nswa = nswa;
-      o_nvalid = nvalid;
-      return true;
+      auto sync = [&](int i) {
+        const uint32_t b = i == 0 ? bar(sm.prod_counts) : bar(sm.prod_list);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b);
+        return warp_wait(cx, b, (u - 1) & 1);
+      };
+      return compact_unit<kN, kProducerWarps>(p, sm, idx_s, u, tile0, warp, lane, rank, sync, o_nswa, o_nvalid);
     };
-
     int next_j = pg;                         // the next tile this group issues (after the loop: past its last one)
-    int nswa = 0, nvalid = 0;                // the current unit's counts
-    bool ok = nunits == 0 || compact(0, 0, nswa, nvalid);
+    int nswa = nunits > 0 ? sm.unit[0].nswa : 0, nvalid = nunits > 0 ? sm.unit[0].nvalid : 0;   // the current unit's counts
+    bool ok = true;
     int tile0 = 0;                           // the current unit's first tile
     for (int u = 0; ok && u < nunits; ++u) {
       const int tswa = (nswa + kN - 1) / kN;
@@ -533,119 +589,124 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // at most one per stage.  Normally the consumers have waited for them.
     for (int jj = max(pg, next_j - C::kStages); jj < next_j; ++jj)
       if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
-  } else if (warp < kMmaWarp + kQkWarps) {
-    // ============================================================ Q load and QK issue
-    // QK and PV are issued by different warps so that a QK never waits behind
-    // a PV (which waits for the softmax): the QK of tile j depends only on its
-    // data, the unit's Q and a free S buffer.  The issuer of the unit's first
-    // tile goes first and the others start once that QK has
-    // completed (on a GB300 a QK issued by a second warp before the first one
-    // finished gave wrong logits for some heads in repeated runs; observed,
-    // cause not identified).
-    constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
-    const int qi = warp - kMmaWarp;
-    const uint32_t qbytes = (uint32_t)(C::kRegions * H * 128);
-    // Q of token tq, loaded by warp kMmaWarp: the first unit's at once (before
-    // its index compaction is done), a later unit's once every QK of the
-    // previous unit that used Q is done.  The first unit counts as using Q
-    // even when it has no tile, so that every load is followed by one wait of
-    // every QK warp and one commit of each (no parity wait can fall two
-    // phases behind or ahead).
-    auto load_q = [&](int tq) {
-      if (qi == 0 && lane == 0) {
-        mbar_arrive_expect_tx(bar(sm.q_full), qbytes);
-        for (int kb = 0; kb < C::kRegions; ++kb)
-          tma_load_3d(q_addr + kb * C::kRegionQ, &P.tm_q, (int)rank * kHalfDims + kb * (128 / C::kElem), 0, tq,
-                      bar(sm.q_full));
-      }
-      __syncwarp();
-    };
-    bool ok = true;
-    int ne = 0;                              // units that used Q so far
-    int nf = 0;                              // units with tiles so far
-    if (nunits > 0) load_q(sm.unit[0].t);
-    for (int u = 0; ok && u < nunits; ++u) {
-      if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
-      const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0, t = sm.unit[u].t;
-      if (ntiles == 0 && u > 0) continue;
-      if (u > 0) {
-        if (qi == 0 && !(ok = warp_wait(cx, bar(sm.qk_unit_done), (ne - 1) & 1))) break;
-        load_q(t);
-      }
-      if (!(ok = warp_wait(cx, bar(sm.q_full), ne & 1))) break;
-      const int first = (qi - tile0 % kSBufs + kSBufs) % kSBufs;   // this warp's first tile of the unit (local index)
-      if (first > 0 && first < ntiles && !(ok = warp_wait(cx, bar(sm.qk_first), nf & 1))) break;
-      for (int k = first; k < ntiles; k += kQkWarps) {
-        const int j = tile0 + k;
-        const int st = j % C::kStages;
-        if (!(ok = warp_wait(cx, bar(sm.kv_full[st]), (j / C::kStages) & 1))) break;
-        const int b = j % kSBufs;
-        if (!(ok = warp_wait(cx, bar(sm.s_empty[b]), ((j / kSBufs) & 1) ^ 1))) break;
-        fence_proxy_async_smem();
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t stage = kv_addr + st * C::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < C::kK1; ++kk) {
-            const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
-            const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
-            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(sm.s_full[b]));
-          if (k == 0) mma_commit(bar(sm.qk_first));
+  } else if (warp < kSoftmaxWarp0) {
+    regs_decrease<kRegsMma>();
+    if (warp < kMmaWarp + kQkWarps) {
+      // ============================================================ Q load and QK issue
+      // QK and PV are issued by different warps so that a QK never waits behind
+      // a PV (which waits for the softmax): the QK of tile j depends only on its
+      // data, the unit's Q and a free S buffer.  The issuer of the unit's first
+      // tile goes first and the others start once that QK has
+      // completed (on a GB300 a QK issued by a second warp before the first one
+      // finished gave wrong logits for some heads in repeated runs; observed,
+      // cause not identified).
+      constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
+      const int qi = warp - kMmaWarp;
+      const uint32_t qbytes = (uint32_t)(C::kRegions * H * 128);
+      // Q of token tq, loaded by warp kMmaWarp: the first unit's at once (before
+      // its index compaction is done), a later unit's once every QK of the
+      // previous unit that used Q is done.  The first unit counts as using Q
+      // even when it has no tile, so that every load is followed by one wait of
+      // every QK warp and one commit of each (no parity wait can fall two
+      // phases behind or ahead).
+      auto load_q = [&](int tq) {
+        if (qi == 0 && lane == 0) {
+          mbar_arrive_expect_tx(bar(sm.q_full), qbytes);
+          for (int kb = 0; kb < C::kRegions; ++kb)
+            tma_load_3d(q_addr + kb * C::kRegionQ, &P.tm_q, (int)rank * kHalfDims + kb * (128 / C::kElem), 0, tq,
+                        bar(sm.q_full));
         }
         __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) mma_commit(bar(sm.qk_unit_done));     // completes once every QK above is done
-      __syncwarp();
-      ++ne;
-      if (ntiles > 0) ++nf;
-    }
-    if (lane == 0) mma_commit(bar(sm.qk_done));
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ============================================================ PV issue
-    constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
-    bool ok = true;
-    for (int u = 0; ok && u < nunits; ++u) {
-      if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
-      // the unit's first PV overwrites O: the previous unit's O must have been
-      // read out (waited for every unit, so that this warp runs at most one
-      // unit ahead of the epilogue)
-      if (u > 0 && !(ok = warp_wait(cx, bar(sm.o_free), (u - 1) & 1))) break;
-      const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0;
-      for (int k = 0; k < ntiles; ++k) {
-        const int j = tile0 + k;
-        const int b = j & 1, st = j % C::kStages;
-        if (!(ok = warp_wait(cx, bar(sm.p_full[b]), (j >> 1) & 1))) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t stage = kv_addr + st * C::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < C::kK2; ++kk) {
-            const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
-            mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
-                             idesc_pv, (k > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(sm.p_empty[b]));
-          mma_commit(bar(sm.kv_empty[st]));
+      };
+      bool ok = true;
+      int ne = 0;                              // units that used Q so far
+      int nf = 0;                              // units with tiles so far
+      if (nunits > 0) load_q(sm.unit[0].t);
+      for (int u = 0; ok && u < nunits; ++u) {
+        if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
+        const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0, t = sm.unit[u].t;
+        if (ntiles == 0 && u > 0) continue;
+        if (u > 0) {
+          if (qi == 0 && !(ok = warp_wait(cx, bar(sm.qk_unit_done), (ne - 1) & 1))) break;
+          load_q(t);
         }
+        if (!(ok = warp_wait(cx, bar(sm.q_full), ne & 1))) break;
+        const int first = (qi - tile0 % kSBufs + kSBufs) % kSBufs;   // this warp's first tile of the unit (local index)
+        if (first > 0 && first < ntiles && !(ok = warp_wait(cx, bar(sm.qk_first), nf & 1))) break;
+        for (int k = first; k < ntiles; k += kQkWarps) {
+          const int j = tile0 + k;
+          const int st = j % C::kStages;
+          if (!(ok = warp_wait(cx, bar(sm.kv_full[st]), (j / C::kStages) & 1))) break;
+          const int b = j % kSBufs;
+          if (!(ok = warp_wait(cx, bar(sm.s_empty[b]), ((j / kSBufs) & 1) ^ 1))) break;
+          fence_proxy_async_smem();
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t stage = kv_addr + st * C::kStageBytes;
+  #pragma unroll
+            for (int kk = 0; kk < C::kK1; ++kk) {
+              const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
+              const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
+              mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(sm.s_full[b]));
+            if (k == 0) mma_commit(bar(sm.qk_first));
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(bar(sm.qk_unit_done));     // completes once every QK above is done
+        __syncwarp();
+        ++ne;
+        if (ntiles > 0) ++nf;
+      }
+      if (lane == 0) mma_commit(bar(sm.qk_done));
+      __syncwarp();
+    } else {
+      // ============================================================ PV issue
+      constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
+      bool ok = true;
+      for (int u = 0; ok && u < nunits; ++u) {
+        if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
+        // the unit's first PV overwrites O: the previous unit's O must have been
+        // read out (waited for every unit, so that this warp runs at most one
+        // unit ahead of the epilogue)
+        if (u > 0 && !(ok = warp_wait(cx, bar(sm.o_free), (u - 1) & 1))) break;
+        const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0;
+        for (int k = 0; k < ntiles; ++k) {
+          const int j = tile0 + k;
+          const int b = j & 1, st = j % C::kStages;
+          if (!(ok = warp_wait(cx, bar(sm.p_full[b]), (j >> 1) & 1))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t stage = kv_addr + st * C::kStageBytes;
+  #pragma unroll
+            for (int kk = 0; kk < C::kK2; ++kk) {
+              const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
+              mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
+                               idesc_pv, (k > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(sm.p_empty[b]));
+            mma_commit(bar(sm.kv_empty[st]));
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(bar(sm.unit_pv_done));     // completes once every PV of the unit is done
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(bar(sm.unit_pv_done));     // completes once every PV of the unit is done
+      if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every PV issued above is done
       __syncwarp();
     }
-    if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every PV issued above is done
-    __syncwarp();
-  } else if (warp >= kSoftmaxWarp0) {
+  } else if (warp < kPushWarp0) {
+    regs_increase<kRegsSoftmax>();
     // ============================================================ softmax / epilogue
     // Two warpgroups take turns: warpgroup g handles tiles j with j % 2 == g
     // (all N slots; S, P and exchange buffer g).  The only hand-off between
     // consecutive tiles of a unit is the running reference maximum m(j),
     // published by the warpgroup of tile j as soon as it is known, so one
-    // warpgroup's exponentials overlap the other's loads and exchange.
+    // warpgroup's exponentials overlap the other's loads.  The push warps
+    // send this CTA's partial S to the peer.
     const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;
@@ -654,11 +715,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
     const uint32_t xbytes = (uint32_t)(H * kN * 3);    // bytes the peer pushes per tile (24-bit logits)
-    constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
-    const uint32_t x_mine = x_addr + g * C::kXBytes;
-    const uint32_t x_peer = map_to_rank(x_mine, peer);
-    const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer) + g * kBarStride;
-    const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[0]), peer) + g * kBarStride;
+    const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[g]), peer);
     const uint32_t p_cols = C::kPCol + g * C::kPCols;  // P buffer g
     // the output scales, loaded now so that their latency hides behind the first tile
     if (active)
@@ -671,41 +728,9 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       tmem_st16(tl + p_cols, zr);
       tmem_wait_st();
     }
-    // send this CTA's partial S of tile jj (a tile of my warpgroup) to the peer
-    auto push = [&](int jj) -> bool {
-      const int sb = jj % kSBufs;
-      if (!warp_wait(cx, bar(sm.s_full[sb]), (jj / kSBufs) & 1)) return false;
-      tc_fence_after();
-      if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[g]), ((jj >> 1) & 1) ^ 1, true)) return false;
-      if (active) {
-        const uint32_t xb = x_peer + (uint32_t)(h * 16);
-#pragma unroll
-        for (int hb = 0; hb < kN / 16; ++hb) {
-          uint32_t v[16];
-          tmem_ld16(tl + kSCol + sb * kN + hb * 16, v);
-          tmem_wait_ld();
-          // 24-bit logits: the low mantissa byte is dropped after rounding;
-          // values a, b, c, d travel as [a1 a2 a3 d1] [b1 b2 b3 d2] [c1 c2 c3 d3]
-          uint32_t w[12];
-#pragma unroll
-          for (int gq = 0; gq < 4; ++gq) {
-            const uint32_t d = v[4 * gq + 3] + 0x80u;
-            w[3 * gq] = __byte_perm(v[4 * gq] + 0x80u, d, 0x5321);
-            w[3 * gq + 1] = __byte_perm(v[4 * gq + 1] + 0x80u, d, 0x6321);
-            w[3 * gq + 2] = __byte_perm(v[4 * gq + 2] + 0x80u, d, 0x7321);
-          }
-#pragma unroll
-          for (int q = 0; q < 3; ++q)
-            st_async_v4(xb + (uint32_t)((hb * 3 + q) * 128 * 16), __uint_as_float(w[4 * q]),
-                        __uint_as_float(w[4 * q + 1]), __uint_as_float(w[4 * q + 2]), __uint_as_float(w[4 * q + 3]),
-                        xin_full_peer);
-        }
-      }
-      return true;
-    };
-
     const uint64_t c2 = f2_pack(c, c);
     bool ok = true;
+    int npiece = 0;                                    // balanced-mode pieces ended so far
     for (int u = 0; u < nunits; ++u) {
       if (ok) ok = warp_wait(cx, bar(sm.unit_ready[u]), 0);
       const Unit& U = sm.unit[u];
@@ -718,10 +743,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       // (the same choice in both CTAs: ntiles is the pair's).
       const float thr = (kFp8 && ntiles <= kExactRefTiles) ? 0.f : kRescaleThreshold;
       const int first = (tile0 & 1) == g ? 0 : 1;        // my first tile of the unit (local index)
-      if (first < ntiles) {
-        if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
-        ok = push(tile0 + first);
-      }
       for (int j = tile0 + first; ok && j < jend; j += 2) {   // j: tile number within the cluster's work
         // slots of tile j: N but for the unit's last SWA tile and its last tile
         // (read from shared memory where needed, which keeps them out of the
@@ -729,7 +750,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         const int n_cur = j == jswa - 1 ? *reinterpret_cast<volatile const int32_t*>(&U.swa_tail)
                         : j == jend - 1 ? *reinterpret_cast<volatile const int32_t*>(&U.last_tail) : kN;
         const int sb = j % kSBufs;
-        // S(j) is final (this warpgroup pushed it): its TMEM load overlaps the wait for the peer's half
+        // the peer's half of S(j) lands here: arm for its bytes (they may come first)
+        if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
+        // this CTA's half: S(j) from TMEM, then the S buffer is free for QK(j + 3)
+        if (!(ok = warp_wait(cx, bar(sm.s_full[sb]), (j / kSBufs) & 1))) break;
+        tc_fence_after();
         float sv[kN];
         if (active) {
 #pragma unroll
@@ -739,12 +764,14 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
           }
+          tmem_wait_ld();
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.s_empty[sb]));
         if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
-        tc_fence_after();
         float mt = -INFINITY;
         if (active) {
-          tmem_wait_ld();
           const uint4* xp = reinterpret_cast<const uint4*>(base + C::kOffX + g * C::kXBytes) + h;
 #pragma unroll
           for (int hb = 0; hb < kN / 16; ++hb) {
@@ -778,13 +805,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           }
           mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
-        if (leader && j + 2 < jend) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(sm.s_empty[sb]));                       // S buffer sb may be overwritten
-          mbar_arrive_cluster_relaxed(xout_free_peer);             // exchange buffer g read out
-        }
+        if (lane == 0) mbar_arrive_cluster_relaxed(xout_free_peer);   // exchange buffer g read out
         // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
         float m_prev = -INFINITY;
         if (j > tile0) {
@@ -795,9 +817,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         sm.m_buf[g][h] = m_cur;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
-        // ---- look ahead: my next tile's partial S to the peer (before this tile's
-        // exponentials, so that the peer has it by the time it gets there)
-        if (j + 2 < jend && !(ok = push(j + 2))) break;
         // ---- P = 2^(x - m(j)); this warpgroup's row sum, rescaled to m(j)
         if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
         tc_fence_after();
@@ -871,6 +890,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         ok = warp_wait(cx, bar(sm.unit_pv_done), u & 1);
         tc_fence_after();
       }
+      float l_keep = 0.f, lse_keep = -INFINITY;          // this unit's row sum and LSE (for a piece merge)
+      // The last unit's rows go out through shared memory (the KV stages are
+      // free once its last PV is done): whole 256-byte row segments per half
+      // warp instead of one 16-byte piece of 32 rows per warp instruction.
+      const bool staged = u == nunits - 1;
+      unsigned char* stg = base + C::kOffKV + g * (128 * 256);
       if (active) {
         float l_tot = 0.f, m_fin = -INFINITY;
         if (ok) {
@@ -907,24 +932,194 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          uint4* o = reinterpret_cast<uint4*>(dst + (int)rank * kHalfDims + col);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        }
-        if (rank == 0 && g == 0) {
-          if (!U.partial) {
-            if (p.out_lse) p.out_lse[(int64_t)U.t * H + h] = lse;
-          } else {
-            (P.clusters ? P.piece_lse : p.part_lse)[U.lse_row + (int64_t)h * U.lse_hstride] = lse;
+          for (int q = 0; q < 4; ++q) {
+            const uint4 x = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            if (staged)   // 16-byte chunks XOR-swizzled by the row against bank conflicts
+              *reinterpret_cast<uint4*>(stg + h * 256 + (((cc * 4 + q) ^ (h & 15)) << 4)) = x;
+            else
+              reinterpret_cast<uint4*>(dst + (int)rank * kHalfDims + col)[q] = x;
           }
+        }
+        if (!U.partial) {
+          if (rank == 0 && g == 0 && p.out_lse) p.out_lse[(int64_t)U.t * H + h] = lse;
+        } else if (P.clusters) {
+          if (g == 0) P.piece_lse[U.lse_row + (int64_t)rank * H + h] = lse;   // each CTA its own copy
+        } else {
+          if (rank == 0 && g == 0) p.part_lse[U.lse_row + (int64_t)h * U.lse_hstride] = lse;
+        }
+        l_keep = l_tot;
+        lse_keep = lse;
+      }
+      if (staged) {
+        // copy-out of this warpgroup's 128 columns: half a warp per row
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.epi_staged[g]));
+        if (ok) ok = warp_wait(cx, bar(sm.epi_staged[g]), 0);
+        if (ok) {
+          __nv_bfloat16* row0 = U.partial ? (P.clusters ? P.piece_o : p.part_o) + U.part_row
+                                          : p.out + (int64_t)U.t * H * kHeadDim;
+          const int64_t rstride = U.partial ? U.part_hstride : kHeadDim;
+          const int ch = lane & 15;
+          for (int r = (warp & 3) * 2 + (lane >> 4); r < H; r += 8) {
+            const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((ch ^ (r & 15)) << 4));
+            *reinterpret_cast<uint4*>(row0 + r * rstride + (int)rank * kHalfDims + g * (kHalfDims / 2) + ch * 8) = x;
+          }
+        }
+      }
+      if (P.clusters && U.partial) {
+        // A piece of a cut token: publish it (device-wide), count it, and if it
+        // is the token's last piece to finish, merge all of them (this CTA's
+        // half of the dims) into the output.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.piece_sync));
+        if (warp == kSoftmaxWarp0) {
+          const bool all = ok && warp_wait(cx, bar(sm.piece_sync), npiece & 1);
+          if (lane == 0) {
+            sm.piece_last = all && atomicAdd(P.piece_cnt + 2 * U.merge_first + rank, 1u) == (uint32_t)(U.merge_n - 1);
+            __threadfence();
+            mbar_arrive(bar(sm.piece_dec));
+          }
+          __syncwarp();
+        }
+        if (ok) ok = warp_wait(cx, bar(sm.piece_dec), npiece & 1);
+        ++npiece;
+        if (ok && *reinterpret_cast<volatile int32_t*>(&sm.piece_last) && active) {
+          __threadfence();
+          const int own = (int)(U.part_row / ((int64_t)H * kHeadDim));   // this piece's slot
+          const int nmerge = U.merge_n, first_c = U.merge_first;
+          auto slot = [&](int k) { return k == 0 ? 2 * first_c + 1 : 2 * (first_c + k); };
+          auto piece_row = [&](int k) {
+            return P.piece_o + ((int64_t)slot(k) * H + h) * kHeadDim + (int)rank * kHalfDims + g * (kHalfDims / 2);
+          };
+          // the other pieces' 256-byte row segments into L1 while their LSEs load
+          for (int k = 0; k < nmerge; ++k)
+            if (slot(k) != own) {
+              prefetch_l1(piece_row(k));
+              prefetch_l1(piece_row(k) + 64);
+            }
+          // weights 2^(LSE_k - max) of every piece, this one from its fp32 O
+          float mx = lse_keep;
+          for (int k = 0; k < nmerge; ++k)
+            if (slot(k) != own) mx = fmaxf(mx, __ldcg(P.piece_lse + ((int64_t)slot(k) * 2 + rank) * H + h));
+          const float w_own = lse_keep == -INFINITY ? 0.f : fast_exp2(lse_keep - mx);
+          float wsum = w_own;
+          for (int k = 0; k < nmerge; ++k) {
+            if (slot(k) == own) continue;
+            const float lk = __ldcg(P.piece_lse + ((int64_t)slot(k) * 2 + rank) * H + h);
+            wsum += lk == -INFINITY ? 0.f : fast_exp2(lk - mx);
+          }
+          const bool have_any = mx != -INFINITY && wsum > 0.f;
+          const float lse_tot = have_any ? mx + fast_log2(wsum) : -INFINITY;
+          const float2 e = sm.epi[g][h];
+          float f = have_any ? e.x / wsum : 0.f;
+          if (p.sinks != nullptr && have_any) f *= 1.f / (1.f + fast_exp2(e.y - lse_tot));
+          const float f_own = l_keep > 0.f ? w_own / l_keep : 0.f;     // O (unnormalised) x this piece's weight
+          __nv_bfloat16* out_row = p.out + ((int64_t)U.t * H + h) * kHeadDim + (int)rank * kHalfDims;
+#pragma unroll 1
+          for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+            const int col = g * (kHalfDims / 2) + cc * 32;
+            float acc[32];
+            {
+              uint32_t r[32];
+              tmem_ld32(tl + kOCol + col, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = f_own != 0.f ? __uint_as_float(r[i]) * f_own : 0.f;
+            }
+            for (int k = 0; k < nmerge; ++k) {
+              if (slot(k) == own) continue;
+              const float lk = __ldcg(P.piece_lse + ((int64_t)slot(k) * 2 + rank) * H + h);
+              if (lk == -INFINITY) continue;                          // an empty piece is all zero
+              const float wk = fast_exp2(lk - mx);
+              const uint4* src = reinterpret_cast<const uint4*>(piece_row(k) + cc * 32);
+              uint4 x[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) x[q] = src[q];                // L1 hits after the prefetch
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t xs[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 fv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[i]));
+                  acc[8 * q + 2 * i] = fmaf(wk, fv.x, acc[8 * q + 2 * i]);
+                  acc[8 * q + 2 * i + 1] = fmaf(wk, fv.y, acc[8 * q + 2 * i + 1]);
+                }
+              }
+            }
+            uint4* o = reinterpret_cast<uint4*>(out_row + col);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              o[q] = make_uint4(pack_bf16x2(acc[8 * q] * f, acc[8 * q + 1] * f), pack_bf16x2(acc[8 * q + 2] * f, acc[8 * q + 3] * f),
+                                pack_bf16x2(acc[8 * q + 4] * f, acc[8 * q + 5] * f), pack_bf16x2(acc[8 * q + 6] * f, acc[8 * q + 7] * f));
+          }
+          if (rank == 0 && g == 0 && p.out_lse) p.out_lse[(int64_t)U.t * H + h] = lse_tot;
         }
       }
       // O read out: the next unit's first PV may overwrite it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(sm.o_free));
+    }
+  } else {
+    regs_decrease<kRegsPush>();
+    // ============================================================ partial-S exchange
+    // Warp kPushWarp0 + q sends lanes [32 q, 32 q + 32) of every tile's S (this
+    // CTA's half of the logits, heads in TMEM lanes) to the peer's exchange
+    // buffer j % 2 with st.async as 24-bit floats (four values in three words),
+    // completing bytes on the peer's mbarrier, once the peer has read the
+    // buffer's previous tile.  Tiles go in order, as soon as their QK is done.
+    const int q4 = warp & 3;
+    const int h = q4 * 32 + lane;
+    const bool active = q4 * 32 < H;                   // warp-uniform
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t x_peer = map_to_rank(x_addr, peer) + (uint32_t)(h * 16);
+    const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer);
+    bool ok = true;
+    for (int u = 0; ok && u < nunits; ++u) {
+      if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
+      const int tile0 = sm.unit[u].tile0, jend = tile0 + sm.unit[u].ntiles;
+      for (int j = tile0; j < jend; ++j) {
+        const int g = j & 1, sb = j % kSBufs;
+        if (!(ok = warp_wait(cx, bar(sm.s_full[sb]), (j / kSBufs) & 1))) break;
+        tc_fence_after();
+        if (j >= 2 && !(ok = warp_wait(cx, bar(sm.xout_free[g]), ((j >> 1) & 1) ^ 1, true))) break;
+        if (active) {
+          const uint32_t xb = x_peer + (uint32_t)(g * C::kXBytes);
+          const uint32_t xbar = xin_full_peer + (uint32_t)(g * sizeof(uint64_t));
+#pragma unroll
+          for (int hh = 0; hh < kN / 32; ++hh) {
+            uint32_t v[32];
+            tmem_ld32(tl + kSCol + sb * kN + hh * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int hb = hh * 2 + half;             // 16-slot block
+              // the low mantissa byte is dropped after rounding; values a, b,
+              // c, d travel as [a1 a2 a3 d1] [b1 b2 b3 d2] [c1 c2 c3 d3]
+              uint32_t w[12];
+#pragma unroll
+              for (int gq = 0; gq < 4; ++gq) {
+                const int i = half * 16 + 4 * gq;
+                const uint32_t d = v[i + 3] + 0x80u;
+                w[3 * gq] = __byte_perm(v[i] + 0x80u, d, 0x5321);
+                w[3 * gq + 1] = __byte_perm(v[i + 1] + 0x80u, d, 0x6321);
+                w[3 * gq + 2] = __byte_perm(v[i + 2] + 0x80u, d, 0x7321);
+              }
+#pragma unroll
+              for (int q = 0; q < 3; ++q)
+                st_async_v4(xb + (uint32_t)((hb * 3 + q) * 128 * 16), __uint_as_float(w[4 * q]),
+                            __uint_as_float(w[4 * q + 1]), __uint_as_float(w[4 * q + 2]),
+                            __uint_as_float(w[4 * q + 3]), xbar);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.s_empty[sb]));   // S buffer sb read
+      }
     }
   }
 
@@ -1002,13 +1197,14 @@ int tc_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemByte
 int tc_threads() { return kThreads; }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, int clusters, __nv_bfloat16* piece_o, float* piece_lse,
-                             cudaStream_t stream) {
+                             uint32_t* piece_cnt, cudaStream_t stream) {
   TcParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
   P.clusters = clusters;
   P.piece_o = piece_o;
   P.piece_lse = piece_lse;
+  P.piece_cnt = piece_cnt;
   // a pool of fewer than N rows holds no run of N rows: its run map is never used
   const int64_t run_rows = p.dtype == SMLA_BF16 ? Cfg<false>::kN : Cfg<true>::kN;
   const int swa_run = (int)std::max<int64_t>(1, std::min(run_rows, p.swa_rows));
@@ -1021,6 +1217,20 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, int clusters, __nv
   if (e != cudaSuccess) return e;
   const int smem = tc_smem_bytes(p.dtype);
   auto launch = [&](auto kernel) -> cudaError_t {
+    // The softmax warpgroups' setmaxnreg.inc waits for registers that the
+    // launch must hold: refuse to launch a build whose per-thread count is
+    // below the one the split was sized for (the wait would never end).
+    static std::atomic<int> launch_regs[2];            // per kernel (BF16, E4M3); 0 = not queried yet
+    std::atomic<int>& cached = launch_regs[p.dtype == SMLA_BF16 ? 0 : 1];
+    int regs = cached.load(std::memory_order_relaxed);
+    if (regs == 0) {
+      cudaFuncAttributes fa;
+      cudaError_t err = cudaFuncGetAttributes(&fa, kernel);
+      if (err != cudaSuccess) return err;
+      regs = fa.numRegs;
+      cached.store(regs, std::memory_order_relaxed);
+    }
+    if (regs < kLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     kernel<<<grid, kThreads, smem, stream>>>(P);

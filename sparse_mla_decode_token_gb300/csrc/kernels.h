@@ -17,14 +17,15 @@ smla_status record_error(smla_status st, const char* msg);
 // units of at most SMLA_TC_MAX_SPLIT_COLS index columns of one token, at most
 // SMLA_TC_MAX_UNITS per cluster.  clusters == 0: one unit per (token, split)
 // (grid = 2 T S); clusters = P > 0: balanced mode, cluster c takes the c-th of
-// P equal shares of the T x W columns (grid = 2 P) and writes the pieces of
-// cut tokens to piece_o [P][2][H][512] / piece_lse [P][2][H].
+// P equal shares of the T x W columns (grid = 2 P); the pieces of cut tokens
+// go through piece_o [P][2][H][512], piece_lse [P][2][2][H] and piece_cnt
+// [P][2] (zero at launch), and the last piece of each token merges them.
 #define SMLA_TC_MAX_SPLIT_COLS 2304
 #define SMLA_TC_MAX_UNITS 16
 int tc_smem_bytes(int dtype);
 int tc_threads();
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, int clusters, __nv_bfloat16* piece_o, float* piece_lse,
-                             cudaStream_t stream);
+                             uint32_t* piece_cnt, cudaStream_t stream);
 
 // tcgen05 decode kernel for E4M3 rows with head-owned softmax
 // (decode_tc_head_owned.cu): a 2-CTA cluster per (token, split), same column limit.
@@ -34,9 +35,5 @@ cudaError_t launch_decode_tc_head_owned(const DecodeParams& p, int grid, cudaStr
 
 // Split-K log-sum-exp combine (combine.cu)
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
-// Merge of the pieces of tokens cut by the balanced mode's share boundaries
-// (combine.cu); clusters = P > 1.
-cudaError_t launch_combine_pieces(const DecodeParams& p, int clusters, const __nv_bfloat16* piece_o,
-                                  const float* piece_lse, cudaStream_t stream);
 
 }  // namespace smla

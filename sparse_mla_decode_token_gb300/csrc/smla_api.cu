@@ -257,9 +257,10 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
       plan->grid = (int32_t)(2 * P);
       if (P > 1) {
         const size_t rows = (size_t)2 * P * a->num_heads;
-        // BF16 normalised pieces, then their fp32 base-2 LSEs
-        plan->workspace_bytes =
-            align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256) + align_up(rows * sizeof(float), 256);
+        // BF16 normalised pieces, their fp32 base-2 LSEs (a copy per CTA of a
+        // pair), then one counter per cut token and CTA
+        plan->workspace_bytes = align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256) +
+                                align_up(2 * rows * sizeof(float), 256) + align_up((size_t)2 * P * sizeof(uint32_t), 256);
       }
       return SMLA_OK;
     }
@@ -414,11 +415,15 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   }
   __nv_bfloat16* piece_o = nullptr;
   float* piece_lse = nullptr;
+  uint32_t* piece_cnt = nullptr;
   if (plan.clusters > 1) {
     const size_t rows = (size_t)2 * plan.clusters * a->num_heads;
-    piece_o = reinterpret_cast<__nv_bfloat16*>(a->workspace);
-    piece_lse = reinterpret_cast<float*>(reinterpret_cast<char*>(a->workspace) +
-                                         align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256));
+    char* w = reinterpret_cast<char*>(a->workspace);
+    piece_o = reinterpret_cast<__nv_bfloat16*>(w);
+    w += align_up(rows * kHeadDim * sizeof(__nv_bfloat16), 256);
+    piece_lse = reinterpret_cast<float*>(w);
+    w += align_up(2 * rows * sizeof(float), 256);
+    piece_cnt = reinterpret_cast<uint32_t*>(w);
   }
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
@@ -426,17 +431,19 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
     ce = cudaEventRecord(reinterpret_cast<cudaEvent_t>(a->profile_event_begin), stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(ce));
   }
+  if (piece_cnt != nullptr) {
+    // the pieces of each cut token count themselves here: zero before the launch
+    ce = cudaMemsetAsync(piece_cnt, 0, (size_t)2 * plan.clusters * sizeof(uint32_t), stream);
+    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(ce));
+  }
   if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     ce = launch_decode_tc_head_owned(p, plan.grid, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05)
-    ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, stream);
+    ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, piece_cnt, stream);
   else
     ce = launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
-  if (plan.clusters > 1) {
-    ce = launch_combine_pieces(p, plan.clusters, piece_o, piece_lse, stream);
-    if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
-  } else if (plan.num_splits > 1) {
+  if (plan.num_splits > 1) {
     ce = launch_combine(p, stream);
     if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(ce));
   }

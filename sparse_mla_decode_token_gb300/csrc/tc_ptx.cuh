@@ -357,6 +357,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 namespace smla {
 namespace ptx {
 
+// Prefetch the 128-byte line holding addr into L1.
+__device__ __forceinline__ void prefetch_l1(const void* addr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(addr));
+}
+
+// Per-thread register limit of the executing warpgroup (all four warps run
+// the same instruction): inc waits until the CTA's pool holds the registers.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // TMA tile load of a 3-D box at (x, y, z) into shared memory at dst (swizzled
 // as the tensor map says); completes its bytes on the mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar) {

@@ -49,11 +49,13 @@ int main(void) {
         p.grid, p.clusters, p.threads, p.smem_bytes);
 
   /* balanced schedule: 76 pairs with equal column shares; pieces of cut
-     tokens in 2 x 76 x 128 BF16 rows of 512 plus their LSEs */
+     tokens in 2 x 76 x 128 BF16 rows of 512, their LSEs (a copy per CTA) and
+     2 x 76 counters */
   a.schedule = SMLA_SCHEDULE_BALANCED;
   st = smla_plan_decode_for_sm_count(&a, 152, &p);
   size_t pieces = (size_t)2 * 76 * 128;
-  size_t want_pieces = (pieces * 512 * 2 + 255) / 256 * 256 + (pieces * 4 + 255) / 256 * 256;
+  size_t want_pieces = (pieces * 512 * 2 + 255) / 256 * 256 + (2 * pieces * 4 + 255) / 256 * 256 +
+                       (2 * 76 * 4 + 255) / 256 * 256;
   CHECK(st == SMLA_OK && p.num_splits == 1 && p.grid == 152 && p.clusters == 76 && p.workspace_bytes == want_pieces,
         "plan 128 tokens, balanced: splits %d grid %d clusters %d workspace %zu", p.num_splits, p.grid, p.clusters,
         p.workspace_bytes);

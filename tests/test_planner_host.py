@@ -7,8 +7,9 @@ Rules (tcgen05 kernel, 2-CTA clusters, 152 SMs = 76 pairs on GB300):
 * balanced mode when the schedule is BALANCED, num_splits and max_splits
   are 0, the kernel is TCGEN05, W <= 2304 and T <= 14 x pairs: P = min(pairs, T W / 64)
   clusters (at least 1) take equal shares of the T x W columns; grid = 2 P,
-  num_splits = 1; with P > 1 the workspace holds 2 P x H BF16 pieces of 512
-  and their fp32 LSEs (each part 256-byte aligned);
+  num_splits = 1; with P > 1 the workspace holds 2 P x H BF16 pieces of
+  512, their fp32 LSEs (one copy per CTA of a pair) and 2 P counters (each
+  part 256-byte aligned);
 * otherwise (and under the default schedule) grid mode, one cluster per
   (token, split): S = floor(pairs / T)
   so that every cluster runs in one wave, at least 1, capped by max_splits
@@ -146,7 +147,9 @@ def test_tc_plan_rule(T, W_, max_splits, schedule):
         # balanced mode: equal shares, pieces of cut tokens in the workspace
         assert p["num_splits"] == 1 and p["grid"] == 2 * P
         assert P <= GB300_SMS // 2 and (P == GB300_SMS // 2 or P == max(1, T * W_ // 64))
-        assert p["workspace_bytes"] == (workspace(2 * P * 128) if P > 1 else 0)
+        rows = 2 * P * 128
+        want = -(-rows * 1024 // 256) * 256 + -(-2 * rows * 4 // 256) * 256 + -(-2 * P * 4 // 256) * 256
+        assert p["workspace_bytes"] == (want if P > 1 else 0)
         return
     S = p["num_splits"]
     assert S == expected_tc_splits(T, W_, max_splits)
