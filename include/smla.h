@@ -78,7 +78,10 @@ typedef enum smla_dtype {
  * tokens plus the pieces of the tokens cut at its share's ends.  A piece goes
  * to the workspace with its LSE and counts itself on its token's counter
  * (the call zeroes the counters with cudaMemsetAsync before the launch); the
- * token's last piece to finish merges them into the output.  AUTO is GRID. */
+ * token's last piece to finish merges them into the output.  BALANCED runs a
+ * separate kernel (several units per CTA pair, a warpgroup for the exchange
+ * of partial logits); on a GB300 it measured slower than GRID for batches of
+ * 38 to 300 tokens except just past a wave (77 tokens), so AUTO is GRID. */
 typedef enum smla_schedule {
   SMLA_SCHEDULE_AUTO = 0,
   SMLA_SCHEDULE_GRID = 1,

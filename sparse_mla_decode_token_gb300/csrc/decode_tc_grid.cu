@@ -1,0 +1,827 @@
+// tcgen05 / TMEM sparse MLA decode kernel for sm_103a, grid schedule.
+//
+// Work unit: one (token, split) runs on a cluster of two CTAs (the balanced
+// schedule's kernel, decode_tcgen05.cu, works through several units per
+// cluster instead).  CTA r of the
+// pair owns output dims [256 r, 256 r + 256): an fp32 accumulator for 128 heads
+// x 512 dims is 256 KB, the whole tensor memory of one SM, so the output is
+// split across the pair.  Per tile of up to N selected slots (N = 64 for E4M3,
+// 32 for BF16):
+//
+//   set-up (all warps)  stage the split's index columns and compact the valid
+//                       slots (per-warp ballots and scans) into a list: SWA
+//                       slots, then compressed slots; tiles are runs of N list
+//                       entries of one pool (masked slots are never loaded)
+//   producer warps 0-3  the pair's half of every selected row (256 dims) with
+//                       TMA tile::gather4 (four rows of 128 bytes per request)
+//                       into a 128-byte-swizzled, UMMA-canonical shared-memory
+//                       tile of a 7-stage (E4M3) or 6-stage (BF16) ring; a
+//                       warp's TMA requests are served one after another, so a
+//                       tile's 32 requests are spread over the two warps of
+//                       one of two groups taking alternate tiles; a tile of N
+//                       consecutive rows is one box copy per 128-byte block
+//   QK warps 4-6        S_r = Q_r K_r^T   (M = 128 heads, N slots, K = 256 dims)
+//                       into one of three TMEM S buffers, warp 4 + b issuing
+//                       the tiles of buffer b; warp 4 also allocates and
+//                       frees TMEM
+//   PV warp 7           O_r += P V_r      (M = 128 heads, N = 256 dims, K = N slots,
+//                       P read from TMEM); a separate issuer so that no QK
+//                       waits behind a PV that waits for the softmax
+//   softmax warps 8-15  two warpgroups taking whole tiles in turn (warpgroup
+//                       g takes tiles j with j % 2 == g), one thread per head:
+//                       read S_r from TMEM, push it to the peer CTA with
+//                       st.async (completing bytes on the peer's mbarrier) as
+//                       24-bit floats (four values in three words), add
+//                       the peer's partial (S = S_0 + S_1; each CTA adds its
+//                       own exact half), settle the running reference maximum m(j) from
+//                       m(j-1) (handed over by the other warpgroup through
+//                       shared memory), exponentials in base 2 with lazy
+//                       rescaling of O, write P (BF16 or E4M3) into TMEM;
+//                       finally normalise O and store it (BF16 output, or BF16
+//                       split partials staged through shared memory) plus the
+//                       LSE.  Each warpgroup pushes its next tile's partial S
+//                       before its exponentials; one warpgroup's exponentials
+//                       overlap the other's loads and exchange.
+//
+// The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
+// (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
+// the normaliser and the split partials follow the cake_sparse_mla_sm120 page
+// (Parameters: out_lse, attn_sink, mid_out / mid_lse).
+//
+// Every mbarrier wait is bounded (2 s); on expiry the CTA raises an abort flag,
+// ORs SMLA_DEVERR_TIMEOUT into the error word, lets every role leave its loop,
+// waits for its own copies and MMAs, frees its TMEM and returns.  No role
+// waits on an unbounded hardware barrier inside its loop.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace smla {
+namespace {
+
+using namespace ptx;
+using namespace tc;
+
+constexpr int kMaxN = 64;            // largest tile (slots per tile)
+constexpr int kHalfDims = 256;       // output dims per CTA
+constexpr int kProducerWarps = 4;    // TMA gathers
+constexpr int kProducerGroups = 2;   // tiles alternate between two groups of two warps that share each tile
+constexpr int kMmaWarp = kProducerWarps;        // first QK issuer; allocates and frees TMEM
+constexpr int kQkWarps = 3;                     // QK issuers: warp kMmaWarp + i issues the tiles k with k % 3 == i
+constexpr int kPvWarp = kMmaWarp + kQkWarps;    // PV issue
+constexpr int kSoftmaxWarp0 = kPvWarp + 1;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = (kSoftmaxWarp0 + kSoftmaxWarps) * 32;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
+constexpr int kMaxChunks = kMaxCols / 32;                 // 32-column chunks of a staged index row
+constexpr int kChunksPerWarp = (kMaxChunks + kWarps - 1) / kWarps;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 0;        // O: 256 fp32 columns
+constexpr uint32_t kSCol = 256;      // S: three buffers of N fp32 columns, then P: two buffers of 16 columns
+constexpr int kSBufs = 3;
+static_assert(kQkWarps == kSBufs, "one QK issuer per S buffer");
+constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 2^8
+constexpr int kExactRefTiles = 8;          // E4M3 P: chains of at most this many tiles follow the exact maximum
+constexpr int kMaxStages = 8;
+
+struct TcSmall {
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
+  uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[2], p_empty[2];
+  uint64_t xin_full[2], xout_free[2];
+  uint64_t m_ready[2];                   // m_buf[g] written by warpgroup g's four warps
+  uint64_t lsum_full;
+  uint64_t o_full;                       // every PV done (committed by the PV warp)
+  uint64_t qk0_done;                     // the CTA's first QK done (single use)
+  uint64_t qk_done;                      // every QK done (one commit per QK warp)
+  float m_end[2][128];                   // final reference maximum per [warpgroup][head]
+  float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
+  float lsum[2][128];                    // [warpgroup][head]
+  int32_t chunk_off[kMaxChunks];        // compacted-slot count of each 32-column chunk, then its offset
+  int32_t nswa;                          // valid slots in the SWA columns of the split
+  int32_t nvalid;                        // valid slots of the split
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
+  static constexpr int kRegions = kHalfDims * kElem / 128;     // 128-byte column blocks per half row
+  static constexpr int kChunks = kHalfDims * kElem / 16;       // 16-byte chunks per half row
+  static constexpr int kStages = kFp8 ? 7 : 6;                 // KV ring (FP8: the smaller exchange buffers make room for a 7th)
+  static constexpr int kKStep = 32 / kElem;                    // MMA K per instruction
+  static constexpr int kK1 = kHalfDims / kKStep;               // QK K steps
+  static constexpr int kK2 = kN / kKStep;                      // PV K steps
+  static constexpr int kPCols = kN * kElem / 4;                // TMEM columns of one P buffer
+  static constexpr uint32_t kPCol = kSCol + kSBufs * kN;
+  static constexpr int kRegionQ = 128 * 128;                   // 128 rows x 128 B
+  static constexpr int kRegionKV = kN * 128;                   // N rows x 128 B
+  static constexpr int kQBytes = kRegions * kRegionQ;
+  static constexpr int kStageBytes = kRegions * kRegionKV;
+  static constexpr int kXBytes = 128 * kN * 3;                 // one exchange buffer: 128 rows of N 24-bit logits
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kQBytes;
+  static constexpr int kOffX = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffIdx = kOffX + 2 * kXBytes;
+  static constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
+  static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
+  static_assert(kStages <= kMaxStages, "barrier arrays");
+  static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
+  static_assert(kN <= kMaxN, "row lists");
+  static_assert(kPCols == 16, "P buffer width");
+  static_assert(kN % 32 == 0, "tiles are whole 32-column groups");
+  static_assert(kPCol + 2 * kPCols <= kTmemCols, "tensor memory budget");
+  static_assert(kStages * kStageBytes >= 2 * 128 * 256, "BF16 partial staging fits in the KV stages");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Kernel parameters: the shared decode parameters plus two TMA descriptors per
+// KV pool ([rows, 512] with the pool's row stride; 128-byte swizzle): box =
+// 128 bytes x 1 row for tile::gather4, and 128 bytes x N rows for whole-tile
+// copies of N consecutive rows.
+struct TcParams {
+  CUtensorMap tm_swa;
+  CUtensorMap tm_comp;
+  CUtensorMap tm_swa_run;
+  CUtensorMap tm_comp_run;
+  DecodeParams p;
+};
+
+// kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
+// epilogue stages the partial rows in shared memory for contiguous stores (a
+// separate instantiation, so that the single-split code is compiled alone).
+template <bool kFp8, bool kPartial>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ TcParams P) {
+  using C = Cfg<kFp8>;
+  const DecodeParams& p = P.p;
+  constexpr int kN = C::kN;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_addr - raw_addr);
+  TcSmall& sm = *reinterpret_cast<TcSmall*>(base + C::kOffSmall);
+  int32_t* idx_s = reinterpret_cast<int32_t*>(base + C::kOffIdx);
+  const uint32_t q_addr = base_addr + C::kOffQ;
+  const uint32_t kv_addr = base_addr + C::kOffKV;
+  const uint32_t x_addr = base_addr + C::kOffX;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t peer = rank ^ 1u;
+  const int S = p.num_splits;
+  const int unit = blockIdx.x >> 1;
+  const int s = unit % S;
+  const int t = unit / S;
+  const int H = p.H;
+  // Column range of this split, from the table width only (so that the index
+  // loads need not wait for any device value): [c0, c0 + ceil(W / S)); in the
+  // page-table form rounded up to whole 64-slot runs, so that every full tile
+  // of compressed slots lies on one page when pages hold a multiple of 64 rows.
+  int per_split = (p.W + S - 1) / S;
+  if (p.bt) per_split = (per_split + kMaxN - 1) / kMaxN * kMaxN;
+  const int c0 = min(p.W, s * per_split);
+  int c1 = min(p.W, c0 + per_split);
+  if (c1 - c0 > kMaxCols) {           // the planner prevents this; never read past the staging buffer
+    if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
+    c1 = c0 + kMaxCols;
+  }
+
+  auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
+
+  // ---------------------------------------------------------------- set-up
+  // Q first: its copies need nothing but (t, rank)
+  {
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
+                              ((int64_t)t * p.q_stride_token + (int64_t)rank * kHalfDims) * C::kElem;
+    for (int c = tid; c < H * C::kChunks; c += kThreads) {
+      const int h = c / C::kChunks, cc = c % C::kChunks;
+      cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7),
+                  qb + (int64_t)h * kHeadDim * C::kElem + cc * 16);
+    }
+  }
+  // the split's index columns, in flight together with the token metadata loads
+  const int nchunks = (c1 - c0 + 31) / 32;
+  const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+  int32_t rv[kChunksPerWarp];
+  if (p.bt == nullptr) {             // index form (a loop of its own: the FP8 code keeps its registers)
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (warp + q * kWarps) * 32 + lane;
+      rv[q] = (col < c1) ? __ldg(irow + col) : -1;
+    }
+  } else {                           // page-table form: compressed rows from the page table
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int col = c0 + (warp + q * kWarps) * 32 + lane;
+      rv[q] = -1;
+      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
+    }
+  }
+  const TokenInfo ti = token_info(p, t);
+  c1 = min(c1, max(c0, ti.n_lim));    // active columns of the split
+  {
+    // zero the KV stages (rows past a tile's slot count then hold finite data)
+    // and the Q rows of absent heads
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
+    const int zn = C::kStages * C::kStageBytes / 16;
+    for (int i = tid; i < zn; i += kThreads) zp[i] = z;
+    if (H < 128) {
+      for (int kb = 0; kb < C::kRegions; ++kb) {
+        uint4* qz = reinterpret_cast<uint4*>(base + C::kOffQ + kb * C::kRegionQ + H * 128);
+        for (int i = tid; i < (128 - H) * 8; i += kThreads) qz[i] = z;
+      }
+    }
+    if (tid == 0) {
+      for (int i = 0; i < C::kStages; ++i) {
+        mbar_init(bar(sm.kv_full[i]), 1);
+        mbar_init(bar(sm.kv_empty[i]), 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+
+        mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
+        mbar_init(bar(sm.p_empty[b]), 1);
+        mbar_init(bar(sm.xin_full[b]), 1);
+        mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps / 2);
+        mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
+      }
+      mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
+      for (int b = 0; b < kSBufs; ++b) {
+        mbar_init(bar(sm.s_full[b]), 1);
+        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+      }
+      mbar_init(bar(sm.o_full), 1);
+      mbar_init(bar(sm.qk0_done), 1);
+      mbar_init(bar(sm.qk_done), kQkWarps);
+      sm.abort_flag = 0;
+      sm.nswa = 0;
+      fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
+    // slots first, then valid compressed slots, each in column order
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int k = warp + q * kWarps;
+      if (k < nchunks) {
+        const int col = c0 + k * 32 + lane;
+        const int idx = rv[q];
+        rv[q] = -1;
+        if (col < c1) {
+          const bool swa = col < kSwaCols;
+          bool ok = idx != -1 && (!swa || col < ti.w_swa);
+          if (ok) {
+            const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+            if (idx < 0 || (int64_t)idx >= nrows) {
+              ok = false;
+              if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+            }
+          }
+          if (ok) rv[q] = idx;
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+        const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
+        if (lane == 0) {
+          sm.chunk_off[k] = __popc(ball);
+          if (ball_swa) atomicAdd(&sm.nswa, __popc(ball_swa));
+        }
+      }
+    }
+    __syncthreads();
+    // every warp scans the chunk counts itself (at most kMaxChunks = 72, three
+    // shuffle scans), which saves a serialised scan and a block barrier
+    int chunk_base[kChunksPerWarp];
+    {
+      int carry = 0;
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
+      for (int base0 = 0; base0 < nchunks; base0 += 32) {
+        const int k = base0 + lane;
+        const int v = k < nchunks ? sm.chunk_off[k] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        // exclusive prefix of this warp's chunks k = warp + q * kWarps in this group of 32
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int kq = warp + q * kWarps;
+          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
+          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (warp == 0 && lane == 0) sm.nvalid = carry;
+    }
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int k = warp + q * kWarps;
+      if (k < nchunks) {
+        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+        if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+      }
+    }
+    if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    // Q is read by the tensor core (async proxy): every thread waits for its
+    // own Q copies and fences them into the async proxy before the barrier,
+    // so no QK can start on a Q row that is not yet visible to it
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+  }
+  const uint32_t tmem = sm.tmem_base;
+  const Ctx cx{&sm.abort_flag, p.err};
+  // tiles: runs of up to N compacted slots of one pool
+  const int nswa = sm.nswa, nvalid = sm.nvalid;
+  const int tswa = (nswa + kN - 1) / kN;
+  const int ntiles = tswa + (nvalid - nswa + kN - 1) / kN;
+  auto tile_start = [&](int j) { return j < tswa ? j * kN : nswa + (j - tswa) * kN; };
+  auto tile_n = [&](int j) { return min(kN, (j < tswa ? nswa : nvalid) - tile_start(j)); };
+
+  if (warp < kProducerWarps) {
+    // ============================================================ producer
+    // A warp's TMA requests are served one after another (about 50 ns per
+    // gather4), so a tile's requests are spread over the three warps of its
+    // group; two groups take alternate tiles (measured: one group of six
+    // sharing every tile reaches ~15 GB/s per SM from HBM, warps owning whole
+    // tiles ~24 GB/s but with a long issue time per tile; two groups of three
+    // were fastest in the full kernel).  A full tile of N consecutive rows (a
+    // page run of the page-table form, or a run in the index table) is one
+    // box copy per 128-byte column block instead.
+    if (tid == 0) {
+      prefetch_tensormap(&P.tm_swa);
+      prefetch_tensormap(&P.tm_comp);
+      prefetch_tensormap(&P.tm_swa_run);
+      prefetch_tensormap(&P.tm_comp_run);
+    }
+    // Producer group pg (kWarpsPerGroup warps) gathers tiles pg, pg + kProducerGroups, ...
+    constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
+    const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
+    int j = pg;                              // after the loop: past the last tile this group issued
+    for (; j < ntiles; j += kProducerGroups) {
+      const int st = j % C::kStages;
+      if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
+      const int start = tile_start(j), n = tile_n(j);
+      const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
+      const uint32_t stage = kv_addr + st * C::kStageBytes;
+      const int32_t* rows = idx_s + start;
+      bool run = false;                      // rows[r] == rows[0] + r for every r < N
+      if (n == kN) {
+        const uint32_t r0 = (uint32_t)rows[0];
+        bool ok = true;
+#pragma unroll
+        for (int r = lane; r < kN; r += 32) ok = ok && (uint32_t)rows[r] == r0 + (uint32_t)r;
+        run = __all_sync(0xffffffffu, ok);
+      }
+      if (run) {
+        // every row of the box was checked against the pool's row count in the set-up
+        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa_run) : static_cast<const void*>(&P.tm_comp_run);
+        if (pw == 0 && lane < C::kRegions)
+          tma_load_2d(stage + lane * C::kRegionKV, tmap, (int)rank * kHalfDims + lane * (128 / C::kElem), rows[0],
+                      bar(sm.kv_full[st]));
+      } else {
+        const void* tmap = j < tswa ? static_cast<const void*>(&P.tm_swa) : static_cast<const void*>(&P.tm_comp);
+        const int groups = (n4 / 4) * C::kRegions;
+        for (int gi = pw + kWarpsPerGroup * lane; gi < groups; gi += kWarpsPerGroup * 32) {
+          const int kb = gi % C::kRegions, r0 = (gi / C::kRegions) * 4;
+          tma_gather4(stage + kb * C::kRegionKV + r0 * 128, tmap, (int)rank * kHalfDims + kb * (128 / C::kElem),
+                      rows[r0], rows[min(r0 + 1, n - 1)], rows[min(r0 + 2, n - 1)], rows[min(r0 + 3, n - 1)],
+                      bar(sm.kv_full[st]));
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // Leave no TMA write of this group in flight, also after an abort: wait
+    // (bounded, not cut short by the abort flag) for the last tiles it issued,
+    // at most one per stage.  Normally the consumers have waited for them.
+    for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
+      if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
+  } else if (warp < kMmaWarp + kQkWarps) {
+    // ============================================================ QK issue
+    // QK and PV are issued by different warps so that a QK never waits behind
+    // a PV (which waits for the softmax): the QK of tile k depends only on its
+    // data and a free S buffer.  A thread's chain of dependent MMAs into one
+    // accumulator is issued about one instruction per 150 ns (measured), so
+    // the tiles' QK chains are spread over three warps, one per S buffer,
+    // whose MMAs the tensor core interleaves.
+    constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
+    const int qi = warp - kMmaWarp;
+    // The other issuers start only once the CTA's first QK has completed:
+    // on a GB300, a QK issued by a second warp before the first one finished
+    // gave wrong logits for some heads in repeated runs (observed, cause
+    // not identified); after that the issuers' chains overlap freely.
+    bool ok = qi == 0 || ntiles <= qi || warp_wait(cx, bar(sm.qk0_done), 0);
+    for (int k = qi; ok && k < ntiles; k += kQkWarps) {
+      const int st = k % C::kStages;
+      if (!warp_wait(cx, bar(sm.kv_full[st]), (k / C::kStages) & 1)) break;
+      const int b = k % kSBufs;
+      if (!warp_wait(cx, bar(sm.s_empty[b]), ((k / kSBufs) & 1) ^ 1)) break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t stage = kv_addr + st * C::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kK1; ++kk) {
+          const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
+          const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
+          mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(sm.s_full[b]));
+        if (k == 0) mma_commit(bar(sm.qk0_done));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(bar(sm.qk_done));   // completes once every QK issued above is done
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ============================================================ PV issue
+    constexpr uint32_t idesc_pv = idesc(kFp8, 128, kHalfDims, true);
+    for (int jj = 0; jj < ntiles; ++jj) {
+      const int b = jj & 1, st = jj % C::kStages;
+      if (!warp_wait(cx, bar(sm.p_full[b]), (jj >> 1) & 1)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t stage = kv_addr + st * C::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kK2; ++kk) {
+          const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
+          mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
+                           idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(sm.p_empty[b]));
+        mma_commit(bar(sm.kv_empty[st]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(bar(sm.o_full));    // completes once every PV issued above is done
+    __syncwarp();
+  } else {
+    // ============================================================ softmax / epilogue
+    // Two warpgroups take turns: warpgroup g handles tiles j with j % 2 == g
+    // (all N slots; S, P and exchange buffer g).  The only hand-off between
+    // consecutive tiles is the running reference maximum m(j), published by
+    // the warpgroup of tile j as soon as it is known, so one warpgroup's
+    // exponentials overlap the other's loads and exchange.
+    const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup
+    const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
+    const int h = q4 * 32 + lane;
+    const bool active = q4 * 32 < H;                   // warp-uniform
+    const bool leader = (warp - kSoftmaxWarp0) % 4 == 0 && lane == 0;   // one thread per warpgroup
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+    const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
+    const uint32_t xbytes = (uint32_t)(H * kN * 3);    // bytes the peer pushes per tile (24-bit logits)
+    constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
+    const uint32_t x_mine = x_addr + g * C::kXBytes;
+    const uint32_t x_peer = map_to_rank(x_mine, peer);
+    const uint32_t xin_full_peer = map_to_rank(bar(sm.xin_full[0]), peer) + g * kBarStride;
+    const uint32_t xout_free_peer = map_to_rank(bar(sm.xout_free[0]), peer) + g * kBarStride;
+    const uint32_t p_cols = C::kPCol + g * C::kPCols;  // P buffer g
+    if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);
+    if (!active) {
+      // rows of absent heads: P = 0, so O stays 0 there
+      uint32_t zr[C::kPCols];
+#pragma unroll
+      for (int i = 0; i < C::kPCols; ++i) zr[i] = 0u;
+      tmem_st16(tl + p_cols, zr);
+      tmem_wait_st();
+    }
+    // send this CTA's partial S of tile jj (a tile of my warpgroup) to the peer
+    auto push = [&](int jj) -> bool {
+      const int sb = jj % kSBufs;
+      if (!warp_wait(cx, bar(sm.s_full[sb]), (jj / kSBufs) & 1)) return false;
+      tc_fence_after();
+      if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[g]), ((jj >> 1) & 1) ^ 1, true)) return false;
+      if (active) {
+        const uint32_t xb = x_peer + (uint32_t)(h * 16);
+#pragma unroll
+        for (int hb = 0; hb < kN / 16; ++hb) {
+          uint32_t v[16];
+          tmem_ld16(tl + kSCol + sb * kN + hb * 16, v);
+          tmem_wait_ld();
+          // 24-bit logits: the low mantissa byte is dropped after rounding;
+          // values a, b, c, d travel as [a1 a2 a3 d1] [b1 b2 b3 d2] [c1 c2 c3 d3]
+          uint32_t w[12];
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint32_t d = v[4 * gq + 3] + 0x80u;
+            w[3 * gq] = __byte_perm(v[4 * gq] + 0x80u, d, 0x5321);
+            w[3 * gq + 1] = __byte_perm(v[4 * gq + 1] + 0x80u, d, 0x6321);
+            w[3 * gq + 2] = __byte_perm(v[4 * gq + 2] + 0x80u, d, 0x7321);
+          }
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            st_async_v4(xb + (uint32_t)((hb * 3 + q) * 128 * 16), __uint_as_float(w[4 * q]),
+                        __uint_as_float(w[4 * q + 1]), __uint_as_float(w[4 * q + 2]), __uint_as_float(w[4 * q + 3]),
+                        xin_full_peer);
+        }
+      }
+      return true;
+    };
+
+    float m_last = -INFINITY, l_run = 0.f;            // reference and row sum of my warpgroup's tiles
+    // E4M3 P keeps 3 mantissa bits: under a lagging reference a row's largest P
+    // (up to 2^8) is rounded by up to 1/16, which shows when few slots carry the
+    // mass, so short tile chains move the reference on every new maximum (the
+    // same choice in both CTAs: ntiles is the pair's).
+    const float thr = (kFp8 && ntiles <= kExactRefTiles) ? 0.f : kRescaleThreshold;
+    bool ok = true;
+    if (g < ntiles) ok = push(g);
+    int j = g;
+    const uint64_t c2 = f2_pack(c, c);
+    for (; ok && j < ntiles; j += 2) {
+      const int n_cur = tile_n(j);
+      const int sb = j % kSBufs;
+      // S(j) is final (this warpgroup pushed it): its TMEM load overlaps the wait for the peer's half
+      float sv[kN];
+      if (active) {
+#pragma unroll
+        for (int hb = 0; hb < kN / 32; ++hb) {
+          uint32_t r[32];
+          tmem_ld32(tl + kSCol + sb * kN + hb * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
+        }
+      }
+      if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
+      tc_fence_after();
+      float mt = -INFINITY;
+      if (active) {
+        tmem_wait_ld();
+        const uint4* xp = reinterpret_cast<const uint4*>(base + C::kOffX + g * C::kXBytes) + h;
+#pragma unroll
+        for (int hb = 0; hb < kN / 16; ++hb) {
+          uint32_t w[12];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const uint4 x = xp[(hb * 3 + q) * 128];
+            w[4 * q] = x.x;
+            w[4 * q + 1] = x.y;
+            w[4 * q + 2] = x.z;
+            w[4 * q + 3] = x.w;
+          }
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint32_t w0 = w[3 * gq], w1 = w[3 * gq + 1], w2 = w[3 * gq + 2];
+            const float pa = __uint_as_float(w0 << 8), pb = __uint_as_float(w1 << 8), pc = __uint_as_float(w2 << 8);
+            const float pd = __uint_as_float(__byte_perm(__byte_perm(w0, w1, 0x7373), w2, 0x7103));
+            const int i = hb * 16 + 4 * gq;
+            f2_unpack(f2_mul(f2_add(f2_pack(sv[i], sv[i + 1]), f2_pack(pa, pb)), c2), sv[i], sv[i + 1]);
+            f2_unpack(f2_mul(f2_add(f2_pack(sv[i + 2], sv[i + 3]), f2_pack(pc, pd)), c2), sv[i + 2], sv[i + 3]);
+          }
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (n_cur >= kN) {
+#pragma unroll
+          for (int i = 0; i < kN; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if (i < n_cur) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        }
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
+      if (leader) mbar_arrive_expect_tx(bar(sm.xin_full[g]), xbytes);   // for tile j + 2
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(sm.s_empty[sb]));                         // S buffer sb may be overwritten
+        mbar_arrive_cluster_relaxed(xout_free_peer);               // exchange buffer g read out
+      }
+      // ---- reference maximum: m(j) = mt if it exceeds m(j-1) by the threshold, else m(j-1)
+      float m_prev = -INFINITY;
+      if (j > 0) {
+        if (!(ok = warp_wait(cx, bar(sm.m_ready[g ^ 1]), ((j - 1) >> 1) & 1))) break;
+        m_prev = sm.m_buf[g ^ 1][h];
+      }
+      const float m_cur = (mt > m_prev + thr) ? mt : m_prev;
+      sm.m_buf[g][h] = m_cur;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.m_ready[g]));
+      // ---- look ahead: my next tile's partial S to the peer (before this tile's
+      // exponentials, so that the peer has it by the time it gets there)
+      if (j + 2 < ntiles && !(ok = push(j + 2))) break;
+      // ---- P = 2^(x - m(j)); this warpgroup's row sum, rescaled to m(j)
+      if (!(ok = warp_wait(cx, bar(sm.p_empty[g]), ((j >> 1) & 1) ^ 1))) break;   // PV(j - 2) done
+      tc_fence_after();
+      if (active) {
+        l_run *= (m_last == -INFINITY) ? 0.f : fast_exp2(m_last - m_cur);
+        m_last = m_cur;
+        const uint64_t nm2 = f2_pack(-m_cur, -m_cur);
+#pragma unroll
+        for (int i = 0; i < kN; i += 2) {
+          float x0, x1;
+          f2_unpack(f2_add(f2_pack(sv[i], sv[i + 1]), nm2), x0, x1);
+          sv[i] = fast_exp2(x0);
+          sv[i + 1] = fast_exp2(x1);
+        }
+        if (n_cur < kN) {
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if (i >= n_cur) sv[i] = 0.f;
+        }
+        uint64_t s4[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < kN; i += 2) s4[(i >> 1) & 1] = f2_add(s4[(i >> 1) & 1], f2_pack(sv[i], sv[i + 1]));
+        float s0, s1, s2, s3;
+        f2_unpack(s4[0], s0, s1);
+        f2_unpack(s4[1], s2, s3);
+        l_run += (s0 + s1) + (s2 + s3);
+        uint32_t pr[C::kPCols];
+        if constexpr (kFp8) {
+#pragma unroll
+          for (int i = 0; i < C::kPCols; ++i)
+            pr[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i], sv[4 * i + 1]), __NV_SATFINITE, __NV_E4M3) |
+                    ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(sv[4 * i + 2], sv[4 * i + 3]), __NV_SATFINITE, __NV_E4M3) << 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+        }
+        tmem_st16(tl + p_cols, pr);
+      }
+      // ---- O rescale when the reference moved (O holds tiles < j at m(j-1))
+      const bool rescale = active && j > 0 && m_cur != m_prev;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!(ok = warp_wait(cx, bar(sm.p_empty[g ^ 1]), ((j - 1) >> 1) & 1))) break;
+        tc_fence_after();
+        const float alpha = rescale ? fast_exp2(m_prev - m_cur) : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalfDims / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(tl + kOCol + cc * 16, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st16(tl + kOCol + cc * 16, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sm.p_full[g]));
+    }
+    // total row sum: both warpgroups' sums brought to the final reference
+    if (active) {
+      sm.lsum[g][h] = l_run;
+      sm.m_end[g][h] = m_last;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(sm.lsum_full));
+    if (ok) ok = warp_wait(cx, bar(sm.lsum_full), 0);
+    if (ok && ntiles > 0) {
+      ok = warp_wait(cx, bar(sm.o_full), 0);
+      tc_fence_after();
+    }
+    if (active) {
+      float l_tot = 0.f, m_fin = -INFINITY;
+      if (ok) {
+        const float ma = sm.m_end[0][h], mb = sm.m_end[1][h];
+        m_fin = fmaxf(ma, mb);
+        if (m_fin != -INFINITY) {
+          if (ma != -INFINITY) l_tot += sm.lsum[0][h] * fast_exp2(ma - m_fin);
+          if (mb != -INFINITY) l_tot += sm.lsum[1][h] * fast_exp2(mb - m_fin);
+        }
+      }
+      const bool have = ok && ntiles > 0 && l_tot > 0.f;
+      const float lse = have ? m_fin + fast_log2(l_tot) : -INFINITY;
+      float f = have ? 1.f / l_tot : 0.f;
+      if (S == 1) {
+        f *= load_scale(p.bmm2, p.bmm2_dev);
+        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
+      }
+      const int64_t row_th = (int64_t)t * H + h;
+      if constexpr (!kPartial) {
+#pragma unroll 1
+      for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+        const int col = g * (kHalfDims / 2) + cc * 32;
+        float v[32];
+        if (have) {
+          uint32_t r[32];
+          tmem_ld32(tl + kOCol + col, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        const int d0 = (int)rank * kHalfDims + col;
+        uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      }
+      if (rank == 0 && g == 0) {
+        if (S == 1) {
+          if (p.out_lse) p.out_lse[row_th] = lse;
+        } else {
+          p.part_lse[row_th * S + s] = lse;
+        }
+      }
+      } else {
+        // BF16 partial rows go through shared memory (the KV stages are free
+        // once every PV is done), so that the global stores below are whole
+        // 256-byte row segments rather than one 16-byte piece per row per warp
+        // instruction.  Warpgroup g stages its 128 columns; 16-byte chunks are
+        // XOR-swizzled by the row to spread banks.
+        unsigned char* row = base + C::kOffKV + g * (128 * 256) + h * 256;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+          const int col = g * (kHalfDims / 2) + cc * 32;
+          float v[32];
+          if (have) {
+            uint32_t r[32];
+            tmem_ld32(tl + kOCol + col, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        }
+        if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
+      }
+    }
+    // copy-out of this warpgroup's staged partial columns, 256 contiguous bytes
+    // per row (half a warp per row)
+    if constexpr (kPartial) {
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(128) : "memory");
+      const unsigned char* stg = base + C::kOffKV + g * (128 * 256);
+      const int w4 = (warp - kSoftmaxWarp0) & 3;
+      const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
+      const int c = lane & 15;
+      for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
+        const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((c ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + c * 8) = x;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    // no MMA may still use TMEM (bounded, and not cut short by the abort flag)
+    drain_wait(bar(sm.qk_done), 0);
+    drain_wait(bar(sm.o_full), 0);
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  tc_fence_before();
+  cluster_sync();                          // the peer is done with this CTA's shared memory
+}
+
+}  // namespace
+
+int tc_grid_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes; }
+int tc_grid_threads() { return kThreads; }
+
+cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t stream) {
+  TcParams P;
+  memset(&P, 0, sizeof(P));
+  P.p = p;
+  // a pool of fewer than N rows holds no run of N rows: its run map is never used
+  const int64_t run_rows = p.dtype == SMLA_BF16 ? Cfg<false>::kN : Cfg<true>::kN;
+  const int swa_run = (int)std::max<int64_t>(1, std::min(run_rows, p.swa_rows));
+  const int comp_run = (int)std::max<int64_t>(1, std::min(run_rows, p.comp_rows));
+  cudaError_t e = encode_pool_map(&P.tm_swa, p.swa, p.swa_rows, p.swa_stride, p.dtype, 1);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp, p.comp, p.comp_rows, p.comp_stride, p.dtype, 1);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_swa_run, p.swa, p.swa_rows, p.swa_stride, p.dtype, swa_run);
+  if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp_run, p.comp, p.comp_rows, p.comp_stride, p.dtype, comp_run);
+  if (e != cudaSuccess) return e;
+  const int smem = tc_grid_smem_bytes(p.dtype);
+  auto launch = [&](auto kernel) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, stream>>>(P);
+    return cudaSuccess;
+  };
+  const bool partial = p.num_splits > 1;
+  if (p.dtype == SMLA_BF16)
+    e = partial ? launch(decode_tc_kernel<false, true>) : launch(decode_tc_kernel<false, false>);
+  else
+    e = partial ? launch(decode_tc_kernel<true, true>) : launch(decode_tc_kernel<true, false>);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace smla

@@ -107,8 +107,8 @@ constexpr int kThreads = (kPushWarp0 + kPushWarps) * 32;
 constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;
 constexpr int kRegsProducer = kLaunchRegs;
 constexpr int kRegsMma = 40;
-constexpr int kRegsSoftmax = 128;
-constexpr int kRegsPush = 80;
+constexpr int kRegsSoftmax = 136;
+constexpr int kRegsPush = 64;
 static_assert(128 * (kRegsProducer + kRegsMma + kRegsPush) + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
               "the warpgroups' registers after the split fit in what the launch holds");
 constexpr int kMaxCols = SMLA_TC_MAX_SPLIT_COLS;
@@ -431,9 +431,18 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
 
   // ---------------------------------------------------------------- set-up
+  int nswa0 = 0, nvalid0 = 0;               // unit 0's counts (every thread of the set-up's compaction has them)
   {
+    if (tid == 0) {
+      prefetch_tensormap(&P.tm_q);
+      prefetch_tensormap(&P.tm_swa);
+      prefetch_tensormap(&P.tm_comp);
+      prefetch_tensormap(&P.tm_swa_run);
+      prefetch_tensormap(&P.tm_comp_run);
+    }
     // zero the KV stages (rows past a tile's slot count then hold finite
-    // data) and the Q rows of absent heads (the Q box loads only H rows)
+    // data) and the Q rows of absent heads (the Q box loads only H rows);
+    // each thread orders its stores before later TMA writes to the same bytes
     const uint4 z = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
     const int zn = C::kStages * C::kStageBytes / 16;
@@ -444,7 +453,19 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         for (int i = tid; i < (128 - H) * 8; i += kThreads) qz[i] = z;
       }
     }
+    fence_proxy_async_smem();
     if (tid == 0) {
+      // the first unit's Q first: its load needs only the unit's token
+      mbar_init(bar(sm.q_full), 1);
+      fence_mbar_init_cluster();
+      fence_proxy_async_smem();
+      sm.nunits = make_units(P, blockIdx.x >> 1, sm.unit);
+      if (sm.nunits > 0) {
+        mbar_arrive_expect_tx(bar(sm.q_full), (uint32_t)(C::kRegions * H * 128));
+        for (int kb = 0; kb < C::kRegions; ++kb)
+          tma_load_3d(q_addr + kb * C::kRegionQ, &P.tm_q, (int)rank * kHalfDims + kb * (128 / C::kElem), 0,
+                      sm.unit[0].t, bar(sm.q_full));
+      }
       for (int i = 0; i < C::kStages; ++i) {
         mbar_init(bar(sm.kv_full[i]), 1);
         mbar_init(bar(sm.kv_empty[i]), 1);
@@ -463,7 +484,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       for (int u = 0; u < kMaxUnits; ++u) mbar_init(bar(sm.unit_ready[u]), 1);
       mbar_init(bar(sm.prod_counts), kProducerWarps);
       mbar_init(bar(sm.prod_list), kProducerWarps);
-      mbar_init(bar(sm.q_full), 1);
       mbar_init(bar(sm.qk_first), 1);
       mbar_init(bar(sm.qk_unit_done), kQkWarps);
       mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
@@ -476,21 +496,24 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       mbar_init(bar(sm.o_full), 1);
       mbar_init(bar(sm.qk_done), kQkWarps);
       sm.abort_flag = 0;
-      sm.nunits = make_units(P, blockIdx.x >> 1, sm.unit);
       fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
     __syncthreads();
     // unit 0's index compaction by every warp, before the roles split
-    if (sm.nunits > 0) {
-      int n0 = 0, v0 = 0;
+    if (sm.nunits > 0)
       compact_unit<kN, kThreads / 32>(p, sm, idx_s, 0, 0, warp, lane, rank, [](int) { __syncthreads(); return true; },
-                                      n0, v0);
-    }
+                                      nswa0, nvalid0);
+    // The producers start gathering at once: their TMA writes and barriers
+    // are this CTA's own, ordered after the set-up by the compaction's block
+    // barriers.  Every other warp waits for the pair.
     fence_proxy_async_smem();
     tc_fence_before();
-    cluster_sync();
-    tc_fence_after();
+    cluster_arrive();
+    if (warp >= kProducerWarps) {
+      cluster_wait();
+      tc_fence_after();
+    }
   }
   const uint32_t tmem = sm.tmem_base;
   const Ctx cx{&sm.abort_flag, p.err};
@@ -508,12 +531,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // group; two groups take alternate tiles.  A full tile of N consecutive
     // rows (a page run of the page-table form, or a run in the index table) is
     // one box copy per 128-byte column block instead.
-    if (tid == 0) {
-      prefetch_tensormap(&P.tm_swa);
-      prefetch_tensormap(&P.tm_comp);
-      prefetch_tensormap(&P.tm_swa_run);
-      prefetch_tensormap(&P.tm_comp_run);
-    }
     constexpr int kWarpsPerGroup = kProducerWarps / kProducerGroups;
     const int pg = warp / kWarpsPerGroup, pw = warp % kWarpsPerGroup;
     // units 1, 2, ... are compacted here (unit 0 in the set-up, by every warp)
@@ -527,7 +544,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       return compact_unit<kN, kProducerWarps>(p, sm, idx_s, u, tile0, warp, lane, rank, sync, o_nswa, o_nvalid);
     };
     int next_j = pg;                         // the next tile this group issues (after the loop: past its last one)
-    int nswa = nunits > 0 ? sm.unit[0].nswa : 0, nvalid = nunits > 0 ? sm.unit[0].nvalid : 0;   // the current unit's counts
+    int nswa = nswa0, nvalid = nvalid0;      // the current unit's counts
     bool ok = true;
     int tile0 = 0;                           // the current unit's first tile
     for (int u = 0; ok && u < nunits; ++u) {
@@ -589,6 +606,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // at most one per stage.  Normally the consumers have waited for them.
     for (int jj = max(pg, next_j - C::kStages); jj < next_j; ++jj)
       if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
+    cluster_wait();                        // the set-up's cluster barrier (arrived at the end of the set-up)
   } else if (warp < kSoftmaxWarp0) {
     regs_decrease<kRegsMma>();
     if (warp < kMmaWarp + kQkWarps) {
@@ -603,12 +621,11 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       constexpr uint32_t idesc_qk = idesc(kFp8, 128, kN, false);
       const int qi = warp - kMmaWarp;
       const uint32_t qbytes = (uint32_t)(C::kRegions * H * 128);
-      // Q of token tq, loaded by warp kMmaWarp: the first unit's at once (before
-      // its index compaction is done), a later unit's once every QK of the
-      // previous unit that used Q is done.  The first unit counts as using Q
-      // even when it has no tile, so that every load is followed by one wait of
-      // every QK warp and one commit of each (no parity wait can fall two
-      // phases behind or ahead).
+      // Q of token tq: the first unit's is loaded at the start of the set-up, a
+      // later unit's by warp kMmaWarp once every QK of the previous unit that
+      // used Q is done.  The first unit counts as using Q even when it has no
+      // tile, so that every load is followed by one wait of every QK warp and
+      // one commit of each (no parity wait can fall two phases behind or ahead).
       auto load_q = [&](int tq) {
         if (qi == 0 && lane == 0) {
           mbar_arrive_expect_tx(bar(sm.q_full), qbytes);
@@ -621,7 +638,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       bool ok = true;
       int ne = 0;                              // units that used Q so far
       int nf = 0;                              // units with tiles so far
-      if (nunits > 0) load_q(sm.unit[0].t);
       for (int u = 0; ok && u < nunits; ++u) {
         if (!(ok = warp_wait(cx, bar(sm.unit_ready[u]), 0))) break;
         const int ntiles = sm.unit[u].ntiles, tile0 = sm.unit[u].tile0, t = sm.unit[u].t;

@@ -13,7 +13,13 @@ cudaError_t launch_decode_cuda_core(const DecodeParams& p, int grid, cudaStream_
 // Sets the text smla_last_error() returns on this thread; returns st (smla_api.cu).
 smla_status record_error(smla_status st, const char* msg);
 
-// tcgen05 decode kernel (decode_tcgen05.cu): 2-CTA clusters working through
+// tcgen05 decode kernel, grid schedule (decode_tc_grid.cu): a 2-CTA cluster
+// per (token, split) of at most SMLA_TC_MAX_SPLIT_COLS columns.
+int tc_grid_smem_bytes(int dtype);
+int tc_grid_threads();
+cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t stream);
+
+// tcgen05 decode kernel, balanced schedule (decode_tcgen05.cu): 2-CTA clusters working through
 // units of at most SMLA_TC_MAX_SPLIT_COLS index columns of one token, at most
 // SMLA_TC_MAX_UNITS per cluster.  clusters == 0: one unit per (token, split)
 // (grid = 2 T S); clusters = P > 0: balanced mode, cluster c takes the c-th of

@@ -230,8 +230,8 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
     plan->kernel = head_owned ? SMLA_KERNEL_TCGEN05_HEAD_OWNED : SMLA_KERNEL_TCGEN05;
     plan->ctas_per_split = 2;
-    plan->threads = head_owned ? tc_head_owned_threads() : tc_threads();
-    plan->smem_bytes = head_owned ? tc_head_owned_smem_bytes() : tc_smem_bytes(a->dtype);
+    plan->threads = head_owned ? tc_head_owned_threads() : tc_grid_threads();
+    plan->smem_bytes = head_owned ? tc_head_owned_smem_bytes() : tc_grid_smem_bytes(a->dtype);
     const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
     if (s_min > SMLA_MAX_SPLITS)
       return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
@@ -255,6 +255,8 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
       plan->num_splits = 1;
       plan->clusters = (int32_t)P;
       plan->grid = (int32_t)(2 * P);
+      plan->threads = tc_threads();
+      plan->smem_bytes = tc_smem_bytes(a->dtype);
       if (P > 1) {
         const size_t rows = (size_t)2 * P * a->num_heads;
         // BF16 normalised pieces, their fp32 base-2 LSEs (a copy per CTA of a
@@ -438,8 +440,10 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   }
   if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     ce = launch_decode_tc_head_owned(p, plan.grid, stream);
-  else if (plan.kernel == SMLA_KERNEL_TCGEN05)
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05 && plan.clusters > 0)
     ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, piece_cnt, stream);
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05)
+    ce = launch_decode_tc_grid(p, plan.grid, stream);
   else
     ce = launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
