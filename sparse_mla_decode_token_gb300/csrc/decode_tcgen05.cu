@@ -504,16 +504,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     if (sm.nunits > 0)
       compact_unit<kN, kThreads / 32>(p, sm, idx_s, 0, 0, warp, lane, rank, [](int) { __syncthreads(); return true; },
                                       nswa0, nvalid0);
-    // The producers start gathering at once: their TMA writes and barriers
-    // are this CTA's own, ordered after the set-up by the compaction's block
-    // barriers.  Every other warp waits for the pair.
     fence_proxy_async_smem();
     tc_fence_before();
-    cluster_arrive();
-    if (warp >= kProducerWarps) {
-      cluster_wait();
-      tc_fence_after();
-    }
+    cluster_sync();
+    tc_fence_after();
   }
   const uint32_t tmem = sm.tmem_base;
   const Ctx cx{&sm.abort_flag, p.err};
@@ -606,7 +600,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // at most one per stage.  Normally the consumers have waited for them.
     for (int jj = max(pg, next_j - C::kStages); jj < next_j; ++jj)
       if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
-    cluster_wait();                        // the set-up's cluster barrier (arrived at the end of the set-up)
   } else if (warp < kSoftmaxWarp0) {
     regs_decrease<kRegsMma>();
     if (warp < kMmaWarp + kQkWarps) {
