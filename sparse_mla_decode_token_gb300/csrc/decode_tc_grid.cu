@@ -2,10 +2,9 @@
 //
 // Work unit: one (token, split) runs on a cluster of two CTAs (the balanced
 // schedule's kernel, decode_tcgen05.cu, works through several units per
-// cluster instead).  CTA r of the
-// pair owns output dims [256 r, 256 r + 256): an fp32 accumulator for 128 heads
-// x 512 dims is 256 KB, the whole tensor memory of one SM, so the output is
-// split across the pair.  Per tile of up to N selected slots (N = 64 for E4M3,
+// cluster instead).  CTA r of the pair owns output dims [256 r, 256 r + 256):
+// an fp32 accumulator for 128 heads x 512 dims is 256 KB, the whole tensor
+// memory of one SM, so the output is split across the pair.  Per tile of up to N selected slots (N = 64 for E4M3,
 // 32 for BF16):
 //
 //   set-up (all warps)  stage the split's index columns and compact the valid
