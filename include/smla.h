@@ -63,13 +63,19 @@ typedef enum smla_dtype {
   SMLA_E4M3 = 1                    /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */
 } smla_dtype;
 
-/* Kernel selection (smla_args.kernel).  AUTO picks the tensor-core kernel.
- * The tensor-core kernels run on pairs of CTAs, CTA r keeping output dims
- * [256 r, 256 r + 256) of every head; they differ in where the softmax runs.  TCGEN05: both CTAs add the peer's partial logits
- * and run the softmax of every head.  TCGEN05_HEAD_OWNED (E4M3 rows; BF16
- * rows take TCGEN05): each CTA runs the softmax of half the heads and sends
- * the peer their E4M3 P; it moves fewer bytes between the CTAs but is slower
- * (a round trip per tile), and is kept as an alternative. */
+/* Kernel selection (smla_args.kernel).  The tensor-core kernels run on pairs
+ * of CTAs, CTA r keeping output dims [256 r, 256 r + 256) of every head; they
+ * differ in how the logits are split between the CTAs.  TCGEN05: each CTA
+ * gathers its dims half of every row, computes partial logits, and both CTAs
+ * add the peer's partial and run the softmax of every head.
+ * TCGEN05_SLOT_SPLIT (E4M3 rows; BF16 rows take TCGEN05): CTA r gathers the
+ * full rows of half of every 128-slot tile, computes their complete logits,
+ * and the pair exchanges per-head maxima, E4M3 P halves and the rows' other
+ * output half instead of partial logits.  TCGEN05_HEAD_OWNED (E4M3 rows;
+ * BF16 rows take TCGEN05): each CTA runs the softmax of half the heads and
+ * sends the peer their E4M3 P; slower (a round trip per tile), kept as an
+ * alternative.  AUTO picks TCGEN05_SLOT_SPLIT for E4M3 rows (TCGEN05 when
+ * the BALANCED schedule is asked for) and TCGEN05 for BF16 rows. */
 /* Work hand-out of the TCGEN05 kernel (smla_args.schedule).  GRID: one CTA
  * pair per (token, split), the split count from num_splits / max_splits.
  * BALANCED (with num_splits == 0 and max_splits == 0, W <= 2304 and T <= 14
@@ -92,7 +98,8 @@ typedef enum smla_kernel {
   SMLA_KERNEL_AUTO = 0,
   SMLA_KERNEL_CUDA_CORE = 1,          /* plain CUDA-core kernel (fp32 FMA) */
   SMLA_KERNEL_TCGEN05 = 2,            /* tcgen05 / TMEM tensor-core kernel */
-  SMLA_KERNEL_TCGEN05_HEAD_OWNED = 3  /* tcgen05 kernel, softmax split between the CTAs by head */
+  SMLA_KERNEL_TCGEN05_HEAD_OWNED = 3, /* tcgen05 kernel, softmax split between the CTAs by head */
+  SMLA_KERNEL_TCGEN05_SLOT_SPLIT = 4  /* tcgen05 kernel, each CTA of a pair takes half of every tile's slots */
 } smla_kernel;
 
 /* Bits the kernels OR into *error_word (device-side detection, no trap). */

@@ -26,7 +26,7 @@ MAX_SPLITS = 64
 
 SMLA_OK, SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE_TOO_SMALL, SMLA_ERR_CUDA = range(5)
 SMLA_BF16, SMLA_E4M3 = 0, 1
-KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED, KERNEL_TCGEN05_SLOT_SPLIT = 0, 1, 2, 3, 4
 SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_BALANCED = 0, 1, 2
 DEVERR_INDEX_OUT_OF_RANGE = 0x1
 

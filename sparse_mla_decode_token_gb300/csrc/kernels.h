@@ -39,6 +39,13 @@ int tc_head_owned_smem_bytes();
 int tc_head_owned_threads();
 cudaError_t launch_decode_tc_head_owned(const DecodeParams& p, int grid, cudaStream_t stream);
 
+// tcgen05 decode kernel for E4M3 rows with the slot-split pair
+// (decode_tc_slot.cu): a 2-CTA cluster per (token, split), same column limit;
+// each CTA computes the full logits of its half of every 128-slot tile.
+int tc_slot_smem_bytes();
+int tc_slot_threads();
+cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, cudaStream_t stream);
+
 // Split-K log-sum-exp combine (combine.cu)
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
 

@@ -61,7 +61,7 @@ smla_status check_shapes(const smla_args* a) {
   if (a->schedule < SMLA_SCHEDULE_AUTO || a->schedule > SMLA_SCHEDULE_BALANCED)
     return fail(SMLA_ERR_INVALID_ARG, "schedule %d is not an smla_schedule", a->schedule);
   if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05 &&
-      a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED)
+      a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->kernel != SMLA_KERNEL_TCGEN05_SLOT_SPLIT)
     return fail(SMLA_ERR_INVALID_ARG, "kernel %d is not a smla_kernel", a->kernel);
   if (a->swa_rows < 0 || a->comp_rows < 0)
     return fail(SMLA_ERR_INVALID_ARG, "negative pool row count");
@@ -199,9 +199,15 @@ smla_status validate_host(const smla_args* a) {
   return SMLA_OK;
 }
 
-// Kernel and schedule that SMLA_KERNEL_AUTO / SMLA_SCHEDULE_AUTO select.
-constexpr int kAutoKernel = SMLA_KERNEL_TCGEN05;
+// Kernel and schedule that SMLA_KERNEL_AUTO / SMLA_SCHEDULE_AUTO select: the
+// slot-split kernel for E4M3 rows (unless the balanced schedule is asked
+// for, which only the dims-split kernel runs), the dims-split kernel for BF16.
 constexpr int kAutoSchedule = SMLA_SCHEDULE_GRID;
+int auto_kernel(const smla_args* a) {
+  const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
+  return a->dtype == SMLA_E4M3 && schedule != SMLA_SCHEDULE_BALANCED ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
+                                                                     : SMLA_KERNEL_TCGEN05;
+}
 
 std::atomic<int> g_sm_count[64];   // per device; 0 = not queried yet (callers may be on several threads)
 
@@ -223,15 +229,23 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
-  const int kernel = a->kernel == SMLA_KERNEL_AUTO ? kAutoKernel : a->kernel;
+  const int kernel = a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a) : a->kernel;
   int S = a->num_splits;
-  if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED) {
+  if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED ||
+      kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT) {
     // 2-CTA clusters: balanced mode, else one cluster per (token, split).
+    // The head-owned and slot-split forms are E4M3 only (BF16 takes the
+    // dims-split kernel) and run the grid schedule.
     const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
-    plan->kernel = head_owned ? SMLA_KERNEL_TCGEN05_HEAD_OWNED : SMLA_KERNEL_TCGEN05;
+    const bool slot_split = kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT && a->dtype == SMLA_E4M3;
+    plan->kernel = head_owned   ? SMLA_KERNEL_TCGEN05_HEAD_OWNED
+                   : slot_split ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
+                                : SMLA_KERNEL_TCGEN05;
     plan->ctas_per_split = 2;
-    plan->threads = head_owned ? tc_head_owned_threads() : tc_grid_threads();
-    plan->smem_bytes = head_owned ? tc_head_owned_smem_bytes() : tc_grid_smem_bytes(a->dtype);
+    plan->threads = head_owned ? tc_head_owned_threads() : slot_split ? tc_slot_threads() : tc_grid_threads();
+    plan->smem_bytes = head_owned   ? tc_head_owned_smem_bytes()
+                       : slot_split ? tc_slot_smem_bytes()
+                                    : tc_grid_smem_bytes(a->dtype);
     const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
     if (s_min > SMLA_MAX_SPLITS)
       return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
@@ -240,7 +254,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
                   S, s_min, SMLA_TC_MAX_SPLIT_COLS);
     const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
     const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
-    if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned &&
+    if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned && !slot_split &&
         a->width <= SMLA_TC_MAX_SPLIT_COLS && a->sum_q <= (int64_t)(SMLA_TC_MAX_UNITS - 2) * pairs) {
       // Balanced mode: P clusters, one per SM pair, take equal shares of the
       // T x W columns, each share at least 64 columns.  A share of at most
@@ -440,6 +454,8 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   }
   if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     ce = launch_decode_tc_head_owned(p, plan.grid, stream);
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT)
+    ce = launch_decode_tc_slot(p, plan.grid, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05 && plan.clusters > 0)
     ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, piece_cnt, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05)

@@ -385,3 +385,51 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
 
 }  // namespace ptx
 }  // namespace smla
+
+namespace smla {
+namespace ptx {
+
+// Shared-memory matrix descriptor without swizzle (K-major "interleaved"
+// canonical layout: 8-row x 16-byte core matrices of 128 contiguous bytes;
+// lbo = byte distance between core matrices adjacent along K, sbo = between
+// 8-row groups), layout type 0 at bits 61-63.
+__device__ __forceinline__ uint64_t desc_noswizzle(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's (destination and mbarrier addresses from map_to_rank); the
+// bytes complete on that CTA's mbarrier.  Source and destination are read and
+// written through the async proxy.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// 16-byte store to this CTA's shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Prefetch the 128-byte line holding addr into L2.
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
+// Named barrier over `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace ptx
+}  // namespace smla

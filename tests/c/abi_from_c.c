@@ -43,7 +43,7 @@ int main(void) {
   smla_args a = base(128, 2176);
   smla_plan p;
   smla_status st = smla_plan_decode_for_sm_count(&a, 152, &p);
-  CHECK(st == SMLA_OK && p.kernel == SMLA_KERNEL_TCGEN05 && p.num_splits == 1 && p.grid == 256 &&
+  CHECK(st == SMLA_OK && p.kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT && p.num_splits == 1 && p.grid == 256 &&
             p.clusters == 0 && p.workspace_bytes == 0,
         "plan 128 tokens: kernel %d splits %d grid %d clusters %d threads %d smem %d", p.kernel, p.num_splits,
         p.grid, p.clusters, p.threads, p.smem_bytes);

@@ -23,7 +23,7 @@ def built():
     B.lib()
 
 
-@pytest.mark.parametrize("kernel", [B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED, B.KERNEL_CUDA_CORE])
+@pytest.mark.parametrize("kernel", [B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED, B.KERNEL_TCGEN05_SLOT_SPLIT, B.KERNEL_CUDA_CORE])
 @pytest.mark.parametrize("dtype,splits", [("bf16", 1), ("e4m3", 1), ("bf16", 3), ("e4m3", 2)])
 def test_decode_replays_from_a_cuda_graph(kernel, dtype, splits):
     w = W.make_workload(name="graph", seed=41, dtype=dtype, batch=3, q_lens=[1, 2, 1], num_heads=128,

@@ -16,7 +16,7 @@ from gpu_helpers import compare, device_inputs, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED]
+KERNELS = [B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED, B.KERNEL_TCGEN05_SLOT_SPLIT]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -104,9 +104,12 @@ def test_plans_of_the_committed_traffic_records():
 @pytest.mark.parametrize("n,splits,grid", [(1, 4, 16), (2, 2, 128), (3, 1, 256), (4, 1, 324),
                                            (5, 19, 152), (6, 1, 256)])
 def test_named_workload_plans(n, splits, grid):
+    """E4M3 workloads (3, 5, 6) take the slot-split kernel, BF16 ones the
+    dims-split kernel; both by the grid-mode rule."""
     p = plan(workload_args(n))
+    kernel = B.KERNEL_TCGEN05_SLOT_SPLIT if workload_args(n).dtype == B.SMLA_E4M3 else B.KERNEL_TCGEN05
     assert (p["kernel"], p["num_splits"], p["grid"], p["ctas_per_split"], p["clusters"]) == \
-        (B.KERNEL_TCGEN05, splits, grid, 2, 0)
+        (kernel, splits, grid, 2, 0)
 
 
 @pytest.mark.parametrize("n,grid,clusters", [(1, 16, 8), (2, 152, 76), (3, 152, 76), (4, 152, 76),
@@ -129,6 +132,27 @@ def test_head_owned_form_is_opt_in_and_e4m3_only():
     assert (ho["num_splits"], ho["grid"], ho["ctas_per_split"]) == (expected_tc_splits(128, 2176), 256, 2)
     bf = plan(args(32, 640, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05_HEAD_OWNED, schedule=B.SCHEDULE_BALANCED))
     assert bf["kernel"] == B.KERNEL_TCGEN05 and bf["clusters"] == 76
+
+
+def test_slot_split_form_is_the_e4m3_default():
+    """The slot-split form runs on E4M3 rows only (BF16 rows asking for it get
+    the dims-split kernel); it is what AUTO picks for E4M3 rows, except under
+    the balanced schedule, which only the dims-split kernel runs.  Like the
+    head-owned form it has no balanced mode and takes the grid-mode rule."""
+    auto = plan(args(128, 2176))
+    assert auto["kernel"] == B.KERNEL_TCGEN05_SLOT_SPLIT and auto["clusters"] == 0
+    bal = plan(args(128, 2176, schedule=B.SCHEDULE_BALANCED))
+    assert bal["kernel"] == B.KERNEL_TCGEN05 and bal["clusters"] == 76
+    assert plan(args(32, 640, dtype=B.SMLA_BF16))["kernel"] == B.KERNEL_TCGEN05
+    ss = plan(args(128, 2176, kernel=B.KERNEL_TCGEN05_SLOT_SPLIT, schedule=B.SCHEDULE_BALANCED))
+    assert ss["kernel"] == B.KERNEL_TCGEN05_SLOT_SPLIT and ss["clusters"] == 0
+    assert (ss["num_splits"], ss["grid"], ss["ctas_per_split"]) == (expected_tc_splits(128, 2176), 256, 2)
+    assert ss["threads"] == 512 and ss["smem_bytes"] <= 232448
+    for T, W_ in [(4, 16512), (32, 640), (1, 65536)]:
+        p = plan(args(T, W_, kernel=B.KERNEL_TCGEN05_SLOT_SPLIT))
+        assert p["kernel"] == B.KERNEL_TCGEN05_SLOT_SPLIT and p["num_splits"] == expected_tc_splits(T, W_)
+    bf = plan(args(32, 640, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05_SLOT_SPLIT))
+    assert bf["kernel"] == B.KERNEL_TCGEN05
 
 
 def workspace(rows):
@@ -203,7 +227,7 @@ def test_bad_sm_count_and_null_plan():
     assert B.lib().smla_plan_decode_for_sm_count(None, 152, None) == B.SMLA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("field,value", [("kernel", 4), ("kernel", -1), ("schedule", 3), ("schedule", -1)])
+@pytest.mark.parametrize("field,value", [("kernel", 5), ("kernel", -1), ("schedule", 3), ("schedule", -1)])
 def test_unknown_kernel_or_schedule_is_an_error(field, value):
     a = args(8, 640)
     setattr(a, field, value)
