@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 6
+#define SMLA_ABI_VERSION 7
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */

@@ -367,6 +367,20 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == B.SMLA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_slot_split_many_units(H, splits):
+    """More (token, split) units than SM pairs (several waves of the
+    slot-split kernel): tokens of one to four 128-slot tiles, every fourth
+    token fully masked (no slot at all), and split partials."""
+    w = small_case(500 + H + splits, dtype="e4m3", H=H, batch=200, width=128 + 400)
+    w.indices[::4, :] = -1
+    out, lse, plan = run_gpu(w, kernel=B.KERNEL_TCGEN05_SLOT_SPLIT, num_splits=splits)
+    assert plan["kernel"] == B.KERNEL_TCGEN05_SLOT_SPLIT and plan["num_splits"] == splits
+    assert plan["grid"] == 2 * 200 * splits
+    compare(w, out, lse)
+
+
 def test_many_tokens_grid():
     """More than 65535 tokens: tokens live on grid.x, so no launch limit is hit.
 
