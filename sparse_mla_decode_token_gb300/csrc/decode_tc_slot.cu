@@ -395,8 +395,8 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       prefetch_tensormap(&P.tm_comp_run);
     }
     const uint32_t r_free_peer = map_to_rank(bar(sm.r_free[0]), peer);
-    int j = 0;
-    for (; j < ntiles; ++j) {
+    int issued = 0;                          // tiles whose gathers were issued
+    for (int j = 0; j < ntiles; ++j) {
       const int iv = j % kNV, ik = j % kNK, ir = j % kNR;
       // the V entry is free once this CTA's PV of the own slots of tile j - 4
       // is done; the K entry once the QK of tile j - 3 is done and its copy
@@ -434,6 +434,7 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
         }
       }
       }
+      issued = j + 1;
       // the R entry of tile j is free once this CTA's PV of the peer's slots
       // of tile j - 4 is done: arm it and let the peer send its copy
       if (!warp_wait(cx, bar(sm.r_empty[ir]), ((j / kNR) & 1) ^ 1)) break;
@@ -443,9 +444,9 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       }
     }
     // leave no TMA write in flight (bounded, not cut short by the abort
-    // flag): the last tiles issued, at most one per V entry
-    for (int jj = max(0, min(j, ntiles) - kNV); jj < min(j, ntiles); ++jj)
-      drain_wait(bar(sm.kv_full[jj % kNV]), (jj / kNV) & 1);
+    // flag): the last tiles issued (also one whose R entry wait gave up), at
+    // most one per V entry
+    for (int jj = max(0, issued - kNV); jj < issued; ++jj) drain_wait(bar(sm.kv_full[jj % kNV]), (jj / kNV) & 1);
   } else if (warp < kSoftmaxWarp0) {
     regs_decrease<kRegsMma>();
     if (warp < kMmaWarp + kQkWarps) {
