@@ -46,6 +46,24 @@ Readings where the pages are silent (each is listed in the design notes):
 * An index < -1 or >= the pool's row count is a caller error: raised by
   default, or treated as masked with ``invalid_index="mask"``.
 
+Packed KV rows (§8(f) f2; trtllm_batch_decode_sparse_mla_dsv4, description,
+SM120/SM121 paragraph: "packed uint8 ... 584 bytes per token", BF16 query;
+cake_sparse_mla_sm120_dsv4_nvfp4_decode, Parameters: kv_cache "NVFP4 ...
+384 bytes per token", q "448 NoPE dims, then 64 RoPE dims").  The pages give
+only the sizes; the byte layouts are our reading (PARITY UNPINNED by the
+pages for the layout; pinned here against the bit-format definitions):
+
+* ``packed_fp8`` (584 B): bytes [0, 448) the 448 NoPE values in E4M3; bytes
+  [448, 455) seven UE8M0 block exponents e_b, NoPE dim d scaled by
+  2^(e_{d // 64} - 127); byte 455 unused; bytes [456, 584) the 64 RoPE values
+  in BF16 (little-endian).
+* ``nvfp4`` (384 B): bytes [0, 224) the 448 NoPE values in E2M1, dim 2i in
+  the low nibble and dim 2i + 1 in the high nibble of byte i; bytes
+  [224, 252) 28 E4M3 block scales, NoPE dim d scaled by scale_{d // 16};
+  bytes [252, 380) the 64 RoPE values in BF16; bytes [380, 384) an fp32 row
+  scale applied to every NoPE value.
+* With either, the query is BF16; K = V = the decoded 512-wide row.
+
 Page-table form of the compressed segment (trtllm_batch_decode_sparse_mla_dsv4,
 Parameters: hca_swa_indices, hca_compressed_block_tables, hca_seq_lens,
 swa_topk_lens, hca_sparse_indices_format):
@@ -109,12 +127,74 @@ def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
     return E4M3_TABLE[np.asarray(bits, dtype=np.uint8)]
 
 
+def _e2m1_value(code: int) -> float:
+    """OCP 4-bit floating point E2M1: 1 sign bit, 2 exponent bits (bias 1),
+    1 mantissa bit; exponent field 0 encodes the subnormal m/2."""
+    sign = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return sign * m * 0.5
+    return sign * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+PACKED_ROW_BYTES = {"packed_fp8": 584, "nvfp4": 384}
+NOPE_DIMS = 448
+
+
+def ue8m0_to_f64(bits: np.ndarray) -> np.ndarray:
+    """UE8M0 (unsigned exponent-only scale): 2^(e - 127)."""
+    return np.exp2(np.asarray(bits, dtype=np.float64) - 127.0)
+
+
+def _bf16_pairs(raw: np.ndarray) -> np.ndarray:
+    """[..., 2n] bytes (little-endian) -> [..., n] BF16 values."""
+    u16 = raw[..., 0::2].astype(np.uint16) | (raw[..., 1::2].astype(np.uint16) << np.uint16(8))
+    return bf16_to_f64(u16)
+
+
+def decode_packed_fp8_rows(rows: np.ndarray) -> np.ndarray:
+    """[n, 584] uint8 -> [n, 512] float64 (layout in the module docstring)."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    nope = e4m3_to_f64(rows[:, :NOPE_DIMS])
+    scale = ue8m0_to_f64(rows[:, NOPE_DIMS:NOPE_DIMS + 7])            # [n, 7]
+    nope = nope * np.repeat(scale, 64, axis=1)
+    rope = _bf16_pairs(rows[:, 456:584])
+    return np.concatenate([nope, rope], axis=1)
+
+
+def decode_nvfp4_rows(rows: np.ndarray) -> np.ndarray:
+    """[n, 384] uint8 -> [n, 512] float64 (layout in the module docstring)."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    packed = rows[:, :224]
+    codes = np.empty((rows.shape[0], NOPE_DIMS), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0x0F
+    codes[:, 1::2] = packed >> 4
+    block = e4m3_to_f64(rows[:, 224:252])                              # [n, 28]
+    row_scale = rows[:, 380:384].copy().view(np.float32).astype(np.float64)   # [n, 1]
+    nope = E2M1_TABLE[codes] * np.repeat(block, 16, axis=1) * row_scale
+    rope = _bf16_pairs(rows[:, 252:380])
+    return np.concatenate([nope, rope], axis=1)
+
+
 def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
-    if dtype == "bf16":
+    """Query elements (bf16 / e4m3 bits; BF16 for the packed KV forms)."""
+    if dtype in ("bf16", "packed_fp8", "nvfp4"):
         return bf16_to_f64(bits)
     if dtype == "e4m3":
         return e4m3_to_f64(bits)
     raise ValueError(dtype)
+
+
+def decode_rows(rows: np.ndarray, dtype: str) -> np.ndarray:
+    """KV rows of one pool -> [n, 512] float64."""
+    if dtype == "packed_fp8":
+        return decode_packed_fp8_rows(rows)
+    if dtype == "nvfp4":
+        return decode_nvfp4_rows(rows)
+    return decode(rows, dtype)
 
 
 # --------------------------------------------------------------------------
@@ -264,7 +344,7 @@ def _gather(pool_bits: dict, slots, dtype: str) -> np.ndarray:
     if not slots:
         return np.zeros((0, HEAD_DIM))
     rows = [pool_bits[p][r] for (_, p, r) in slots]
-    return decode(np.stack(rows), dtype)
+    return decode_rows(np.stack(rows), dtype)
 
 
 def sparse_mla_decode(*, dtype: str, batch: int, q, swa_kv, comp_kv, indices,

@@ -30,6 +30,14 @@ H in {64, 128}, BF16 or per-tensor FP8 E4M3) and the vLLM DeepSeek-V4 caller's
 scale folding (``bmm1 = softmax_scale * q_scale * kv_scale``, ``bmm2 = kv_scale``).
 Values are N(0, 1); FP8 tensors are quantised with a per-tensor scale
 ``amax / 448`` by round-to-nearest-even after clamping to the E4M3 range.
+
+Packed KV rows (``dtype`` ``"packed_fp8"``: 584 bytes, ``"nvfp4"``: 384
+bytes per row; the byte layouts are the oracle's reading of the FlashInfer
+pages, which give only the sizes) hold the same N(0, 1) values: the 448 NoPE
+dims quantised per block (packed_fp8: a power-of-two UE8M0 exponent per 64
+dims so that the block fits E4M3; nvfp4: an fp32 row scale amax / (6 * 448)
+and an E4M3 scale per 16 dims so that the block fits E2M1), the 64 RoPE dims
+in BF16.  The query is BF16 with these rows.
 """
 from __future__ import annotations
 
@@ -43,6 +51,9 @@ import torch
 HEAD_DIM = 512
 SWA_COLS = 128
 E4M3_MAX = 448.0
+NOPE_DIMS = 448
+PACKED_ROW_BYTES = {"packed_fp8": 584, "nvfp4": 384}
+E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
 @dataclasses.dataclass
@@ -84,7 +95,17 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
+        """Bytes per KV element (packed rows: per byte of the row)."""
         return 2 if self.dtype == "bf16" else 1
+
+    @property
+    def packed(self) -> bool:
+        return self.dtype in PACKED_ROW_BYTES
+
+    @property
+    def row_bytes(self) -> int:
+        """Bytes of one KV row (512 elements, or the packed row size)."""
+        return PACKED_ROW_BYTES[self.dtype] if self.packed else HEAD_DIM * self.elem_bytes
 
 
 # --------------------------------------------------------------------------
@@ -106,6 +127,63 @@ def _normal(gen: torch.Generator, shape) -> torch.Tensor:
 
 def _encode(x: torch.Tensor, dtype: str, scale: float) -> np.ndarray:
     return _to_bf16_bits(x) if dtype == "bf16" else _to_e4m3_bits(x, scale)
+
+
+def _bf16_bytes(x: torch.Tensor) -> np.ndarray:
+    """[n, k] values -> [n, 2k] bytes of their BF16 bits, little-endian."""
+    return np.ascontiguousarray(_to_bf16_bits(x)).view(np.uint8)
+
+
+def _to_packed_fp8_rows(x: torch.Tensor) -> np.ndarray:
+    """[n, 512] values -> [n, 584] packed rows (448 E4M3 NoPE scaled by a
+    UE8M0 exponent per 64 dims, 8 bytes of exponents, 64 BF16 RoPE)."""
+    n = x.shape[0]
+    nope = x[:, :NOPE_DIMS].reshape(n, 7, 64)
+    amax = nope.abs().amax(dim=2).clamp_min(1e-30)
+    e = torch.ceil(torch.log2(amax / E4M3_MAX)).clamp(-127, 127)        # block / 2^e fits E4M3
+    codes = _to_e4m3_bits((nope / torch.exp2(e)[:, :, None]).reshape(n, NOPE_DIMS), 1.0)
+    rows = np.zeros((n, 584), dtype=np.uint8)
+    rows[:, :NOPE_DIMS] = codes
+    rows[:, NOPE_DIMS:NOPE_DIMS + 7] = (e + 127).to(torch.int64).numpy().astype(np.uint8)
+    rows[:, 456:584] = _bf16_bytes(x[:, NOPE_DIMS:])
+    return rows
+
+
+def _to_e2m1_codes(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code of each value (|v| <= 6 expected)."""
+    mid = (E2M1_MAGNITUDES[1:] + E2M1_MAGNITUDES[:-1]) / 2.0
+    mag = np.searchsorted(mid, np.abs(v)).astype(np.uint8)              # 0..7
+    return mag | np.where(v < 0, 8, 0).astype(np.uint8)
+
+
+def _to_nvfp4_rows(x: torch.Tensor) -> np.ndarray:
+    """[n, 512] values -> [n, 384] rows (448 E2M1 NoPE, 28 E4M3 block scales
+    per 16 dims, 64 BF16 RoPE, an fp32 row scale)."""
+    n = x.shape[0]
+    nope = x[:, :NOPE_DIMS].double()
+    g = (nope.abs().amax(dim=1) / (6.0 * E4M3_MAX)).clamp_min(1e-30).float()           # fp32 row scale
+    blocks = nope.reshape(n, 28, 16)
+    bscale = (blocks.abs().amax(dim=2) / 6.0 / g.double()[:, None]).float()
+    bcodes = _to_e4m3_bits(bscale, 1.0)                                                  # [n, 28]
+    bval = torch.from_numpy(bcodes.copy()).view(torch.float8_e4m3fn).double()
+    denom = (bval * g.double()[:, None]).clamp_min(1e-300)
+    v = (blocks / denom[:, :, None]).reshape(n, NOPE_DIMS).numpy()
+    codes = _to_e2m1_codes(v)
+    rows = np.zeros((n, 384), dtype=np.uint8)
+    rows[:, :224] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    rows[:, 224:252] = bcodes
+    rows[:, 252:380] = _bf16_bytes(x[:, NOPE_DIMS:])
+    rows[:, 380:384] = np.ascontiguousarray(g.numpy().astype(np.float32)).view(np.uint8).reshape(n, 4)
+    return rows
+
+
+def _encode_rows(x: torch.Tensor, dtype: str, scale: float) -> np.ndarray:
+    """KV pool values -> the pool's stored form."""
+    if dtype == "packed_fp8":
+        return _to_packed_fp8_rows(x)
+    if dtype == "nvfp4":
+        return _to_nvfp4_rows(x)
+    return _encode(x, dtype, scale)
 
 
 def _pertensor_scale(*xs: torch.Tensor) -> float:
@@ -154,7 +232,8 @@ def _unique_rows(rng: np.random.Generator, n_rows: int, k: int) -> np.ndarray:
 
 def _draw_values(gen: torch.Generator, dtype: str, sum_q: int, num_heads: int,
                  swa_rows: int, comp_rows: int):
-    """N(0, 1) query and pools, encoded; FP8 takes per-tensor scales amax / 448."""
+    """N(0, 1) query and pools, encoded; FP8 takes per-tensor scales amax / 448;
+    packed rows carry their own scales and go with a BF16 query."""
     qf = _normal(gen, (sum_q, num_heads, HEAD_DIM))
     swaf = _normal(gen, (swa_rows, HEAD_DIM))
     compf = _normal(gen, (comp_rows, HEAD_DIM))
@@ -163,8 +242,9 @@ def _draw_values(gen: torch.Generator, dtype: str, sum_q: int, num_heads: int,
         kv_scale = _pertensor_scale(swaf, compf)
     else:
         q_scale = kv_scale = 1.0
-    return (_encode(qf, dtype, q_scale), _encode(swaf, dtype, kv_scale),
-            _encode(compf, dtype, kv_scale), q_scale, kv_scale)
+    q_dtype = "e4m3" if dtype == "e4m3" else "bf16"
+    return (_encode(qf, q_dtype, q_scale), _encode_rows(swaf, dtype, kv_scale),
+            _encode_rows(compf, dtype, kv_scale), q_scale, kv_scale)
 
 
 def _lengths(q_lens, seq_lens, batch: int):
@@ -194,7 +274,7 @@ def make_workload(*, name: str = "custom", seed: int, dtype: str, batch: int,
     per-token sequence.  SWA columns come from a per-request ring of
     ``ring_len`` rows (default ``swa_rows // batch``).
     """
-    assert dtype in ("bf16", "e4m3")
+    assert dtype in ("bf16", "e4m3", "packed_fp8", "nvfp4")
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
     q_lens, seq_lens, cum = _lengths(q_lens, seq_lens, batch)
@@ -255,7 +335,7 @@ def make_paged_workload(*, name: str = "paged", seed: int, dtype: str, batch: in
     given, else the seq_lens rule.  ``width`` (logical columns) defaults to
     ``128 + max_pages * page_size``.
     """
-    assert dtype in ("bf16", "e4m3")
+    assert dtype in ("bf16", "e4m3", "packed_fp8", "nvfp4")
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
     q_lens, seq_lens, cum = _lengths(q_lens, seq_lens, batch)

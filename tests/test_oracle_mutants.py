@@ -18,6 +18,7 @@ import pytest
 
 from oracle import oracle as orc
 
+import test_oracle_packed_pins as packed_pins
 import test_oracle_pins as pins
 
 
@@ -33,6 +34,9 @@ def _plant(monkeypatch, fn_name: str, old: str, new: str) -> None:
     if fn_name == "_e4m3_value":                         # the table is built from it at import
         monkeypatch.setattr(orc, "E4M3_TABLE",
                             np.array([scope[fn_name](c) for c in range(256)], dtype=np.float64))
+    if fn_name == "_e2m1_value":
+        monkeypatch.setattr(orc, "E2M1_TABLE",
+                            np.array([scope[fn_name](c) for c in range(16)], dtype=np.float64))
 
 
 def _split2():
@@ -54,6 +58,28 @@ MUTANTS = [
      pins.test_e4m3_decode_matches_torch_for_every_code),
     ("e4m3_no_nan", "_e4m3_value", "if e == 0xF and m == 0x7:", "if False:",
      pins.test_e4m3_decode_matches_torch_for_every_code),
+    # packed KV rows
+    ("e2m1_bias_0", "_e2m1_value", "2.0 ** (e - 1)", "2.0 ** e",
+     packed_pins.test_e2m1_decode_matches_the_specification_for_every_code),
+    ("e2m1_subnormal_implicit_one", "_e2m1_value", "return sign * m * 0.5", "return sign * (1.0 + m) * 0.5",
+     packed_pins.test_e2m1_decode_matches_the_specification_for_every_code),
+    ("ue8m0_bias_128", "ue8m0_to_f64", "- 127.0", "- 128.0", packed_pins.test_ue8m0_is_a_power_of_two_exponent),
+    ("packed_fp8_blocks_reversed", "decode_packed_fp8_rows", "np.repeat(scale, 64, axis=1)",
+     "np.repeat(scale[:, ::-1], 64, axis=1)", packed_pins.test_packed_fp8_row_closed_form),
+    ("packed_fp8_rope_shifted", "decode_packed_fp8_rows", "rows[:, 456:584]", "rows[:, 454:582]",
+     packed_pins.test_packed_fp8_row_closed_form),
+    ("nvfp4_high_nibble_first", "decode_nvfp4_rows", "codes[:, 0::2] = packed & 0x0F",
+     "codes[:, 0::2] = packed >> 4", packed_pins.test_nvfp4_row_closed_form),
+    ("nvfp4_blocks_reversed", "decode_nvfp4_rows", "np.repeat(block, 16, axis=1)",
+     "np.repeat(block[:, ::-1], 16, axis=1)", packed_pins.test_nvfp4_row_closed_form),
+    ("nvfp4_row_scale_dropped", "decode_nvfp4_rows", "* np.repeat(block, 16, axis=1) * row_scale",
+     "* np.repeat(block, 16, axis=1)", packed_pins.test_nvfp4_row_closed_form),
+    ("nvfp4_rope_shifted", "decode_nvfp4_rows", "rows[:, 252:380]", "rows[:, 256:384]",
+     packed_pins.test_nvfp4_row_closed_form),
+    ("packed_query_as_e4m3", "decode", 'if dtype in ("bf16", "packed_fp8", "nvfp4"):',
+     'if dtype in ("bf16",):', packed_pins.test_single_slot_through_an_nvfp4_row),
+    ("packed_rows_decoded_as_bf16", "decode_rows", 'if dtype == "packed_fp8":', 'if dtype == "packed":',
+     packed_pins.test_single_slot_through_a_packed_fp8_row),
     # token metadata
     ("dense_tokens_strided", "token_request", "return t // q_len, t % q_len, q_len",
      "return t % batch, t // batch, q_len", pins.test_varlen_right_aligned_positions),
