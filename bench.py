@@ -39,6 +39,9 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 HEAD_DIM, SWA_COLS = 512, 128
+# fp32 FMA peak of the CUDA cores (the CUDA-core kernel's bound, which the
+# packed KV forms run on): 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 # ------------------------------------------------------------------ accounting
@@ -299,13 +302,14 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     w = W.config_workload(args.config)
     n_valid = valid_slots_per_token(w)
-    eb = w.elem_bytes
-    gathered_bytes = int(n_valid.sum()) * HEAD_DIM * eb          # per step
+    gathered_bytes = int(n_valid.sum()) * w.row_bytes             # per step (the packed rows' own size)
     flops = int(n_valid.sum()) * 2 * 2 * HEAD_DIM * w.num_heads   # QK + PV, 2 flops per MAC
 
     def kv(a):
         t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(torch.int16).view(torch.bfloat16) if w.dtype == "bf16" else t.view(torch.float8_e4m3fn))
+        if a.dtype == np.uint16:                                # BF16 bits (query, or BF16 rows)
+            return t.view(torch.int16).view(torch.bfloat16)
+        return t if w.packed else t.view(torch.float8_e4m3fn)   # packed rows stay uint8
 
     def i32(a):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
@@ -516,14 +520,20 @@ def run_gpu(args):
     d2h = e2e_sets[0]["h_res"].numel()                  # bytes of the one packed copy out per step
 
     hbm_gbs, bf16_tf, peak_src = peaks()
-    if w.dtype == "e4m3":
+    cuda_core = plan.kernel == B.KERNEL_CUDA_CORE
+    if cuda_core:
+        # fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 flops x 2.07 GHz
+        dtype_tf, tensor_src = FP32_ALU_TFLOPS, "fp32 FMA lanes x clock (152 SMs x 128 x 2 x 2.07 GHz)"
+    elif w.dtype == "e4m3":
         dtype_tf, tensor_src = fp8_tensor_peak(bf16_tf)
     else:
         dtype_tf, tensor_src = bf16_tf, peak_src
     main_s = statistics.mean(main_ms) / 1e3
     t_hbm = gathered_bytes / (hbm_gbs * 1e9)
     t_tc = flops / (dtype_tf * 1e12)
-    if t_hbm >= t_tc:
+    if cuda_core and t_tc > t_hbm:
+        roof = {"bound": "alu", "achieved": flops / main_s / 1e12, "peak": dtype_tf, "unit": "TFLOP/s"}
+    elif t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": gathered_bytes / main_s / 1e9, "peak": hbm_gbs,
                 "unit": "GB/s"}
     else:
@@ -552,7 +562,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if w.dtype == "e4m3" else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("f32" if plan.kernel == B.KERNEL_CUDA_CORE else
+                                       "e4m3" if w.dtype == "e4m3" else "bf16"), "data": "synthetic",
         "config": workload_config(w, args.config),
         "gathered_kv_gbs": gathered_bytes * K * ws_ / total_s / 1e9,
         "roofline": roof,
@@ -576,7 +587,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8],
                     help="workload (3 = FP8 decode, 128 tokens, H=128; 6 = the same with page-table "
                          "compressed segments)")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")

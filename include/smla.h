@@ -58,9 +58,26 @@ typedef enum smla_status {
   SMLA_ERR_CUDA = 4                /* a CUDA runtime call or launch failed */
 } smla_status;
 
+/* Element types.  The packed forms take a BF16 query and KV pools of uint8
+ * rows whose row strides (swa_row_stride, comp_row_stride) count bytes; the
+ * pages (FlashInfer trtllm_batch_decode_sparse_mla_dsv4, description,
+ * SM120/SM121 paragraph; cake_sparse_mla_sm120_dsv4_nvfp4_decode, Parameters:
+ * kv_cache) give only their sizes, the layouts are this library's reading:
+ *   SMLA_PACKED_FP8 (584 bytes, stride a multiple of 8): bytes [0, 448) the
+ *     448 NoPE values in E4M3, [448, 455) seven UE8M0 exponents e (NoPE dim d
+ *     scaled by 2^(e[d / 64] - 127)), byte 455 unused, [456, 584) the 64 RoPE
+ *     values in BF16;
+ *   SMLA_NVFP4 (384 bytes, stride a multiple of 16): bytes [0, 224) the 448
+ *     NoPE values in E2M1 (dim 2i in the low nibble of byte i), [224, 252)
+ *     28 E4M3 block scales (dim d scaled by scale[d / 16]), [252, 380) the 64
+ *     RoPE values in BF16, [380, 384) an fp32 scale of every NoPE value.
+ * Only the CUDA-core kernel decodes the packed forms (it dequantises each
+ * gathered row into shared memory); other kernel requests plan to it. */
 typedef enum smla_dtype {
   SMLA_BF16 = 0,                   /* bfloat16 query and KV rows */
-  SMLA_E4M3 = 1                    /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */
+  SMLA_E4M3 = 1,                   /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */
+  SMLA_PACKED_FP8 = 2,             /* BF16 query, 584-byte packed FP8 KV rows */
+  SMLA_NVFP4 = 3                   /* BF16 query, 384-byte NVFP4 KV rows */
 } smla_dtype;
 
 /* Kernel selection (smla_args.kernel).  The tensor-core kernels run on pairs
@@ -116,13 +133,15 @@ typedef struct smla_args {
   int32_t batch;        /* requests B >= 1 */
   int32_t num_heads;    /* H: 64 or 128 (vLLM get_padded_num_q_heads) */
   int32_t width;        /* index-table columns W >= 128 (W == 128: SWA-only layer) */
-  int32_t dtype;        /* smla_dtype of q, swa_kv and compressed_kv (one type for all three) */
+  int32_t dtype;        /* smla_dtype of q, swa_kv and compressed_kv (one type for all three; the
+                           packed forms: BF16 q, packed KV rows) */
 
   /* query [T, H, 512]; heads and dims contiguous; token stride [H*512] */
   const void* q;
   int64_t q_stride_token;
 
-  /* SWA pool rows [swa_rows, 512]; row stride [512], a multiple of 16 bytes */
+  /* SWA pool rows [swa_rows, 512]; row stride [512], a multiple of 16 bytes (packed forms:
+     rows of 584 / 384 bytes, stride in bytes [the row size], a multiple of 8 / 16) */
   const void* swa_kv;
   int64_t swa_rows;
   int64_t swa_row_stride;

@@ -25,7 +25,9 @@ SWA_COLS = 128
 MAX_SPLITS = 64
 
 SMLA_OK, SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE_TOO_SMALL, SMLA_ERR_CUDA = range(5)
-SMLA_BF16, SMLA_E4M3 = 0, 1
+SMLA_BF16, SMLA_E4M3, SMLA_PACKED_FP8, SMLA_NVFP4 = 0, 1, 2, 3
+# bytes of one KV row of the packed forms (BF16 query; layouts in include/smla.h)
+PACKED_ROW_BYTES = {SMLA_PACKED_FP8: 584, SMLA_NVFP4: 384}
 KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED, KERNEL_TCGEN05_SLOT_SPLIT = 0, 1, 2, 3, 4
 SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_BALANCED = 0, 1, 2
 DEVERR_INDEX_OUT_OF_RANGE = 0x1
@@ -209,11 +211,21 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q/KV dtype {t.dtype} is not bfloat16 or float8_e4m3fn")
 
 
-def _rows_and_stride(kv: torch.Tensor) -> tuple[int, int]:
-    """Flatten a KV pool view ([..., 512], any page layout) to (rows, row stride)."""
-    if kv.shape[-1] != HEAD_DIM or kv.stride(-1) != 1:
-        raise ValueError(f"KV pool must end in a contiguous dim of {HEAD_DIM}; got {tuple(kv.shape)}")
-    flat = kv.reshape(-1, HEAD_DIM) if kv.dim() != 2 else kv
+def _kv_dtype_code(q: torch.Tensor, kv: torch.Tensor) -> int:
+    """KV element type: the query's, or a packed row form (uint8 rows of 584 or
+    384 bytes with a BF16 query)."""
+    if q.dtype == torch.bfloat16 and kv.dtype == torch.uint8:
+        for code, nbytes in PACKED_ROW_BYTES.items():
+            if kv.shape[-1] == nbytes:
+                return code
+    return _dtype_code(kv)
+
+
+def _rows_and_stride(kv: torch.Tensor, row: int = HEAD_DIM) -> tuple[int, int]:
+    """Flatten a KV pool view ([..., row], any page layout) to (rows, row stride)."""
+    if kv.shape[-1] != row or kv.stride(-1) != 1:
+        raise ValueError(f"KV pool must end in a contiguous dim of {row}; got {tuple(kv.shape)}")
+    flat = kv.reshape(-1, row) if kv.dim() != 2 else kv
     if flat.data_ptr() != kv.data_ptr():
         raise ValueError("KV pool view cannot be flattened to rows without a copy")
     return flat.shape[0], flat.stride(0)
@@ -295,8 +307,12 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
     if sparse_indices.shape[0] < T:
         raise ValueError(f"sparse_indices has {sparse_indices.shape[0]} rows for {T} query tokens")
 
-    swa_rows, swa_stride = _rows_and_stride(swa_kv)
-    comp_rows, comp_stride = _rows_and_stride(compressed_kv)
+    kv_code = _kv_dtype_code(q, swa_kv)
+    if _kv_dtype_code(q, compressed_kv) != kv_code:
+        raise TypeError("swa_kv and compressed_kv must share one element type")
+    row = PACKED_ROW_BYTES.get(kv_code, HEAD_DIM)
+    swa_rows, swa_stride = _rows_and_stride(swa_kv, row)
+    comp_rows, comp_stride = _rows_and_stride(compressed_kv, row)
     a = SmlaArgs()
     a.sum_q, a.num_heads, a.width = T, H, sparse_indices.shape[-1]
     if comp_block_tables is not None:
@@ -312,8 +328,8 @@ def make_args(*, q: torch.Tensor, swa_kv: torch.Tensor, compressed_kv: torch.Ten
         raise ValueError("width is the index table's width in the index form")
     a.swa_topk_lens = _ptr(swa_topk_lens)
     a.batch = B
-    a.dtype = _dtype_code(q)
-    if _dtype_code(swa_kv) != a.dtype or _dtype_code(compressed_kv) != a.dtype:
+    a.dtype = kv_code
+    if kv_code not in PACKED_ROW_BYTES and _dtype_code(q) != kv_code:
         raise TypeError("query, swa_kv and compressed_kv must share one dtype")
     a.q, a.q_stride_token = q.data_ptr(), q.stride(0)
     a.swa_kv, a.swa_rows, a.swa_row_stride = swa_kv.data_ptr(), swa_rows, swa_stride
@@ -400,14 +416,17 @@ def sparse_mla_decode(query: torch.Tensor, swa_kv_cache: torch.Tensor, workspace
 
 def workspace_size(query, sparse_indices, seq_lens, *, num_splits=0, max_splits=0,
                    kernel=KERNEL_AUTO, cum_seq_lens_q=None, device: int = 0,
-                   width: Optional[int] = None, schedule: int = 0) -> int:
+                   width: Optional[int] = None, schedule: int = 0, kv_cache=None) -> int:
     """Workspace bytes for a call with these shapes (no device memory is read);
-    ``width`` = logical columns in the page-table form."""
+    ``width`` = logical columns in the page-table form; ``kv_cache`` (a pool
+    view, metadata only) gives the KV element type when it differs from the
+    query's (packed rows)."""
     a = SmlaArgs()
     q3 = query if query.dim() == 3 else query.view(-1, query.shape[2], query.shape[3])
     a.sum_q, a.num_heads = q3.shape[0], q3.shape[1]
     a.width = sparse_indices.shape[-1] if width is None else int(width)
-    a.batch, a.dtype = seq_lens.numel(), _dtype_code(q3)
+    a.batch = seq_lens.numel()
+    a.dtype = _dtype_code(q3) if kv_cache is None else _kv_dtype_code(q3, kv_cache)
     a.cum_seq_lens_q = _ptr(cum_seq_lens_q)
     a.num_splits, a.max_splits, a.kernel, a.schedule = num_splits, max_splits, kernel, schedule
     return smla_workspace_size(a, device)

@@ -6,7 +6,9 @@
 // warp forms the 32 logits of two heads and runs the online softmax with
 // warp shuffles, then every thread updates its 2 output dims of all 16 heads.
 // This kernel is the plain reference point of the library; the tcgen05
-// kernel carries the throughput.
+// kernels carry the throughput.  It is also the kernel of the packed KV row
+// forms (584-byte packed FP8, 384-byte NVFP4; layouts in include/smla.h),
+// whose rows it dequantises while gathering them into shared memory.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,9 +55,73 @@ __device__ __forceinline__ void decode16_e4m3(const uint4 raw, float* dst) {
   }
 }
 
-template <bool kBf16>
+// E2M1 element values by code (OCP MX specification, FP4 E2M1: sign, two
+// exponent bits with bias 1, one mantissa bit).
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t mag = code & 7u;
+  const float v = mag < 2u ? 0.5f * (float)mag : (float)(2u + (mag & 1u)) * (float)(1u << ((mag >> 1) - 1u)) * 0.5f;
+  return (code & 8u) ? -v : v;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t byte) {
+  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(byte & 0xFFu), __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half*>(&hr.x));
+}
+
+// Packed FP8 row (584 bytes, 8-byte aligned): work item c < 56 decodes NoPE
+// dims [8c, 8c + 8) (E4M3 times 2^(e - 127) of their 64-dim block), item
+// 56 + i RoPE dims [448 + 4i, 448 + 4i + 4) (BF16).
+__device__ __forceinline__ void packed_fp8_item(const unsigned char* row, int c, float* dst) {
+  if (c < 56) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + 8 * c));
+    const float scale = ldexpf(1.0f, (int)__ldg(row + 448 + c / 8) - 127);
+    float v[16];
+    decode16_e4m3(make_uint4(raw.x, raw.y, 0u, 0u), v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[8 * c + k] = v[k] * scale;
+  } else {
+    const int i = c - 56;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row + 456 + 8 * i));
+    float v[8];
+    decode8(make_uint4(raw.x, raw.y, 0u, 0u), v, true);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[448 + 4 * i + k] = v[k];
+  }
+}
+constexpr int kPackedFp8Items = 56 + 16;
+
+// NVFP4 row (384 bytes, 16-byte aligned): work item c < 14 decodes NoPE dims
+// [32c, 32c + 32) (E2M1, low nibble first, times the E4M3 scale of their
+// 16-dim block and the row's fp32 scale), item 14 + i RoPE dims 448 + 2i,
+// 449 + 2i (BF16).
+__device__ __forceinline__ void nvfp4_item(const unsigned char* row, int c, float* dst) {
+  if (c < 14) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + 16 * c));
+    const float g = __ldg(reinterpret_cast<const float*>(row + 380));
+    const float s0 = e4m3_value(__ldg(row + 224 + 2 * c)) * g, s1 = e4m3_value(__ldg(row + 225 + 2 * c)) * g;
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t code = (w[k >> 3] >> (4 * (k & 7))) & 0xFu;
+      dst[32 * c + k] = e2m1_value(code) * (k < 16 ? s0 : s1);
+    }
+  } else {
+    const int i = c - 14;
+    const uint32_t raw = __ldg(reinterpret_cast<const uint32_t*>(row + 252 + 4 * i));
+    float v[8];
+    decode8(make_uint4(raw, 0u, 0u, 0u), v, true);
+    dst[448 + 2 * i] = v[0];
+    dst[449 + 2 * i] = v[1];
+  }
+}
+constexpr int kNvfp4Items = 14 + 32;
+
+// kKind: SMLA_BF16 / SMLA_E4M3 rows and query, or a packed KV form with a BF16 query.
+template <int kKind>
 __global__ void __launch_bounds__(kThreads)
 decode_cuda_core_kernel(const DecodeParams p) {
+  constexpr bool kBf16 = kKind != SMLA_E4M3;                          // query elements
+  constexpr bool kPacked = kKind == SMLA_PACKED_FP8 || kKind == SMLA_NVFP4;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CudaCoreSmem& sm = *reinterpret_cast<CudaCoreSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -113,8 +179,18 @@ decode_cuda_core_kernel(const DecodeParams p) {
     const int nv = sm.n_valid;
     if (nv == 0) { __syncthreads(); continue; }
 
-    // a3: gather rows (16-byte vector loads) into fp32 shared memory
-    {
+    // a3: gather rows (16-byte vector loads) into fp32 shared memory;
+    // packed rows are dequantised on the way
+    if constexpr (kPacked) {
+      constexpr int kItems = kKind == SMLA_PACKED_FP8 ? kPackedFp8Items : kNvfp4Items;
+      for (int c = tid; c < nv * kItems; c += kThreads) {
+        const int r = c / kItems, item = c % kItems;
+        const unsigned char* row =
+            reinterpret_cast<const unsigned char*>(sm.from_swa[r] ? p.swa : p.comp) + sm.row_off[r];
+        if constexpr (kKind == SMLA_PACKED_FP8) packed_fp8_item(row, item, sm.kv[r]);
+        else nvfp4_item(row, item, sm.kv[r]);
+      }
+    } else {
       constexpr int kPer = kBf16 ? 8 : 16;
       constexpr int kChunks = kHeadDim / kPer;
       for (int c = tid; c < nv * kChunks; c += kThreads) {
@@ -225,19 +301,19 @@ int cuda_core_ctas_per_split(int H) { return H / kHeadsPerCta; }
 
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int grid, cudaStream_t stream) {
   const int smem = cuda_core_smem_bytes();
-  cudaError_t e;
-  if (p.dtype == SMLA_BF16) {
-    e = cudaFuncSetAttribute(decode_cuda_core_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto launch = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_cuda_core_kernel<true><<<grid, kThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(decode_cuda_core_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_cuda_core_kernel<false><<<grid, kThreads, smem, stream>>>(p);
+    kernel<<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  };
+  switch (p.dtype) {
+    case SMLA_BF16: return launch(decode_cuda_core_kernel<SMLA_BF16>);
+    case SMLA_E4M3: return launch(decode_cuda_core_kernel<SMLA_E4M3>);
+    case SMLA_PACKED_FP8: return launch(decode_cuda_core_kernel<SMLA_PACKED_FP8>);
+    case SMLA_NVFP4: return launch(decode_cuda_core_kernel<SMLA_NVFP4>);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace smla

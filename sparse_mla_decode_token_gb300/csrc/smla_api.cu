@@ -38,13 +38,19 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-int elem_bytes(int dtype) { return dtype == SMLA_BF16 ? 2 : 1; }
+// Bytes of a query element, and of a KV row element (the packed forms count
+// their rows in bytes: row = 584 / 384 elements of one byte).
+int elem_bytes(int dtype) { return dtype == SMLA_E4M3 ? 1 : 2; }
+int kv_elem_bytes(int dtype) { return dtype == SMLA_BF16 ? 2 : 1; }
+bool packed_dtype(int dtype) { return dtype == SMLA_PACKED_FP8 || dtype == SMLA_NVFP4; }
+int64_t kv_row_elems(int dtype) { return dtype == SMLA_PACKED_FP8 ? 584 : dtype == SMLA_NVFP4 ? 384 : kHeadDim; }
+int kv_stride_align(int dtype) { return dtype == SMLA_PACKED_FP8 ? 8 : 16; }
 
 // Shape checks shared by planning and decoding.
 smla_status check_shapes(const smla_args* a) {
   if (a == nullptr) return fail(SMLA_ERR_INVALID_ARG, "args is NULL");
-  if (a->dtype != SMLA_BF16 && a->dtype != SMLA_E4M3)
-    return fail(SMLA_ERR_INVALID_ARG, "dtype %d is not SMLA_BF16 or SMLA_E4M3", a->dtype);
+  if (a->dtype != SMLA_BF16 && a->dtype != SMLA_E4M3 && !packed_dtype(a->dtype))
+    return fail(SMLA_ERR_INVALID_ARG, "dtype %d is not an smla_dtype", a->dtype);
   if (a->num_heads != 64 && a->num_heads != 128)
     return fail(SMLA_ERR_UNSUPPORTED, "num_heads %d: only 64 or 128 heads are supported", a->num_heads);
   if (a->sum_q < 0) return fail(SMLA_ERR_INVALID_ARG, "sum_q %d < 0", a->sum_q);
@@ -71,11 +77,13 @@ smla_status check_shapes(const smla_args* a) {
   if (qs < min_qs || (qs * eb) % 16 != 0)
     return fail(SMLA_ERR_INVALID_ARG, "q_stride_token %lld must be >= H*512 and a multiple of 16 bytes",
                 (long long)qs);
-  const int64_t ss = a->swa_row_stride ? a->swa_row_stride : kHeadDim;
-  const int64_t cs = a->comp_row_stride ? a->comp_row_stride : kHeadDim;
-  if (ss < kHeadDim || (ss * eb) % 16 != 0 || cs < kHeadDim || (cs * eb) % 16 != 0)
-    return fail(SMLA_ERR_INVALID_ARG, "pool row strides (%lld, %lld) must be >= 512 and multiples of 16 bytes",
-                (long long)ss, (long long)cs);
+  const int64_t row = kv_row_elems(a->dtype);
+  const int keb = kv_elem_bytes(a->dtype), kal = kv_stride_align(a->dtype);
+  const int64_t ss = a->swa_row_stride ? a->swa_row_stride : row;
+  const int64_t cs = a->comp_row_stride ? a->comp_row_stride : row;
+  if (ss < row || (ss * keb) % kal != 0 || cs < row || (cs * keb) % kal != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "pool row strides (%lld, %lld) must be >= %lld and multiples of %d bytes",
+                (long long)ss, (long long)cs, (long long)row, kal);
   const int index_cols = a->comp_block_tables ? kSwaCols : a->width;   // columns the index table holds
   const int64_t is = a->indices_row_stride ? a->indices_row_stride : index_cols;
   if (is < index_cols)
@@ -229,7 +237,9 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
-  const int kernel = a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a) : a->kernel;
+  // the packed KV forms run on the CUDA-core kernel, whatever was asked for
+  const int kernel = packed_dtype(a->dtype) ? SMLA_KERNEL_CUDA_CORE
+                     : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a) : a->kernel;
   int S = a->num_splits;
   if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED ||
       kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT) {
@@ -399,10 +409,10 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   p.q_stride_token = a->q_stride_token ? a->q_stride_token : (int64_t)a->num_heads * kHeadDim;
   p.swa = a->swa_kv;
   p.swa_rows = a->swa_rows;
-  p.swa_stride = a->swa_row_stride ? a->swa_row_stride : kHeadDim;
+  p.swa_stride = a->swa_row_stride ? a->swa_row_stride : kv_row_elems(a->dtype);
   p.comp = a->compressed_kv;
   p.comp_rows = a->comp_rows;
-  p.comp_stride = a->comp_row_stride ? a->comp_row_stride : kHeadDim;
+  p.comp_stride = a->comp_row_stride ? a->comp_row_stride : kv_row_elems(a->dtype);
   p.ind = a->sparse_indices;
   p.ind_stride = a->indices_row_stride ? a->indices_row_stride : (a->comp_block_tables ? kSwaCols : a->width);
   if (a->comp_block_tables) {

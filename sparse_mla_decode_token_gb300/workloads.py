@@ -392,12 +392,16 @@ CONFIG_NAMES = {
     4: "varlen_spec_bf16_h64",
     5: "long_splitk_fp8_b4_h128",
     6: "paged_fp8_b128_h128",
+    7: "nvfp4_decode_b128_h128",
+    8: "packed_fp8_decode_b128_h128",
 }
 
 
 def config_workload(n: int) -> Workload:
-    """Workload ``n`` (1..6); seed 1000 + n.  Workload 6 is workload 3's shape
-    with the compressed segment given as page tables."""
+    """Workload ``n`` (1..8); seed 1000 + n.  Workload 6 is workload 3's shape
+    with the compressed segment given as page tables; workloads 7 and 8 are
+    workload 3's shape with 384-byte NVFP4 and 584-byte packed FP8 KV rows
+    (BF16 query)."""
     seed = 1000 + n
     rng = np.random.default_rng(seed + 7919)
     if n == 1:
@@ -447,5 +451,13 @@ def config_workload(n: int) -> Workload:
                                    page_size=128, max_pages=16, hca_seq_lens=128 + 2048,
                                    seq_lens=rng.integers(8192, 65537, size=128), ring_len=128,
                                    topk_lens=2176)
+    if n in (7, 8):
+        # workload 3's shape (128 tokens, H=128, 128 SWA + 2048 compressed,
+        # all valid) with packed KV rows and a BF16 query
+        return make_workload(name=CONFIG_NAMES[n], seed=seed, dtype="nvfp4" if n == 7 else "packed_fp8",
+                             batch=128, q_lens=1, num_heads=128, swa_rows=128 * 128,
+                             comp_rows=262144, width=2176,
+                             seq_lens=rng.integers(8192, 65537, size=128),
+                             ring_len=128, topk_lens=2176, sinks=False)
     raise ValueError(f"no workload {n}")
 

@@ -54,6 +54,17 @@ def test_paged_parity(kernel, dtype, H, splits, page_size):
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("dtype", ["packed_fp8", "nvfp4"])
+@pytest.mark.parametrize("page_size", [16, 128])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_paged_packed_rows(dtype, page_size, splits):
+    """The page-table form with packed KV rows (CUDA-core kernel)."""
+    w = paged_case(700 + page_size + splits, dtype=dtype, H=128, page_size=page_size)
+    out, lse, plan = run_gpu(w, num_splits=splits)
+    assert plan["kernel"] == B.KERNEL_CUDA_CORE and plan["num_splits"] == splits
+    compare(w, out, lse)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("page_size", [1, 16, 24, 256])

@@ -381,6 +381,32 @@ def test_slot_split_many_units(H, splits):
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("dtype", ["packed_fp8", "nvfp4"])
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("kernel", [B.KERNEL_AUTO, B.KERNEL_TCGEN05_SLOT_SPLIT])
+def test_packed_rows_parity(dtype, H, splits, kernel):
+    """Packed KV rows (584-byte packed FP8, 384-byte NVFP4; BF16 query): the
+    CUDA-core kernel dequantises each gathered row, whatever kernel was asked
+    for; ragged tiles, masked slots, sinks and split partials."""
+    w = small_case(600 + H + splits, dtype=dtype, H=H)
+    out, lse, plan = run_gpu(w, kernel=kernel, num_splits=splits)
+    assert plan["kernel"] == B.KERNEL_CUDA_CORE
+    if splits:
+        assert plan["num_splits"] == splits
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("n", [7, 8])
+def test_packed_rows_workload_sampled(n):
+    """Workload 3's shape with NVFP4 / packed FP8 rows (the bench workloads 7
+    and 8), every 8th token against the oracle."""
+    w = W.config_workload(n)
+    out, lse, plan = run_gpu(w)
+    assert plan["kernel"] == B.KERNEL_CUDA_CORE
+    compare(w, out, lse, tokens=list(range(0, w.sum_q, 8)))
+
+
 def test_many_tokens_grid():
     """More than 65535 tokens: tokens live on grid.x, so no launch limit is hit.
 

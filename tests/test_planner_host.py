@@ -252,3 +252,41 @@ def test_device_plan_equals_the_sm_count_plan():
     for n in (1, 2, 3, 5):
         a = workload_args(n)
         assert B.smla_plan_decode(a, 0).as_dict() == B.smla_plan_decode_for_sm_count(a, sms).as_dict()
+
+
+@pytest.mark.parametrize("dtype", [B.SMLA_PACKED_FP8, B.SMLA_NVFP4])
+def test_packed_rows_plan_the_cuda_core_kernel(dtype):
+    """Packed KV rows run on the CUDA-core kernel, whatever kernel or schedule
+    was asked for (its split rule and workspace)."""
+    for kernel in (B.KERNEL_AUTO, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED,
+                   B.KERNEL_TCGEN05_SLOT_SPLIT, B.KERNEL_CUDA_CORE):
+        for schedule in (B.SCHEDULE_AUTO, B.SCHEDULE_BALANCED):
+            p = plan(args(128, 2176, dtype=dtype, kernel=kernel, schedule=schedule))
+            ref = plan(args(128, 2176, dtype=B.SMLA_BF16, kernel=B.KERNEL_CUDA_CORE))
+            assert p["kernel"] == B.KERNEL_CUDA_CORE and p["clusters"] == 0
+            assert (p["num_splits"], p["grid"], p["workspace_bytes"]) == \
+                (ref["num_splits"], ref["grid"], ref["workspace_bytes"])
+
+
+@pytest.mark.parametrize("dtype,row,align", [(B.SMLA_PACKED_FP8, 584, 8), (B.SMLA_NVFP4, 384, 16)])
+def test_packed_row_strides(dtype, row, align):
+    """Packed pools count their row strides in bytes: at least the row size
+    and a multiple of 8 (packed FP8) or 16 (NVFP4) bytes."""
+    for stride, ok in ((0, True), (row, True), (row + align, True), (row - align, False),
+                       (row + align // 2, False), (512, row <= 512)):
+        a = args(4, 256, dtype=dtype)
+        a.swa_row_stride = a.comp_row_stride = stride
+        if ok:
+            plan(a)
+        else:
+            with pytest.raises(B.SmlaError) as e:
+                plan(a)
+            assert e.value.status == B.SMLA_ERR_INVALID_ARG and "strides" in str(e.value)
+
+
+def test_unknown_dtype_is_an_error():
+    a = args(4, 256)
+    a.dtype = 4
+    with pytest.raises(B.SmlaError) as e:
+        plan(a)
+    assert e.value.status == B.SMLA_ERR_INVALID_ARG and "dtype" in str(e.value)
