@@ -540,7 +540,10 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": flops / main_s / 1e12, "peak": dtype_tf,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    if roof["bound"] == "alu":                          # no measured ALU peak: unit counts x clock
+        roof["peak_source"] = "derived: " + tensor_src
+    else:
+        roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
     roof["tensor_peak_tflops"], roof["tensor_peak_source"] = dtype_tf, tensor_src
     roof["tensor_time_us"] = 1e6 * t_tc
     roof["traffic"], roof["traffic_source"] = traffic_record(W.CONFIG_NAMES[args.config], plan.as_dict())
@@ -590,7 +593,7 @@ def main():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8],
                     help="workload (3 = FP8 decode, 128 tokens, H=128; 6 = the same with page-table "
                          "compressed segments)")
-    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    ap.add_argument("--kernel", type=int, default=0, help="smla_kernel: 0 auto, 1 CUDA-core, 2 tcgen05, 3 tcgen05 head-owned, 4 tcgen05 slot-split")
     ap.add_argument("--num-splits", type=int, default=0, help="0 = the planner's choice")
     ap.add_argument("--schedule", type=int, default=0, help="0 = auto, 1 = grid, 2 = balanced (smla_schedule)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle timing")

@@ -59,7 +59,7 @@ E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 @dataclasses.dataclass
 class Workload:
     name: str
-    dtype: str                      # "bf16" or "e4m3"
+    dtype: str                      # "bf16", "e4m3", "packed_fp8" or "nvfp4"
     batch: int
     num_heads: int
     q: np.ndarray

@@ -73,7 +73,8 @@ def expected_tc_splits(T, W_, max_splits=0, sms=GB300_SMS):
 
 def workload_args(n):
     w = W.config_workload(n)
-    dt = B.SMLA_BF16 if w.dtype == "bf16" else B.SMLA_E4M3
+    dt = {"bf16": B.SMLA_BF16, "e4m3": B.SMLA_E4M3, "packed_fp8": B.SMLA_PACKED_FP8,
+          "nvfp4": B.SMLA_NVFP4}[w.dtype]
     return args(w.sum_q, w.width, H=w.num_heads, dtype=dt, batch=w.batch,
                 varlen=w.cum_seq_lens_q is not None)
 
