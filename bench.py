@@ -46,26 +46,71 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 # ------------------------------------------------------------------ accounting
 
-def valid_slots_per_token(w) -> np.ndarray:
-    """Slots each token reads: columns below clamp(topk_lens, 0, W) that are not
-    -1 and, for SWA columns, inside the window min(128, pos + 1) (or the
-    per-row window lengths); in the page-table form the compressed columns
-    below the request's backed count hca_seq_lens[b]."""
+def active_slots(w) -> np.ndarray:
+    """[T, W] mask of the slots each token reads: columns below
+    clamp(topk_lens, 0, W) that are not -1 and, for SWA columns, inside the
+    window min(128, pos + 1) (or the per-row window lengths); in the
+    page-table form the compressed columns below the request's backed count
+    hca_seq_lens[b]."""
     T, width = w.sum_q, w.width
     n_lim = np.full(T, width) if w.topk_lens is None else np.clip(w.topk_lens, 0, width)
     q_lens = (np.full(w.batch, T // w.batch) if w.cum_seq_lens_q is None
               else np.diff(w.cum_seq_lens_q))
     pos = np.concatenate([np.arange(ql) + sl - ql for sl, ql in zip(w.seq_lens, q_lens)])
     w_swa = np.clip(pos + 1 if w.swa_topk_lens is None else w.swa_topk_lens, 0, SWA_COLS)
+    j = np.arange(width)[None, :]
     if w.paged:
         req = np.repeat(np.arange(w.batch), q_lens)
         n_lim = np.minimum(n_lim, np.maximum(SWA_COLS, w.hca_seq_lens[req]))
-        j = np.arange(SWA_COLS)[None, :]
-        swa = ((j < n_lim[:, None]) & (w.indices != -1) & (j < w_swa[:, None])).sum(axis=1)
-        return swa + np.maximum(0, n_lim - SWA_COLS)
-    j = np.arange(width)[None, :]
-    active = (j < n_lim[:, None]) & (w.indices != -1) & ((j >= SWA_COLS) | (j < w_swa[:, None]))
-    return active.sum(axis=1)
+        swa_ok = np.zeros((T, width), dtype=bool)
+        swa_ok[:, :SWA_COLS] = (w.indices[:, :SWA_COLS] != -1) & (j[:, :SWA_COLS] < w_swa[:, None])
+        return (j < n_lim[:, None]) & (swa_ok | (j >= SWA_COLS))
+    return (j < n_lim[:, None]) & (w.indices != -1) & ((j >= SWA_COLS) | (j < w_swa[:, None]))
+
+
+def valid_slots_per_token(w) -> np.ndarray:
+    """Slots each token reads (see active_slots)."""
+    return active_slots(w).sum(axis=1)
+
+
+def slot_rows(w) -> np.ndarray:
+    """[T, W] row read by each column (int64): SWA rows as given, compressed
+    rows + 2^32 (their own pool); in the page-table form the compressed rows
+    come from the page tables."""
+    T, width = w.sum_q, w.width
+    rows = np.empty((T, width), dtype=np.int64)
+    rows[:, :SWA_COLS] = w.indices[:, :SWA_COLS]
+    if w.paged:
+        c = np.arange(width - SWA_COLS)
+        pages = w.comp_block_tables[:, c // w.comp_page_size].astype(np.int64)
+        rows[:, SWA_COLS:] = pages * w.comp_page_size + c % w.comp_page_size
+    else:
+        rows[:, SWA_COLS:] = w.indices[:, SWA_COLS:]
+    rows[:, SWA_COLS:] += 1 << 32
+    return rows
+
+
+def token_pair_rows(w, num_splits: int) -> int:
+    """Rows the token-pair kernel gathers per launch.  A unit is (tokens 2u
+    and 2u + 1, split s) over the split's columns [s P, s P + P), P =
+    ceil(W / S) (in the page-table form rounded up to a multiple of 64); it
+    reads the union of the two tokens' rows there, or both lists whole when
+    either token reads some row twice."""
+    act, rows = active_slots(w), slot_rows(w)
+    T, width, S = w.sum_q, w.width, num_splits
+    per = -(-width // S)
+    if w.paged:
+        per = -(-per // 64) * 64
+    total = 0
+    for u in range(0, T, 2):
+        for s in range(S):
+            c0, c1 = min(width, s * per), min(width, s * per + per)
+            lists = [rows[t, c0:c1][act[t, c0:c1]] for t in range(u, min(u + 2, T))]
+            if any(len(np.unique(x)) < len(x) for x in lists):
+                total += sum(len(x) for x in lists)
+            else:
+                total += len(np.unique(np.concatenate(lists)))
+    return total
 
 
 def peaks():
@@ -347,6 +392,9 @@ def run_gpu(args):
                          swa_topk_lens=d_win, comp_block_tables=d_bt, comp_page_size=w.comp_page_size,
                          hca_seq_lens=d_hca, width=w.width if w.paged else None)
     plan = B.smla_plan_decode(args_c, local)
+    if plan.kernel == B.KERNEL_TCGEN05_TOKEN_PAIRS:
+        # rows that both tokens of a unit select are gathered once
+        gathered_bytes = token_pair_rows(w, plan.num_splits) * w.row_bytes
     workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     args_c.workspace, args_c.workspace_bytes = workspace.data_ptr(), workspace.numel()
     has_combine = plan.num_splits > 1

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SMLA_ABI_VERSION 7
+#define SMLA_ABI_VERSION 8
 #define SMLA_HEAD_DIM 512      /* 448 NoPE + 64 RoPE */
 #define SMLA_SWA_COLS 128      /* fixed SWA columns at the front of the index table */
 #define SMLA_MAX_SPLITS 64     /* upper bound on split-K partials per token */
@@ -91,7 +91,15 @@ typedef enum smla_dtype {
  * output half instead of partial logits.  TCGEN05_HEAD_OWNED (E4M3 rows;
  * BF16 rows take TCGEN05): each CTA runs the softmax of half the heads and
  * sends the peer their E4M3 P; slower (a round trip per tile), kept as an
- * alternative.  AUTO picks TCGEN05_SLOT_SPLIT for E4M3 rows (TCGEN05 when
+ * alternative.  TCGEN05_TOKEN_PAIRS (H = 64; H = 128 takes TCGEN05): the
+ * TCGEN05 kernel with two consecutive tokens of the flattened batch (2u,
+ * 2u + 1) per CTA pair, token 2u's heads in MMA rows 0-63 and token 2u + 1's
+ * in rows 64-127, over the union of the two tokens' selected rows: a row both
+ * tokens select (the shared SWA window of a request's consecutive tokens,
+ * shared compressed rows) is gathered once, and each head's softmax takes
+ * only its own token's slots.  When either token selects some row more than
+ * once the unit shares nothing (each slot still counts once per selection).
+ * The grid has ceil(T / 2) x S pairs.  AUTO picks TCGEN05_SLOT_SPLIT for E4M3 rows (TCGEN05 when
  * the BALANCED schedule is asked for) and TCGEN05 for BF16 rows. */
 /* Work hand-out of the TCGEN05 kernel (smla_args.schedule).  GRID: one CTA
  * pair per (token, split), the split count from num_splits / max_splits.
@@ -116,7 +124,8 @@ typedef enum smla_kernel {
   SMLA_KERNEL_CUDA_CORE = 1,          /* plain CUDA-core kernel (fp32 FMA) */
   SMLA_KERNEL_TCGEN05 = 2,            /* tcgen05 / TMEM tensor-core kernel */
   SMLA_KERNEL_TCGEN05_HEAD_OWNED = 3, /* tcgen05 kernel, softmax split between the CTAs by head */
-  SMLA_KERNEL_TCGEN05_SLOT_SPLIT = 4  /* tcgen05 kernel, each CTA of a pair takes half of every tile's slots */
+  SMLA_KERNEL_TCGEN05_SLOT_SPLIT = 4, /* tcgen05 kernel, each CTA of a pair takes half of every tile's slots */
+  SMLA_KERNEL_TCGEN05_TOKEN_PAIRS = 5 /* tcgen05 kernel, two tokens of 64 heads per CTA pair over their rows' union */
 } smla_kernel;
 
 /* Bits the kernels OR into *error_word (device-side detection, no trap). */

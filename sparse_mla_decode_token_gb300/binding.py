@@ -28,7 +28,8 @@ SMLA_OK, SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE_TOO_SMAL
 SMLA_BF16, SMLA_E4M3, SMLA_PACKED_FP8, SMLA_NVFP4 = 0, 1, 2, 3
 # bytes of one KV row of the packed forms (BF16 query; layouts in include/smla.h)
 PACKED_ROW_BYTES = {SMLA_PACKED_FP8: 584, SMLA_NVFP4: 384}
-KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED, KERNEL_TCGEN05_SLOT_SPLIT = 0, 1, 2, 3, 4
+(KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TCGEN05, KERNEL_TCGEN05_HEAD_OWNED, KERNEL_TCGEN05_SLOT_SPLIT,
+ KERNEL_TCGEN05_TOKEN_PAIRS) = 0, 1, 2, 3, 4, 5
 SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_BALANCED = 0, 1, 2
 DEVERR_INDEX_OUT_OF_RANGE = 0x1
 

@@ -103,13 +103,22 @@ struct TcSmall {
   float m_buf[2][128];                   // reference maximum after the last tile of warpgroup g
   float lsum[2][128];                    // [warpgroup][head]
   int32_t chunk_off[kMaxChunks];        // compacted-slot count of each 32-column chunk, then its offset
-  int32_t nswa;                          // valid slots in the SWA columns of the split
-  int32_t nvalid;                        // valid slots of the split
+  int32_t nswa;                          // valid slots in the SWA columns of the split (token pair: of the union)
+  int32_t nvalid;                        // valid slots of the split (token pair: of the union)
+  // token pairs only: token B's chunk counts, the chunk counts of B's rows
+  // that token A does not select, and the per-token list sizes
+  int32_t chunk_off_b[kMaxChunks];
+  int32_t only_b_chunk[kMaxChunks];
+  int32_t nswa_a, nswa_b, n_a, n_b, only_b_swa, dup;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
-template <bool kFp8>
+// kPair: a unit holds two tokens of 64 heads each (rows 0-63 of the 128-row
+// MMA tile token A, rows 64-127 token B) over the union of their selected
+// rows: the compacted list can hold both tokens' columns, and a per-tile
+// membership mask tells each row which list entries are its own.
+template <bool kFp8, bool kPair = false>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kN = kFp8 ? 64 : 32;                    // slots per tile
@@ -129,9 +138,25 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
   static constexpr int kOffX = kOffKV + kStages * kStageBytes;
+  static constexpr int kIdxCap = (kPair ? 2 : 1) * kMaxCols;  // list entries (a token pair: the union)
+  static constexpr int kMaxTiles = kIdxCap / kN + 2;           // the SWA and compressed runs may each end in a partial tile
   static constexpr int kOffIdx = kOffX + 2 * kXBytes;
-  static constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
+  static constexpr int kOffMask = kOffIdx + kIdxCap * 4;       // token pairs: uint64 masks [2][kMaxTiles]
+  static constexpr int kOffSmall = kOffMask + (kPair ? 2 * kMaxTiles * 8 : 0);
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
+  // token-pair set-up scratch, in the KV stages before the first gather: an
+  // open-addressing hash of the selected rows (keys, then per-key flags:
+  // bit 0 token A selects it, bit 1 token B), each token's compacted list,
+  // and one membership byte per union entry
+  static constexpr int kHashSlots = 8192;                      // > 2 x kMaxCols: probing always ends
+  static constexpr int kScrFlags = kHashSlots * 4;
+  static constexpr int kScrListA = 2 * kHashSlots * 4;
+  static constexpr int kScrListB = kScrListA + kMaxCols * 4;
+  static constexpr int kScrMemb = kScrListB + kMaxCols * 4;
+  static constexpr int kScrEnd = kScrMemb + kIdxCap;
+  static_assert(!kPair || kScrEnd <= kStages * kStageBytes, "token-pair scratch fits in the KV stages");
+  static_assert(kScrFlags % 16 == 0 && kScrListA % 16 == 0, "scratch arrays start on 16-byte boundaries");
+  static_assert(kHashSlots > 2 * kMaxCols && (kHashSlots & (kHashSlots - 1)) == 0, "hash table size");
   static_assert(kStages <= kMaxStages, "barrier arrays");
   static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
   static_assert(kN <= kMaxN, "row lists");
@@ -157,10 +182,11 @@ struct TcParams {
 // kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
 // epilogue stages the partial rows in shared memory for contiguous stores (a
 // separate instantiation, so that the single-split code is compiled alone).
-template <bool kFp8, bool kPartial>
+// kPair: H = 64 and a unit is (token pair, split), see Cfg.
+template <bool kFp8, bool kPartial, bool kPair>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kPair>;
   const DecodeParams& p = P.p;
   constexpr int kN = C::kN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -169,6 +195,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   unsigned char* base = smem_raw + (base_addr - raw_addr);
   TcSmall& sm = *reinterpret_cast<TcSmall*>(base + C::kOffSmall);
   int32_t* idx_s = reinterpret_cast<int32_t*>(base + C::kOffIdx);
+  uint64_t* mask_a = reinterpret_cast<uint64_t*>(base + C::kOffMask);   // token pairs: [tile] rows of token A
+  uint64_t* mask_b = mask_a + C::kMaxTiles;                             // token pairs: [tile] rows of token B
   const uint32_t q_addr = base_addr + C::kOffQ;
   const uint32_t kv_addr = base_addr + C::kOffKV;
   const uint32_t x_addr = base_addr + C::kOffX;
@@ -179,8 +207,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   const int S = p.num_splits;
   const int unit = blockIdx.x >> 1;
   const int s = unit % S;
-  const int t = unit / S;
+  const int t = kPair ? 2 * (unit / S) : unit / S;   // the token (a pair: token A; token B is t + 1)
+  const bool has_b = kPair && t + 1 < p.sum_q;       // an odd token count leaves the last pair one token
   const int H = p.H;
+  const int rows_used = kPair ? (has_b ? 128 : 64) : H;   // MMA rows that carry a head
   // Column range of this split, from the table width only (so that the index
   // loads need not wait for any device value): [c0, c0 + ceil(W / S)); in the
   // page-table form rounded up to whole 64-slot runs, so that every full tile
@@ -198,7 +228,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 
   // ---------------------------------------------------------------- set-up
   // Q first: its copies need nothing but (t, rank)
-  {
+  if constexpr (!kPair) {
     const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
                               ((int64_t)t * p.q_stride_token + (int64_t)rank * kHalfDims) * C::kElem;
     for (int c = tid; c < H * C::kChunks; c += kThreads) {
@@ -206,123 +236,157 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7),
                   qb + (int64_t)h * kHeadDim * C::kElem + cc * 16);
     }
+  } else {
+    // MMA row h: head h & 63 of token t + (h >> 6)
+    for (int c = tid; c < rows_used * C::kChunks; c += kThreads) {
+      const int h = c / C::kChunks, cc = c % C::kChunks;
+      const unsigned char* qb = reinterpret_cast<const unsigned char*>(p.q) +
+                                ((int64_t)(t + (h >> 6)) * p.q_stride_token + (int64_t)(h & 63) * kHeadDim +
+                                 (int64_t)rank * kHalfDims) * C::kElem;
+      cp_async_16(q_addr + (cc >> 3) * C::kRegionQ + sw128_offset(h, cc & 7), qb + cc * 16);
+    }
   }
   // the split's index columns, in flight together with the token metadata loads
   const int nchunks = (c1 - c0 + 31) / 32;
-  const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+  auto load_cols = [&](int tok, int32_t (&r)[kChunksPerWarp]) {
+    const int32_t* irow = p.ind + (int64_t)tok * p.ind_stride;
+    if (p.bt == nullptr) {             // index form (a loop of its own: the FP8 code keeps its registers)
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int col = c0 + (warp + q * kWarps) * 32 + lane;
+        r[q] = (col < c1) ? __ldg(irow + col) : -1;
+      }
+    } else {                           // page-table form: compressed rows from the page table
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int col = c0 + (warp + q * kWarps) * 32 + lane;
+        r[q] = -1;
+        if (col < c1) r[q] = col >= kSwaCols ? paged_row(p, tok, col - kSwaCols) : __ldg(irow + col);
+      }
+    }
+  };
   int32_t rv[kChunksPerWarp];
-  if (p.bt == nullptr) {             // index form (a loop of its own: the FP8 code keeps its registers)
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = (col < c1) ? __ldg(irow + col) : -1;
-    }
-  } else {                           // page-table form: compressed rows from the page table
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = -1;
-      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
-    }
-  }
+  int32_t rvb[kChunksPerWarp];         // token pairs: token B's columns (unused otherwise)
+  load_cols(t, rv);
+  if (has_b) load_cols(t + 1, rvb);
   const TokenInfo ti = token_info(p, t);
-  c1 = min(c1, max(c0, ti.n_lim));    // active columns of the split
-  {
-    // zero the KV stages (rows past a tile's slot count then hold finite data)
-    // and the Q rows of absent heads
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
-    const int zn = C::kStages * C::kStageBytes / 16;
-    for (int i = tid; i < zn; i += kThreads) zp[i] = z;
-    if (H < 128) {
-      for (int kb = 0; kb < C::kRegions; ++kb) {
-        uint4* qz = reinterpret_cast<uint4*>(base + C::kOffQ + kb * C::kRegionQ + H * 128);
-        for (int i = tid; i < (128 - H) * 8; i += kThreads) qz[i] = z;
-      }
+  const int c1a = min(c1, max(c0, ti.n_lim));    // active columns of the split
+  int c1b = c0, w_swa_b = 0;
+  if (has_b) {
+    const TokenInfo tib = token_info(p, t + 1);
+    c1b = min(c1, max(c0, tib.n_lim));
+    w_swa_b = tib.w_swa;
+  }
+  // a2 for one loaded column: the row, or -1 when the slot is masked (an
+  // index < -1 or past the pool is masked and flagged)
+  auto check_slot = [&](int idx, int col, int c1t, int w_swa) -> int {
+    if (col >= c1t) return -1;
+    const bool swa = col < kSwaCols;
+    if (idx == -1 || (swa && col >= w_swa)) return -1;
+    const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+    if (idx < 0 || (int64_t)idx >= nrows) {
+      if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+      return -1;
     }
-    if (tid == 0) {
-      for (int i = 0; i < C::kStages; ++i) {
-        mbar_init(bar(sm.kv_full[i]), 1);
-        mbar_init(bar(sm.kv_empty[i]), 1);
-      }
-      for (int b = 0; b < 2; ++b) {
-
-        mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
-        mbar_init(bar(sm.p_empty[b]), 1);
-        mbar_init(bar(sm.xin_full[b]), 1);
-        mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps / 2);
-        mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
-      }
-      mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
-      for (int b = 0; b < kSBufs; ++b) {
-        mbar_init(bar(sm.s_full[b]), 1);
-        mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
-      }
-      mbar_init(bar(sm.o_full), 1);
-      mbar_init(bar(sm.qk0_done), 1);
-      mbar_init(bar(sm.qk_done), kQkWarps);
-      sm.abort_flag = 0;
-      sm.nswa = 0;
-      fence_mbar_init_cluster();
-    }
-    __syncthreads();
-    // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
-    // slots first, then valid compressed slots, each in column order
+    return idx;
+  };
+  // per-chunk valid counts of this warp's chunks (k = warp + q * kWarps) and
+  // the valid SWA slots, for one token's loaded columns (valid rows stay in r)
+  auto count_chunks = [&](int32_t (&r)[kChunksPerWarp], int c1t, int w_swa, int32_t* cnt, int32_t* nswa_out) {
 #pragma unroll
     for (int q = 0; q < kChunksPerWarp; ++q) {
       const int k = warp + q * kWarps;
       if (k < nchunks) {
         const int col = c0 + k * 32 + lane;
-        const int idx = rv[q];
-        rv[q] = -1;
-        if (col < c1) {
-          const bool swa = col < kSwaCols;
-          bool ok = idx != -1 && (!swa || col < ti.w_swa);
-          if (ok) {
-            const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
-            if (idx < 0 || (int64_t)idx >= nrows) {
-              ok = false;
-              if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
-            }
-          }
-          if (ok) rv[q] = idx;
-        }
-        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
+        r[q] = check_slot(r[q], col, c1t, w_swa);
+        const unsigned ball = __ballot_sync(0xffffffffu, r[q] >= 0);
+        const unsigned ball_swa = __ballot_sync(0xffffffffu, r[q] >= 0 && col < kSwaCols);
         if (lane == 0) {
-          sm.chunk_off[k] = __popc(ball);
-          if (ball_swa) atomicAdd(&sm.nswa, __popc(ball_swa));
+          cnt[k] = __popc(ball);
+          if (ball_swa) atomicAdd(nswa_out, __popc(ball_swa));
         }
       }
+    }
+  };
+  // every warp scans the chunk counts itself (at most kMaxChunks = 72, three
+  // shuffle scans), which saves a serialised scan and a block barrier:
+  // chunk_base[q] = entries before chunk warp + q * kWarps; returns the total
+  auto scan_chunks = [&](const int32_t* cnt, int nch, int (&chunk_base)[kChunksPerWarp]) -> int {
+    int carry = 0;
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
+    for (int base0 = 0; base0 < nch; base0 += 32) {
+      const int k = base0 + lane;
+      const int v = k < nch ? cnt[k] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      // exclusive prefix of this warp's chunks k = warp + q * kWarps in this group of 32
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int kq = warp + q * kWarps;
+        const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
+        if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return carry;
+  };
+  auto init_barriers = [&]() {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(bar(sm.kv_full[i]), 1);
+      mbar_init(bar(sm.kv_empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(sm.p_full[b]), kSoftmaxWarps / 2);
+      mbar_init(bar(sm.p_empty[b]), 1);
+      mbar_init(bar(sm.xin_full[b]), 1);
+      mbar_init(bar(sm.xout_free[b]), kSoftmaxWarps / 2);
+      mbar_init(bar(sm.m_ready[b]), kSoftmaxWarps / 2);
+    }
+    mbar_init(bar(sm.lsum_full), kSoftmaxWarps);
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(bar(sm.s_full[b]), 1);
+      mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
+    }
+    mbar_init(bar(sm.o_full), 1);
+    mbar_init(bar(sm.qk0_done), 1);
+    mbar_init(bar(sm.qk_done), kQkWarps);
+    sm.abort_flag = 0;
+    sm.nswa = 0;
+  };
+  auto zero_kv_stages = [&]() {
+    // rows past a tile's slot count then hold finite data
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    uint4* zp = reinterpret_cast<uint4*>(base + C::kOffKV);
+    const int zn = C::kStages * C::kStageBytes / 16;
+    for (int i = tid; i < zn; i += kThreads) zp[i] = z;
+  };
+  auto zero_q_rows = [&](int from) {   // Q rows [from, 128) carry no head
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int kb = 0; kb < C::kRegions; ++kb) {
+      uint4* qz = reinterpret_cast<uint4*>(base + C::kOffQ + kb * C::kRegionQ + from * 128);
+      for (int i = tid; i < (128 - from) * 8; i += kThreads) qz[i] = z;
+    }
+  };
+  if constexpr (!kPair) {
+    zero_kv_stages();
+    if (H < 128) zero_q_rows(H);
+    if (tid == 0) {
+      init_barriers();
+      fence_mbar_init_cluster();
     }
     __syncthreads();
-    // every warp scans the chunk counts itself (at most kMaxChunks = 72, three
-    // shuffle scans), which saves a serialised scan and a block barrier
+    // a2: compaction of the split's columns [c0, c1) into idx_s: valid SWA
+    // slots first, then valid compressed slots, each in column order
+    count_chunks(rv, c1a, ti.w_swa, sm.chunk_off, &sm.nswa);
+    __syncthreads();
     int chunk_base[kChunksPerWarp];
-    {
-      int carry = 0;
-#pragma unroll
-      for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
-      for (int base0 = 0; base0 < nchunks; base0 += 32) {
-        const int k = base0 + lane;
-        const int v = k < nchunks ? sm.chunk_off[k] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += u;
-        }
-        // exclusive prefix of this warp's chunks k = warp + q * kWarps in this group of 32
-#pragma unroll
-        for (int q = 0; q < kChunksPerWarp; ++q) {
-          const int kq = warp + q * kWarps;
-          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
-          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
-        }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (warp == 0 && lane == 0) sm.nvalid = carry;
-    }
+    const int total = scan_chunks(sm.chunk_off, nchunks, chunk_base);
+    if (warp == 0 && lane == 0) sm.nvalid = total;
 #pragma unroll
     for (int q = 0; q < kChunksPerWarp; ++q) {
       const int k = warp + q * kWarps;
@@ -331,6 +395,184 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
       }
     }
+  } else {
+    // f1, the rows shared by a pair's tokens gathered once.  Each token's
+    // valid slots are compacted as above; a hash of (pool, row) keys marks
+    // which token selects each row; the union list is token A's list with
+    // B's rows that A does not select inserted after A's SWA and compressed
+    // runs, in B's order:
+    //   [A SWA] [B-only SWA] [A compressed] [B-only compressed]
+    // A row that either token selects more than once counts once per slot in
+    // that token's softmax, which a shared entry cannot express: then the
+    // union is the plain concatenation of the two lists (nothing shared).
+    // The construction is deterministic, so both CTAs of the pair build the
+    // same list (the hash slots may differ; the flags read back do not).
+    uint32_t* hkeys = reinterpret_cast<uint32_t*>(base + C::kOffKV);
+    uint32_t* hflags = reinterpret_cast<uint32_t*>(base + C::kOffKV + C::kScrFlags);
+    int32_t* list_a = reinterpret_cast<int32_t*>(base + C::kOffKV + C::kScrListA);
+    int32_t* list_b = reinterpret_cast<int32_t*>(base + C::kOffKV + C::kScrListB);
+    uint8_t* memb = base + C::kOffKV + C::kScrMemb;
+    constexpr uint32_t kEmpty = 0xffffffffu;
+    auto hkey = [](int row, bool comp) { return (uint32_t)row | (comp ? 0x80000000u : 0u); };
+    auto hslot = [](uint32_t key) { return (key * 2654435761u) >> 19; };     // 13 bits: kHashSlots
+    static_assert(C::kHashSlots == 1 << 13, "hash index width");
+    auto insert = [&](uint32_t key, uint32_t flag) {
+      if (key == kEmpty) {                // (comp row 2^31 - 1) would read as empty: share nothing
+        sm.dup = 1;
+        return;
+      }
+      uint32_t h = hslot(key);
+      for (int probe = 0; probe < C::kHashSlots; ++probe) {
+        const uint32_t prev = atomicCAS(hkeys + h, kEmpty, key);
+        if (prev == kEmpty || prev == key) {
+          if (atomicOr(hflags + h, flag) & flag) sm.dup = 1;    // this token selects the row twice
+          return;
+        }
+        h = (h + 1) & (C::kHashSlots - 1);
+      }
+      sm.dup = 1;                          // not reached: the table has more slots than keys
+    };
+    auto flags_of = [&](uint32_t key) -> uint32_t {
+      uint32_t h = hslot(key);
+      for (int probe = 0; probe < C::kHashSlots; ++probe) {
+        const uint32_t k = hkeys[h];
+        if (k == key) return hflags[h];
+        if (k == kEmpty) return 0u;
+        h = (h + 1) & (C::kHashSlots - 1);
+      }
+      return 0u;
+    };
+    {
+      const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), z = make_uint4(0, 0, 0, 0);
+      uint4* kp = reinterpret_cast<uint4*>(hkeys);
+      uint4* fp = reinterpret_cast<uint4*>(hflags);
+      for (int i = tid; i < C::kHashSlots / 4; i += kThreads) {
+        kp[i] = e4;
+        fp[i] = z;
+      }
+      for (int i = tid; i < 2 * C::kMaxTiles; i += kThreads) mask_a[i] = 0ull;
+    }
+    if (!has_b) zero_q_rows(64);
+    if (tid == 0) {
+      init_barriers();
+      sm.nswa_a = sm.nswa_b = sm.only_b_swa = sm.dup = 0;
+      fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    count_chunks(rv, c1a, ti.w_swa, sm.chunk_off, &sm.nswa_a);
+    if (has_b) count_chunks(rvb, c1b, w_swa_b, sm.chunk_off_b, &sm.nswa_b);
+    __syncthreads();
+    const int nswa_a = sm.nswa_a, nswa_b = sm.nswa_b;
+    {
+      int chunk_base[kChunksPerWarp];
+      const int n_a = scan_chunks(sm.chunk_off, nchunks, chunk_base);
+      if (warp == 0 && lane == 0) sm.n_a = n_a;
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int k = warp + q * kWarps;
+        if (k < nchunks) {
+          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+          if (rv[q] >= 0) {
+            const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
+            list_a[e] = rv[q];
+            insert(hkey(rv[q], e >= nswa_a), 1u);
+          }
+        }
+      }
+      int n_b = 0;
+      if (has_b) {
+        n_b = scan_chunks(sm.chunk_off_b, nchunks, chunk_base);
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int k = warp + q * kWarps;
+          if (k < nchunks) {
+            const unsigned ball = __ballot_sync(0xffffffffu, rvb[q] >= 0);
+            if (rvb[q] >= 0) {
+              const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
+              list_b[e] = rvb[q];
+              insert(hkey(rvb[q], e >= nswa_b), 2u);
+            }
+          }
+        }
+      }
+      if (warp == 0 && lane == 0) sm.n_b = n_b;
+    }
+    __syncthreads();
+    const int n_a = sm.n_a, n_b = sm.n_b;
+    const bool dup = sm.dup != 0;
+    // B's entries that A does not select, counted per 32-entry chunk of B's list
+    const int nch_b = (n_b + 31) / 32;
+    unsigned only_b[kChunksPerWarp];
+#pragma unroll
+    for (int q = 0; q < kChunksPerWarp; ++q) {
+      const int k = warp + q * kWarps;
+      only_b[q] = 0u;
+      if (k < nch_b) {
+        const int i = k * 32 + lane;
+        const bool ob = i < n_b && (dup || !(flags_of(hkey(list_b[i], i >= nswa_b)) & 1u));
+        only_b[q] = __ballot_sync(0xffffffffu, ob);
+        const unsigned ob_swa = __ballot_sync(0xffffffffu, ob && i < nswa_b);
+        if (lane == 0) {
+          sm.only_b_chunk[k] = __popc(only_b[q]);
+          if (ob_swa) atomicAdd(&sm.only_b_swa, __popc(ob_swa));
+        }
+      }
+    }
+    __syncthreads();
+    const int bs = sm.only_b_swa;          // B-only SWA entries (they come first in B's order)
+    const int nswa_u = nswa_a + bs;
+    {
+      int chunk_base[kChunksPerWarp];
+      const int n_only = scan_chunks(sm.only_b_chunk, nch_b, chunk_base);
+      if (warp == 0 && lane == 0) {
+        sm.nswa = nswa_u;
+        sm.nvalid = n_a + n_only;
+      }
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int k = warp + q * kWarps;
+        if (k < nch_b && ((only_b[q] >> lane) & 1u)) {
+          const int r = chunk_base[q] + __popc(only_b[q] & ((1u << lane) - 1u));
+          const int e = r < bs ? nswa_a + r : nswa_u + (n_a - nswa_a) + (r - bs);
+          idx_s[e] = list_b[k * 32 + lane];
+          memb[e] = 2;
+        }
+      }
+      for (int i = tid; i < n_a; i += kThreads) {
+        const int row = list_a[i];
+        const bool comp = i >= nswa_a;
+        const int e = comp ? nswa_u + (i - nswa_a) : i;
+        idx_s[e] = row;
+        memb[e] = (uint8_t)(1u | ((!dup && (flags_of(hkey(row, comp)) & 2u)) ? 2u : 0u));
+      }
+    }
+    __syncthreads();
+    {
+      // per-tile membership masks (bit i: entry i of the tile)
+      const int nswa_t = sm.nswa, nvalid_t = sm.nvalid;
+      const int tswa_t = (nswa_t + kN - 1) / kN;
+      const int ntiles_t = tswa_t + (nvalid_t - nswa_t + kN - 1) / kN;
+      for (int j = warp; j < ntiles_t; j += kWarps) {
+        const int start = j < tswa_t ? j * kN : nswa_t + (j - tswa_t) * kN;
+        const int n = min(kN, (j < tswa_t ? nswa_t : nvalid_t) - start);
+        uint64_t ma = 0ull, mb = 0ull;
+#pragma unroll
+        for (int hb = 0; hb < kN / 32; ++hb) {
+          const int i = hb * 32 + lane;
+          const uint32_t m = i < n ? memb[start + i] : 0u;
+          ma |= (uint64_t)__ballot_sync(0xffffffffu, (m & 1u) != 0u) << (32 * hb);
+          mb |= (uint64_t)__ballot_sync(0xffffffffu, (m & 2u) != 0u) << (32 * hb);
+        }
+        if (lane == 0) {
+          mask_a[j] = ma;
+          mask_b[j] = mb;
+        }
+      }
+    }
+    __syncthreads();                     // the scratch in the KV stages is dead
+    zero_kv_stages();
+  }
+  {
     if (warp == kMmaWarp) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
     // Q is read by the tensor core (async proxy): every thread waits for its
     // own Q copies and fences them into the async proxy before the barrier,
@@ -477,12 +719,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // exponentials overlap the other's loads and exchange.
     const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
-    const int h = q4 * 32 + lane;
-    const bool active = q4 * 32 < H;                   // warp-uniform
+    const int h = q4 * 32 + lane;                      // MMA row (a token pair: head h & 63 of token t + (h >> 6))
+    const bool active = q4 * 32 < rows_used;           // warp-uniform
     const bool leader = (warp - kSoftmaxWarp0) % 4 == 0 && lane == 0;   // one thread per warpgroup
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
-    const uint32_t xbytes = (uint32_t)(H * kN * 3);    // bytes the peer pushes per tile (24-bit logits)
+    const uint32_t xbytes = (uint32_t)(rows_used * kN * 3);   // bytes the peer pushes per tile (24-bit logits)
+    const uint64_t* my_mask = (h < 64) ? mask_a : mask_b;     // token pairs: this row's entries of each tile
     constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
     const uint32_t x_mine = x_addr + g * C::kXBytes;
     const uint32_t x_peer = map_to_rank(x_mine, peer);
@@ -583,7 +826,13 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           }
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (n_cur >= kN) {
+        if constexpr (kPair) {
+          // only the entries of this row's token (the tile's other entries are the other token's)
+          const uint64_t mrow = my_mask[j];
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if ((mrow >> i) & 1ull) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        } else if (n_cur >= kN) {
 #pragma unroll
           for (int i = 0; i < kN; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
         } else {
@@ -627,7 +876,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           sv[i] = fast_exp2(x0);
           sv[i + 1] = fast_exp2(x1);
         }
-        if (n_cur < kN) {
+        if constexpr (kPair) {
+          const uint64_t mrow = my_mask[j];
+#pragma unroll
+          for (int i = 0; i < kN; ++i)
+            if (!((mrow >> i) & 1ull)) sv[i] = 0.f;
+        } else if (n_cur < kN) {
 #pragma unroll
           for (int i = 0; i < kN; ++i)
             if (i >= n_cur) sv[i] = 0.f;
@@ -699,9 +953,9 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       float f = have ? 1.f / l_tot : 0.f;
       if (S == 1) {
         f *= load_scale(p.bmm2, p.bmm2_dev);
-        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
+        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + (kPair ? (h & 63) : h)) * kLog2e - lse));
       }
-      const int64_t row_th = (int64_t)t * H + h;
+      const int64_t row_th = kPair ? (int64_t)(t + (h >> 6)) * H + (h & 63) : (int64_t)t * H + h;
       if constexpr (!kPartial) {
 #pragma unroll 1
       for (int cc = 0; cc < kHalfDims / 64; ++cc) {
@@ -769,9 +1023,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       const int w4 = (warp - kSoftmaxWarp0) & 3;
       const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
       const int c = lane & 15;
-      for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
+      for (int r = w4 + 4 * (lane >> 4); r < rows_used; r += 8) {
         const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((c ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + c * 8) = x;
+        const int64_t row = kPair ? (int64_t)(t + (r >> 6)) * H + (r & 63) : (int64_t)t * H + r;
+        *reinterpret_cast<uint4*>(p.part_o + (row * S + s) * kHeadDim + col0 + c * 8) = x;
       }
     }
   }
@@ -791,10 +1046,14 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 
 }  // namespace
 
-int tc_grid_smem_bytes(int dtype) { return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes; }
+int tc_grid_smem_bytes(int dtype, bool pair) {
+  if (pair) return dtype == SMLA_BF16 ? Cfg<false, true>::kSmemBytes : Cfg<true, true>::kSmemBytes;
+  return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes;
+}
 int tc_grid_threads() { return kThreads; }
 
-cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cudaStream_t stream) {
+  if (pair && p.H != 64) return cudaErrorInvalidValue;   // two tokens of 64 heads fill the 128 MMA rows
   TcParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
@@ -807,7 +1066,7 @@ cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t 
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_swa_run, p.swa, p.swa_rows, p.swa_stride, p.dtype, swa_run);
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp_run, p.comp, p.comp_rows, p.comp_stride, p.dtype, comp_run);
   if (e != cudaSuccess) return e;
-  const int smem = tc_grid_smem_bytes(p.dtype);
+  const int smem = tc_grid_smem_bytes(p.dtype, pair);
   auto launch = [&](auto kernel) -> cudaError_t {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -815,10 +1074,16 @@ cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t 
     return cudaSuccess;
   };
   const bool partial = p.num_splits > 1;
-  if (p.dtype == SMLA_BF16)
-    e = partial ? launch(decode_tc_kernel<false, true>) : launch(decode_tc_kernel<false, false>);
-  else
-    e = partial ? launch(decode_tc_kernel<true, true>) : launch(decode_tc_kernel<true, false>);
+  if (pair) {
+    if (p.dtype == SMLA_BF16)
+      e = partial ? launch(decode_tc_kernel<false, true, true>) : launch(decode_tc_kernel<false, false, true>);
+    else
+      e = partial ? launch(decode_tc_kernel<true, true, true>) : launch(decode_tc_kernel<true, false, true>);
+  } else if (p.dtype == SMLA_BF16) {
+    e = partial ? launch(decode_tc_kernel<false, true, false>) : launch(decode_tc_kernel<false, false, false>);
+  } else {
+    e = partial ? launch(decode_tc_kernel<true, true, false>) : launch(decode_tc_kernel<true, false, false>);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -14,10 +14,12 @@ cudaError_t launch_decode_cuda_core(const DecodeParams& p, int grid, cudaStream_
 smla_status record_error(smla_status st, const char* msg);
 
 // tcgen05 decode kernel, grid schedule (decode_tc_grid.cu): a 2-CTA cluster
-// per (token, split) of at most SMLA_TC_MAX_SPLIT_COLS columns.
-int tc_grid_smem_bytes(int dtype);
+// per (token, split) of at most SMLA_TC_MAX_SPLIT_COLS columns; pair = true
+// (H = 64 only): per (token pair, split), grid = 2 ceil(T / 2) S, the two
+// tokens' heads in one 128-row MMA tile over the union of their rows.
+int tc_grid_smem_bytes(int dtype, bool pair);
 int tc_grid_threads();
-cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cudaStream_t stream);
 
 // tcgen05 decode kernel, balanced schedule (decode_tcgen05.cu): 2-CTA clusters working through
 // units of at most SMLA_TC_MAX_SPLIT_COLS index columns of one token, at most

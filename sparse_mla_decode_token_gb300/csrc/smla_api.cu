@@ -67,7 +67,8 @@ smla_status check_shapes(const smla_args* a) {
   if (a->schedule < SMLA_SCHEDULE_AUTO || a->schedule > SMLA_SCHEDULE_BALANCED)
     return fail(SMLA_ERR_INVALID_ARG, "schedule %d is not an smla_schedule", a->schedule);
   if (a->kernel != SMLA_KERNEL_AUTO && a->kernel != SMLA_KERNEL_CUDA_CORE && a->kernel != SMLA_KERNEL_TCGEN05 &&
-      a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->kernel != SMLA_KERNEL_TCGEN05_SLOT_SPLIT)
+      a->kernel != SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->kernel != SMLA_KERNEL_TCGEN05_SLOT_SPLIT &&
+      a->kernel != SMLA_KERNEL_TCGEN05_TOKEN_PAIRS)
     return fail(SMLA_ERR_INVALID_ARG, "kernel %d is not a smla_kernel", a->kernel);
   if (a->swa_rows < 0 || a->comp_rows < 0)
     return fail(SMLA_ERR_INVALID_ARG, "negative pool row count");
@@ -241,21 +242,27 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   const int kernel = packed_dtype(a->dtype) ? SMLA_KERNEL_CUDA_CORE
                      : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a) : a->kernel;
   int S = a->num_splits;
+  // token units of the grid: tokens, or token pairs for the token-pair kernel
+  int64_t units = a->sum_q;
   if (kernel == SMLA_KERNEL_TCGEN05 || kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED ||
-      kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT) {
-    // 2-CTA clusters: balanced mode, else one cluster per (token, split).
-    // The head-owned and slot-split forms are E4M3 only (BF16 takes the
-    // dims-split kernel) and run the grid schedule.
+      kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT || kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS) {
+    // 2-CTA clusters: balanced mode, else one cluster per (token, split) or
+    // (token pair, split).  The head-owned and slot-split forms are E4M3 only
+    // (BF16 takes the dims-split kernel), the token-pair form H = 64 only
+    // (H = 128 takes the dims-split kernel); all three run the grid schedule.
     const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
     const bool slot_split = kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT && a->dtype == SMLA_E4M3;
-    plan->kernel = head_owned   ? SMLA_KERNEL_TCGEN05_HEAD_OWNED
-                   : slot_split ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
-                                : SMLA_KERNEL_TCGEN05;
+    const bool pairs_of_tokens = kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS && a->num_heads == 64;
+    plan->kernel = head_owned        ? SMLA_KERNEL_TCGEN05_HEAD_OWNED
+                   : slot_split      ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
+                   : pairs_of_tokens ? SMLA_KERNEL_TCGEN05_TOKEN_PAIRS
+                                     : SMLA_KERNEL_TCGEN05;
+    if (pairs_of_tokens) units = (a->sum_q + 1) / 2;
     plan->ctas_per_split = 2;
     plan->threads = head_owned ? tc_head_owned_threads() : slot_split ? tc_slot_threads() : tc_grid_threads();
     plan->smem_bytes = head_owned   ? tc_head_owned_smem_bytes()
                        : slot_split ? tc_slot_smem_bytes()
-                                    : tc_grid_smem_bytes(a->dtype);
+                                    : tc_grid_smem_bytes(a->dtype, pairs_of_tokens);
     const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
     if (s_min > SMLA_MAX_SPLITS)
       return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
@@ -265,6 +272,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
     const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
     if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned && !slot_split &&
+        !pairs_of_tokens &&
         a->width <= SMLA_TC_MAX_SPLIT_COLS && a->sum_q <= (int64_t)(SMLA_TC_MAX_UNITS - 2) * pairs) {
       // Balanced mode: P clusters, one per SM pair, take equal shares of the
       // T x W columns, each share at least 64 columns.  A share of at most
@@ -293,8 +301,9 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     if (S == 0) {
       // as many splits as keep every cluster in one wave (a second, partial
       // wave costs a whole unit of time for a few clusters)
-      int64_t want = a->sum_q > 0 ? pairs / a->sum_q : 1;
-      const int64_t by_width = (a->width + 63) / 64;    // keep >= 64 columns per split
+      int64_t want = units > 0 ? pairs / units : 1;
+      // keep >= 64 columns per split (a token pair's split reads up to twice the columns)
+      const int64_t by_width = ((pairs_of_tokens ? 2 : 1) * (int64_t)a->width + 63) / 64;
       if (want > by_width) want = by_width;
       if (want > max_splits) want = max_splits;
       if (want < s_min) want = s_min;
@@ -317,7 +326,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     }
   }
   plan->num_splits = S;
-  const int64_t grid = (int64_t)a->sum_q * S * plan->ctas_per_split;
+  const int64_t grid = units * S * plan->ctas_per_split;
   if (grid > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "grid of %lld CTAs is too large", (long long)grid);
   plan->grid = (int32_t)grid;
   if (S > 1) {
@@ -468,8 +477,8 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
     ce = launch_decode_tc_slot(p, plan.grid, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05 && plan.clusters > 0)
     ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, piece_cnt, stream);
-  else if (plan.kernel == SMLA_KERNEL_TCGEN05)
-    ce = launch_decode_tc_grid(p, plan.grid, stream);
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05 || plan.kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS)
+    ce = launch_decode_tc_grid(p, plan.grid, plan.kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS, stream);
   else
     ce = launch_decode_cuda_core(p, plan.grid, stream);
   if (ce != cudaSuccess) return fail(SMLA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));

@@ -128,3 +128,64 @@ def test_fp8_tensor_peak_comes_from_the_measured_record(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     tf, src = bench.fp8_tensor_peak(1000.0)
     assert tf == 2000.0 and "nominal" in src
+
+
+def oracle_union_rows(w, S):
+    """Brute force from the oracle's slot lists: per (token pair, split) the
+    distinct (pool, row) pairs, or every slot when a token reads a row twice."""
+    per = -(-w.width // S)
+    if w.paged:
+        per = -(-per // 64) * 64
+    slots = [orc.valid_slots(
+        t, indices=w.indices, topk_lens=w.topk_lens, seq_lens=w.seq_lens,
+        cum_seq_lens_q=w.cum_seq_lens_q, batch=w.batch, swa_rows=w.swa_kv.shape[0],
+        comp_rows=w.comp_kv.shape[0], width=w.width, swa_topk_lens=w.swa_topk_lens,
+        comp_block_tables=w.comp_block_tables, comp_page_size=w.comp_page_size,
+        hca_seq_lens=w.hca_seq_lens, invalid_index="mask") for t in range(w.sum_q)]
+    total = 0
+    for u in range(0, w.sum_q, 2):
+        for s in range(S):
+            lists = [[(p, r) for (j, p, r) in slots[t] if s * per <= j < s * per + per]
+                     for t in range(u, min(u + 2, w.sum_q))]
+            if any(len(set(x)) < len(x) for x in lists):
+                total += sum(len(x) for x in lists)
+            else:
+                total += len(set(lists[0]) | (set(lists[1]) if len(lists) > 1 else set()))
+    return total
+
+
+@pytest.mark.parametrize("S", [1, 2, 3])
+def test_token_pair_rows_match_the_oracle_slot_lists(S):
+    """Rows the token-pair kernel gathers (bench accounting) = brute-force
+    unions of the oracle's slot lists: shared SWA windows of a request's
+    consecutive tokens, copied and shuffled compressed rows, a row read twice,
+    equal row numbers in the two pools, an odd token count."""
+    rng = np.random.default_rng(5)
+    w = W.make_workload(seed=5, dtype="bf16", batch=4, q_lens=[2, 3, 1, 3], num_heads=64,
+                        swa_rows=4 * 128 + 64, comp_rows=1024, width=128 + 200,
+                        seq_lens=[3000, 60, 4000, 5000], ring_len=128,
+                        topk_lens=rng.integers(100, 329, size=9), varlen=True)
+    w.indices[1, 128:] = w.indices[0, 128:]
+    w.indices[3, 128:] = rng.permutation(w.indices[2, 128:])
+    w.indices[5, 128:228] = w.indices[4, :100]            # SWA row numbers in compressed columns
+    w.indices[6, 130] = w.indices[6, 131]                 # a row read twice
+    got = bench.token_pair_rows(w, S)
+    assert got == oracle_union_rows(w, S)
+    assert got < bench.valid_slots_per_token(w).sum()
+
+
+def test_token_pair_rows_page_table_form():
+    w = W.make_paged_workload(seed=3, dtype="bf16", batch=3, q_lens=[2, 3, 2], num_heads=64,
+                              swa_rows=3 * 130 + 10, comp_pages=32, page_size=16, max_pages=20,
+                              hca_seq_lens=[128 + 300, 100, 128 + 17], seq_lens=[5000, 90, 3000],
+                              ring_len=130, topk_lens=[200, 140, 450, 129, 300, 300, 180],
+                              swa_topk_lens=[0, 128, 64, 128, 100, 128, 128], varlen=True)
+    for S in (1, 2):
+        assert bench.token_pair_rows(w, S) == oracle_union_rows(w, S)
+
+
+def test_workload_4_token_pairs_gather_fewer_rows():
+    """The varlen workload (64 requests of 1-4 tokens, H = 64): pairs of a
+    request's consecutive tokens share their SWA window."""
+    w = W.config_workload(4)
+    assert bench.token_pair_rows(w, 1) < bench.valid_slots_per_token(w).sum()

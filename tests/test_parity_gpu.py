@@ -16,7 +16,8 @@ from gpu_helpers import compare, device_inputs, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED, B.KERNEL_TCGEN05_SLOT_SPLIT]
+KERNELS = [B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED, B.KERNEL_TCGEN05_SLOT_SPLIT,
+           B.KERNEL_TCGEN05_TOKEN_PAIRS]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -156,6 +156,34 @@ def test_slot_split_form_is_the_e4m3_default():
     assert bf["kernel"] == B.KERNEL_TCGEN05
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 75, 151, 152, 153, 301, 1000])
+@pytest.mark.parametrize("W_", [128, 640, 2304, 2305, 16512])
+@pytest.mark.parametrize("dtype", [B.SMLA_BF16, B.SMLA_E4M3])
+def test_token_pair_plan_rule(T, W_, dtype):
+    """The token-pair form: ceil(T / 2) units of two tokens, split by the
+    grid-mode rule over units; the split partials stay per token."""
+    for schedule in (B.SCHEDULE_AUTO, B.SCHEDULE_BALANCED):
+        p = plan(args(T, W_, H=64, dtype=dtype, kernel=B.KERNEL_TCGEN05_TOKEN_PAIRS, schedule=schedule))
+        U = (T + 1) // 2
+        assert p["kernel"] == B.KERNEL_TCGEN05_TOKEN_PAIRS and p["clusters"] == 0
+        S = p["num_splits"]
+        # as many splits as keep one wave of units, at least 64 union columns
+        # (up to 2W) per split, and at most 2304 columns of each token
+        want = min(GB300_SMS // 2 // U, math.ceil(2 * W_ / 64), 32)
+        assert S == max(want, math.ceil(W_ / 2304), 1)
+        assert p["grid"] == 2 * U * S and p["ctas_per_split"] == 2
+        assert p["workspace_bytes"] == (0 if S == 1 else workspace(T * 64 * S))
+        assert p["threads"] == 512 and p["smem_bytes"] <= 232448
+
+
+def test_token_pair_form_needs_64_heads():
+    """H = 128 fills the MMA rows alone: a token-pair request runs the
+    dims-split kernel."""
+    for dtype in (B.SMLA_BF16, B.SMLA_E4M3):
+        p = plan(args(77, 640, H=128, dtype=dtype, kernel=B.KERNEL_TCGEN05_TOKEN_PAIRS))
+        assert p["kernel"] == B.KERNEL_TCGEN05 and p["grid"] == 2 * 77 * p["num_splits"]
+
+
 def workspace(rows):
     return -(-rows * 512 * 2 // 256) * 256 + -(-rows * 4 // 256) * 256
 
@@ -228,7 +256,7 @@ def test_bad_sm_count_and_null_plan():
     assert B.lib().smla_plan_decode_for_sm_count(None, 152, None) == B.SMLA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("field,value", [("kernel", 5), ("kernel", -1), ("schedule", 3), ("schedule", -1)])
+@pytest.mark.parametrize("field,value", [("kernel", 6), ("kernel", -1), ("schedule", 3), ("schedule", -1)])
 def test_unknown_kernel_or_schedule_is_an_error(field, value):
     a = args(8, 640)
     setattr(a, field, value)
