@@ -203,17 +203,10 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
 
   // ---------------------------------------------------------------- set-up
-  // Q rows staged in the R ring (free until the set-up's cluster barrier):
-  // row h at 512 h, its 16-byte chunk c at chunk position c ^ (h % 32) so
-  // that the per-head reads below spread over the banks
-  const unsigned char* qrow = reinterpret_cast<const unsigned char*>(p.q) + (int64_t)t * p.q_stride_token;
-  for (int c = tid; c < H * 32; c += kThreads) {
-    const int h = c >> 5, cc = c & 31;
-    cp_async_16(r_addr + h * 512 + ((cc ^ (h & 31)) << 4), qrow + (int64_t)h * kHeadDim + cc * 16);
-  }
   const bool softmax_warp = warp >= kSoftmaxWarp0;
   const int g_sm = softmax_warp ? (warp - kSoftmaxWarp0) >> 2 : 0;
-  // the split's index columns
+  // the split's index columns first: they lead to the first gathers, while Q
+  // is needed only by the first QK
   const int nchunks = (c1 - c0 + 31) / 32;
   const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
   int32_t rv[kChunksPerWarp];
@@ -231,17 +224,28 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
     }
   }
+  // Q rows staged in the R ring (free until the set-up's cluster barrier):
+  // row h at 512 h, its 16-byte chunk c at chunk position c ^ (h % 32) so
+  // that the per-head reads below spread over the banks
+  const unsigned char* qrow = reinterpret_cast<const unsigned char*>(p.q) + (int64_t)t * p.q_stride_token;
+  for (int c = tid; c < H * 32; c += kThreads) {
+    const int h = c >> 5, cc = c & 31;
+    cp_async_16(r_addr + h * 512 + ((cc ^ (h & 31)) << 4), qrow + (int64_t)h * kHeadDim + cc * 16);
+  }
   const TokenInfo ti = token_info(p, t);
   c1 = min(c1, max(c0, ti.n_lim));
   {
-    // zero the V and K rings and the P buffers (rows past a tile's slot
-    // count then hold finite data, P rows of absent heads stay 0); the R
-    // ring's entries are always copied in whole
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    uint4* zp = reinterpret_cast<uint4*>(base + kOffV);
-    for (int i = tid; i < (kOffR - kOffV) / 16; i += kThreads) zp[i] = z;
-    zp = reinterpret_cast<uint4*>(base + kOffP);
-    for (int i = tid; i < 2 * kPBytes / 16; i += kThreads) zp[i] = z;
+    // P rows of absent heads must read 0 (the softmax writes only the rows
+    // of present heads).  The V and K rings are not zeroed whole: rows past
+    // a tile's slot count must only be finite, which every row a gather has
+    // written is, so only those rows of an entry's first use are zeroed,
+    // once the tiles are known (below; the R ring's entries are copies of
+    // the peer's K entries)
+    if (H < 128) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4* zp = reinterpret_cast<uint4*>(base + kOffP);
+      for (int i = tid; i < 2 * kPBytes / 16; i += kThreads) zp[i] = z;
+    }
     if (tid == 0) {
       for (int i = 0; i < kNV; ++i) {
         mbar_init(bar(sm.kv_full[i]), 1);
@@ -348,6 +352,30 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     // [256 g, 256 g + 256) of its 32 heads (64 columns); absent heads get 0
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
+    if (!softmax_warp) {
+      // first use of a V or K entry by a partial tile: rows [n4, 64) of its
+      // column blocks must be finite (they meet P = 0 in the PV, and the K
+      // entry travels to the peer); later uses find rows an earlier tile
+      // wrote there.  n4 = the tile's own slots rounded up to 4 (gather4).
+      const int nsw = sm.nswa, nva = sm.nvalid;
+      const int tsw = (nsw + kNT - 1) / kNT;
+      const int nt = tsw + (nva - nsw + kNT - 1) / kNT;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kNV; ++j) {
+        const int start = j < tsw ? j * kNT : nsw + (j - tsw) * kNT;
+        const int n = j < nt ? max(0, min(kNH, min(kNT, (j < tsw ? nsw : nva) - start) - kNH * (int)rank)) : kNH;
+        const int n4 = (n + 3) & ~3;
+        if (n4 >= kNH) continue;
+        const int per_block = (kNH - n4) * 8;            // 16-byte chunks per column block
+        for (int i = tid; i < 4 * per_block; i += kSoftmaxWarp0 * 32) {
+          const int kb = i / per_block, c = i % per_block;
+          if (kb >= 2 && j >= kNK) continue;
+          unsigned char* blk = kb < 2 ? base + kOffV + j * kEntry + kb * kRegion
+                                      : base + kOffK + j * kEntry + (kb - 2) * kRegion;
+          reinterpret_cast<uint4*>(blk + n4 * 128)[c] = z;
+        }
+      }
+    }
     if (softmax_warp) {
       const int h = (warp & 3) * 32 + lane;
       const unsigned char* qs = base + kOffR + h * 512;
@@ -733,71 +761,51 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
         if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
       }
       const int64_t row_th = (int64_t)t * H + h;
-      if constexpr (!kPartial) {
+      // The normalised BF16 rows go through shared memory, so that the
+      // global stores below are whole 256-byte row segments rather than one
+      // 16-byte piece per row per warp instruction: warpgroup g stages its
+      // 128 columns in half of the V ring (read by nothing but this CTA's QK
+      // and PV, done by now; no copy to the peer reads it), 16-byte chunks
+      // XOR-swizzled by the row to spread the banks
+      unsigned char* row = stage_row(g, h);
 #pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
-          const int col = g * (kHalfDims / 2) + cc * 32;
-          float v[32];
-          if (have) {
-            uint32_t r[32];
-            tmem_ld32(tl + kOCol + col, r);
-            tmem_wait_ld();
+      for (int cc = 0; cc < kHalfDims / 64; ++cc) {
+        const int col = g * (kHalfDims / 2) + cc * 32;
+        float v[32];
+        if (have) {
+          uint32_t r[32];
+          tmem_ld32(tl + kOCol + col, r);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
-          } else {
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-          const int d0 = (int)rank * kHalfDims + col;
-          uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                              pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (rank == 0 && g == 0) {
-          if (S == 1) {
-            if (p.out_lse) p.out_lse[row_th] = lse;
-          } else {
-            p.part_lse[row_th * S + s] = lse;
-          }
-        }
-      } else {
-        // BF16 partial rows staged in shared memory for 256-byte row segment
-        // stores (no copy to the peer reads the V ring, so none in flight
-        // can see them)
-        unsigned char* row = stage_row(g, h);
-#pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
-          const int col = g * (kHalfDims / 2) + cc * 32;
-          float v[32];
-          if (have) {
-            uint32_t r[32];
-            tmem_ld32(tl + kOCol + col, r);
-            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
-                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        }
-        if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      }
+      if (rank == 0 && g == 0) {
+        if (kPartial)
+          p.part_lse[row_th * S + s] = lse;
+        else if (p.out_lse)
+          p.out_lse[row_th] = lse;
       }
     }
-    if constexpr (kPartial) {
-      named_bar_sync(1 + g, 128);
+    // copy-out of this warpgroup's staged columns, 256 contiguous bytes per
+    // row (half a warp per row): the output row, or the split partial row
+    named_bar_sync(1 + g, 128);
+    {
       const int w4 = (warp - kSoftmaxWarp0) & 3;
       const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
       const int cidx = lane & 15;
       for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
         const uint4 x = *reinterpret_cast<const uint4*>(stage_row(g, r) + ((cidx ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(p.part_o + (((int64_t)t * H + r) * S + s) * kHeadDim + col0 + cidx * 8) = x;
+        const int64_t orow = kPartial ? ((int64_t)t * H + r) * S + s : (int64_t)t * H + r;
+        *reinterpret_cast<uint4*>((kPartial ? p.part_o : p.out) + orow * kHeadDim + col0 + cidx * 8) = x;
       }
     }
   }
