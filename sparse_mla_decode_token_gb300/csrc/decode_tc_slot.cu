@@ -10,17 +10,18 @@
 // all 512 dims, so no partial logits cross between the CTAs:
 //
 //   producer warps 0-3  the own slots' full rows (four 128-byte column
-//                       blocks) with TMA tile::gather4 into a 128-byte-
-//                       swizzled, UMMA-canonical tile of a 3-stage ring, the
-//                       tile's 64 requests spread over the four warps; 64
-//                       consecutive rows are one box copy per column block
-//   QK warps 4-6        first copy the peer's output half of the landed own
+//                       blocks) with TMA tile::gather4 into 128-byte-swizzled,
+//                       UMMA-canonical tiles: this CTA's output half into an
+//                       entry of the V ring, the peer's half into one of the
+//                       K ring (rings below); the tile's 64 requests spread
+//                       over the four warps; 64 consecutive rows are one box
+//                       copy per column block
+//   QK warps 4-5        first copy the peer's output half of the landed own
 //                       rows (16 KB) into the peer's stage with one DSMEM bulk
 //                       copy, then S_r = Q K_own^T (M = 128 heads, N = 64 own
-//                       slots, K = 512 dims; Q dims 0-255 are read from tensor
-//                       memory, dims 256-511 from shared memory) into one of
-//                       three TMEM S buffers, warp 4 + b issuing the tiles of
-//                       buffer b
+//                       slots, K = 512 dims; Q is read from tensor memory)
+//                       into one of two TMEM S buffers, warp 4 + b issuing
+//                       the tiles of buffer b
 //   PV warp 7           O_r += P V_r (M = 128 heads, N = 256 output dims, K =
 //                       128 slots): P from shared memory (this CTA's half
 //                       written by its softmax, the peer's half copied in), V
@@ -316,29 +317,34 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       }
     }
     __syncthreads();
+    // every warp scans the chunk counts itself: lane L sums chunks 3L .. 3L + 2
+    // (3 x 32 >= kMaxChunks), one shuffle ladder over the lanes, and each of
+    // the warp's chunks reads its base from the lane that holds it
+    static_assert(3 * 32 >= kMaxChunks, "three chunks per lane");
     int chunk_base[kChunksPerWarp];
     {
-      int carry = 0;
+      const int k3 = 3 * lane;
+      const int e0 = k3 < nchunks ? sm.chunk_off[k3] : 0;
+      const int e1 = k3 + 1 < nchunks ? sm.chunk_off[k3 + 1] : 0;
+      const int e2 = k3 + 2 < nchunks ? sm.chunk_off[k3 + 2] : 0;
+      const int own = e0 + e1 + e2;
+      int incl = own;
 #pragma unroll
-      for (int q = 0; q < kChunksPerWarp; ++q) chunk_base[q] = 0;
-      for (int base0 = 0; base0 < nchunks; base0 += 32) {
-        const int k = base0 + lane;
-        const int v = k < nchunks ? sm.chunk_off[k] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += u;
-        }
-#pragma unroll
-        for (int q = 0; q < kChunksPerWarp; ++q) {
-          const int kq = warp + q * kWarps;
-          const int excl = __shfl_sync(0xffffffffu, incl - v, kq & 31);
-          if ((kq >> 5) == (base0 >> 5)) chunk_base[q] = carry + excl;
-        }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
       }
-      if (warp == 0 && lane == 0) sm.nvalid = carry;
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int kq = warp + q * kWarps;              // warp-uniform
+        const int src = min(kq / 3, 31), r = kq - 3 * src;
+        const int ex = __shfl_sync(0xffffffffu, incl - own, src);
+        const int a0 = __shfl_sync(0xffffffffu, e0, src);
+        const int a1 = __shfl_sync(0xffffffffu, e1, src);
+        chunk_base[q] = ex + (r >= 1 ? a0 : 0) + (r >= 2 ? a1 : 0);
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (warp == 0 && lane == 0) sm.nvalid = total;
     }
 #pragma unroll
     for (int q = 0; q < kChunksPerWarp; ++q) {
