@@ -136,4 +136,18 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// Element decoders of the packed KV forms.
+// E2M1 element values by code (OCP MX specification, FP4 E2M1: sign, two
+// exponent bits with bias 1, one mantissa bit).
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t mag = code & 7u;
+  const float v = mag < 2u ? 0.5f * (float)mag : (float)(2u + (mag & 1u)) * (float)(1u << ((mag >> 1) - 1u)) * 0.5f;
+  return (code & 8u) ? -v : v;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t byte) {
+  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(byte & 0xFFu), __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half*>(&hr.x));
+}
+
 }  // namespace smla

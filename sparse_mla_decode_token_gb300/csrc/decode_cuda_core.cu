@@ -55,19 +55,6 @@ __device__ __forceinline__ void decode16_e4m3(const uint4 raw, float* dst) {
   }
 }
 
-// E2M1 element values by code (OCP MX specification, FP4 E2M1: sign, two
-// exponent bits with bias 1, one mantissa bit).
-__device__ __forceinline__ float e2m1_value(uint32_t code) {
-  const uint32_t mag = code & 7u;
-  const float v = mag < 2u ? 0.5f * (float)mag : (float)(2u + (mag & 1u)) * (float)(1u << ((mag >> 1) - 1u)) * 0.5f;
-  return (code & 8u) ? -v : v;
-}
-
-__device__ __forceinline__ float e4m3_value(uint32_t byte) {
-  __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(byte & 0xFFu), __NV_E4M3);
-  return __half2float(*reinterpret_cast<__half*>(&hr.x));
-}
-
 // Packed FP8 row (584 bytes, 8-byte aligned): work item c < 56 decodes NoPE
 // dims [8c, 8c + 8) (E4M3 times 2^(e - 127) of their 64-dim block), item
 // 56 + i RoPE dims [448 + 4i, 448 + 4i + 4) (BF16).

@@ -179,13 +179,50 @@ struct TcParams {
   DecodeParams p;
 };
 
+// Packed FP8 rows (kPack = SMLA_PACKED_FP8) run the BF16 pipeline: the
+// producers load each selected row's bytes with plain loads (a 584-byte row
+// pitch is no TMA stride) and write its 256 dims of this CTA's output half as
+// BF16 into the stage, in the layout a TMA gather leaves.  Dims [d, d + 64)
+// of a row (d a multiple of 64) as 32 BF16 pairs: the NoPE E4M3 values times
+// 2^(e - 127) of their 64-dim block (exact in BF16), or the 64 RoPE values
+// (BF16 bits copied).
+__device__ __forceinline__ void packed_fp8_dims64(const unsigned char* row, int d, uint32_t (&out)[32]) {
+  if (d >= 448) {                                    // RoPE: BF16 as stored, 8-byte aligned
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(row + 456) + i);
+      out[2 * i] = x.x;
+      out[2 * i + 1] = x.y;
+    }
+    return;
+  }
+  const float scale = ldexpf(1.0f, (int)__ldg(row + 448 + d / 64) - 127);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint2 x = __ldg(reinterpret_cast<const uint2*>(row + d) + i);
+    const uint32_t w[2] = {x.x, x.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[h] >> (16 * k)) & 0xFFFFu), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&hr));
+        out[4 * i + 2 * h + k] = pack_bf16x2(f.x * scale, f.y * scale);
+      }
+    }
+  }
+}
+
 // kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
 // epilogue stages the partial rows in shared memory for contiguous stores (a
 // separate instantiation, so that the single-split code is compiled alone).
 // kPair: H = 64 and a unit is (token pair, split), see Cfg.
-template <bool kFp8, bool kPartial, bool kPair>
+// kPack: 0, or SMLA_PACKED_FP8 (BF16 pipeline: kFp8 false, kPair false).
+template <bool kFp8, bool kPartial, bool kPair, int kPack>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
+  static_assert(kPack == 0 || (kPack == SMLA_PACKED_FP8 && !kFp8 && !kPair),
+                "packed FP8 rows run the BF16 single-token pipeline");
   using C = Cfg<kFp8, kPair>;
   const DecodeParams& p = P.p;
   constexpr int kN = C::kN;
@@ -337,7 +374,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   };
   auto init_barriers = [&]() {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(bar(sm.kv_full[i]), 1);
+      // TMA: one arrival with the byte count; packed rows: one per warp of the producer group
+      mbar_init(bar(sm.kv_full[i]), kPack ? kProducerWarps / kProducerGroups : 1);
       mbar_init(bar(sm.kv_empty[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -616,10 +654,33 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       const int st = j % C::kStages;
       if (!warp_wait(cx, bar(sm.kv_empty[st]), ((j / C::kStages) & 1) ^ 1)) break;
       const int start = tile_start(j), n = tile_n(j);
-      const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
       const uint32_t stage = kv_addr + st * C::kStageBytes;
       const int32_t* rows = idx_s + start;
+      if constexpr (kPack != 0) {
+        // thread i of the group: row i / 2, column blocks 2 (i % 2) and 2 (i % 2) + 1 of this CTA's half
+        const int gi = pw * 32 + lane, r = gi >> 1;
+        if (r < n) {
+          const bool swa = j < tswa;
+          const unsigned char* row = reinterpret_cast<const unsigned char*>(swa ? p.swa : p.comp) +
+                                     (int64_t)rows[r] * (swa ? p.swa_stride : p.comp_stride);
+#pragma unroll 1
+          for (int kk = 0; kk < 2; ++kk) {
+            const int kb = 2 * (gi & 1) + kk;
+            uint32_t v[32];
+            packed_fp8_dims64(row, (int)rank * kHalfDims + 64 * kb, v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(stage + kb * C::kRegionKV + sw128_offset(r, c),
+                           make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          }
+        }
+        fence_proxy_async_smem();            // the tile is read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sm.kv_full[st]));
+        continue;
+      }
+      const int n4 = (n + 3) & ~3;           // gather4 moves four rows: the last row repeats
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar(sm.kv_full[st]), (uint32_t)(C::kRegions * n4 * 128));
       bool run = false;                      // rows[r] == rows[0] + r for every r < N
       if (n == kN) {
         const uint32_t r0 = (uint32_t)rows[0];
@@ -649,8 +710,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // Leave no TMA write of this group in flight, also after an abort: wait
     // (bounded, not cut short by the abort flag) for the last tiles it issued,
     // at most one per stage.  Normally the consumers have waited for them.
-    for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
-      if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
+    // (Packed rows are written with plain stores: nothing is in flight.)
+    if constexpr (kPack == 0)
+      for (int jj = max(pg, min(j, ntiles) - C::kStages); jj < min(j, ntiles); ++jj)
+        if ((jj - pg) % kProducerGroups == 0) drain_wait(bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1);
   } else if (warp < kMmaWarp + kQkWarps) {
     // ============================================================ QK issue
     // QK and PV are issued by different warps so that a QK never waits behind
@@ -1047,16 +1110,34 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 }  // namespace
 
 int tc_grid_smem_bytes(int dtype, bool pair) {
-  if (pair) return dtype == SMLA_BF16 ? Cfg<false, true>::kSmemBytes : Cfg<true, true>::kSmemBytes;
-  return dtype == SMLA_BF16 ? Cfg<false>::kSmemBytes : Cfg<true>::kSmemBytes;
+  // E4M3 rows run the FP8 geometry; BF16 and the packed forms the BF16 one
+  if (pair) return dtype == SMLA_E4M3 ? Cfg<true, true>::kSmemBytes : Cfg<false, true>::kSmemBytes;
+  return dtype == SMLA_E4M3 ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes;
 }
 int tc_grid_threads() { return kThreads; }
 
 cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cudaStream_t stream) {
   if (pair && p.H != 64) return cudaErrorInvalidValue;   // two tokens of 64 heads fill the 128 MMA rows
+  if (p.dtype == SMLA_NVFP4) return cudaErrorInvalidValue;   // NVFP4 rows run the CUDA-core kernel
+  const bool packed = p.dtype == SMLA_PACKED_FP8;
+  if (pair && packed) return cudaErrorInvalidValue;
   TcParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
+  const int smem = tc_grid_smem_bytes(p.dtype, pair);
+  auto launch = [&](auto kernel) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, stream>>>(P);
+    return cudaSuccess;
+  };
+  const bool partial = p.num_splits > 1;
+  if (packed) {                         // no tensor maps: the producers load the rows themselves
+    const cudaError_t e = partial ? launch(decode_tc_kernel<false, true, false, SMLA_PACKED_FP8>)
+                                  : launch(decode_tc_kernel<false, false, false, SMLA_PACKED_FP8>);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   // a pool of fewer than N rows holds no run of N rows: its run map is never used
   const int64_t run_rows = p.dtype == SMLA_BF16 ? Cfg<false>::kN : Cfg<true>::kN;
   const int swa_run = (int)std::max<int64_t>(1, std::min(run_rows, p.swa_rows));
@@ -1066,23 +1147,15 @@ cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cu
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_swa_run, p.swa, p.swa_rows, p.swa_stride, p.dtype, swa_run);
   if (e == cudaSuccess) e = encode_pool_map(&P.tm_comp_run, p.comp, p.comp_rows, p.comp_stride, p.dtype, comp_run);
   if (e != cudaSuccess) return e;
-  const int smem = tc_grid_smem_bytes(p.dtype, pair);
-  auto launch = [&](auto kernel) -> cudaError_t {
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    kernel<<<grid, kThreads, smem, stream>>>(P);
-    return cudaSuccess;
-  };
-  const bool partial = p.num_splits > 1;
   if (pair) {
     if (p.dtype == SMLA_BF16)
-      e = partial ? launch(decode_tc_kernel<false, true, true>) : launch(decode_tc_kernel<false, false, true>);
+      e = partial ? launch(decode_tc_kernel<false, true, true, 0>) : launch(decode_tc_kernel<false, false, true, 0>);
     else
-      e = partial ? launch(decode_tc_kernel<true, true, true>) : launch(decode_tc_kernel<true, false, true>);
+      e = partial ? launch(decode_tc_kernel<true, true, true, 0>) : launch(decode_tc_kernel<true, false, true, 0>);
   } else if (p.dtype == SMLA_BF16) {
-    e = partial ? launch(decode_tc_kernel<false, true, false>) : launch(decode_tc_kernel<false, false, false>);
+    e = partial ? launch(decode_tc_kernel<false, true, false, 0>) : launch(decode_tc_kernel<false, false, false, 0>);
   } else {
-    e = partial ? launch(decode_tc_kernel<true, true, false>) : launch(decode_tc_kernel<true, false, false>);
+    e = partial ? launch(decode_tc_kernel<true, true, false, 0>) : launch(decode_tc_kernel<true, false, false, 0>);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -238,9 +238,17 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
-  // the packed KV forms run on the CUDA-core kernel, whatever was asked for
-  const int kernel = packed_dtype(a->dtype) ? SMLA_KERNEL_CUDA_CORE
-                     : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a) : a->kernel;
+  // Packed FP8 rows run the dims-split tensor-core kernel (its BF16
+  // pipeline behind dequantising producers: the values are exact in BF16), or
+  // the CUDA-core kernel when that is asked for; the E4M3-only and token-pair
+  // forms do not take them.  NVFP4 rows run the CUDA-core kernel: their fp32
+  // row scale multiplies the NoPE dims only, and folded into BF16 tiles it
+  // rounds the logits past the LSE tolerance.
+  const int kernel = a->dtype == SMLA_NVFP4 ? SMLA_KERNEL_CUDA_CORE
+                     : a->dtype == SMLA_PACKED_FP8
+                         ? (a->kernel == SMLA_KERNEL_CUDA_CORE ? SMLA_KERNEL_CUDA_CORE : SMLA_KERNEL_TCGEN05)
+                     : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a)
+                                                     : a->kernel;
   int S = a->num_splits;
   // token units of the grid: tokens, or token pairs for the token-pair kernel
   int64_t units = a->sum_q;
@@ -272,7 +280,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
     const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
     if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned && !slot_split &&
-        !pairs_of_tokens &&
+        !pairs_of_tokens && !packed_dtype(a->dtype) &&
         a->width <= SMLA_TC_MAX_SPLIT_COLS && a->sum_q <= (int64_t)(SMLA_TC_MAX_UNITS - 2) * pairs) {
       // Balanced mode: P clusters, one per SM pair, take equal shares of the
       // T x W columns, each share at least 64 columns.  A share of at most

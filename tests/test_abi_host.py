@@ -33,7 +33,7 @@ def test_library_exports_every_declared_function(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(B.EXPORTS)
-    assert B.smla_abi_version() == 8
+    assert B.smla_abi_version() == 9
 
 
 def test_struct_layout_matches_header(tmp_path):

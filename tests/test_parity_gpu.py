@@ -382,30 +382,42 @@ def test_slot_split_many_units(H, splits):
     compare(w, out, lse)
 
 
+def packed_kernel(dtype, asked):
+    """Kernel a packed form plans to: NVFP4 the CUDA-core kernel always,
+    packed FP8 the dims-split kernel unless the CUDA-core kernel is asked for."""
+    return B.KERNEL_CUDA_CORE if dtype == "nvfp4" or asked == B.KERNEL_CUDA_CORE else B.KERNEL_TCGEN05
+
+
 @pytest.mark.parametrize("dtype", ["packed_fp8", "nvfp4"])
 @pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("splits", [1, 3, 0])
-@pytest.mark.parametrize("kernel", [B.KERNEL_AUTO, B.KERNEL_TCGEN05_SLOT_SPLIT])
+@pytest.mark.parametrize("kernel", [B.KERNEL_AUTO, B.KERNEL_CUDA_CORE, B.KERNEL_TCGEN05_SLOT_SPLIT,
+                                    B.KERNEL_TCGEN05_TOKEN_PAIRS])
 def test_packed_rows_parity(dtype, H, splits, kernel):
     """Packed KV rows (584-byte packed FP8, 384-byte NVFP4; BF16 query): the
-    CUDA-core kernel dequantises each gathered row, whatever kernel was asked
-    for; ragged tiles, masked slots, sinks and split partials."""
+    dims-split tensor-core kernel's producers dequantise each packed FP8 row
+    into BF16 tiles (AUTO, and the E4M3-only and token-pair requests), the
+    CUDA-core kernel each NVFP4 row (any request) and each row it is asked
+    for into fp32 shared memory; ragged tiles, masked slots, sinks and split
+    partials."""
     w = small_case(600 + H + splits, dtype=dtype, H=H)
     out, lse, plan = run_gpu(w, kernel=kernel, num_splits=splits)
-    assert plan["kernel"] == B.KERNEL_CUDA_CORE
+    assert plan["kernel"] == packed_kernel(dtype, kernel)
     if splits:
         assert plan["num_splits"] == splits
     compare(w, out, lse)
 
 
 @pytest.mark.parametrize("n", [7, 8])
-def test_packed_rows_workload_sampled(n):
+@pytest.mark.parametrize("kernel", [B.KERNEL_AUTO, B.KERNEL_CUDA_CORE])
+def test_packed_rows_workload_sampled(n, kernel):
     """Workload 3's shape with NVFP4 / packed FP8 rows (the bench workloads 7
-    and 8), every 8th token against the oracle."""
+    and 8): every 4th token of the tensor-core path, every 8th of the
+    CUDA-core path, against the oracle."""
     w = W.config_workload(n)
-    out, lse, plan = run_gpu(w)
-    assert plan["kernel"] == B.KERNEL_CUDA_CORE
-    compare(w, out, lse, tokens=list(range(0, w.sum_q, 8)))
+    out, lse, plan = run_gpu(w, kernel=kernel)
+    assert plan["kernel"] == packed_kernel(w.dtype, kernel)
+    compare(w, out, lse, tokens=list(range(0, w.sum_q, 8 if plan["kernel"] == B.KERNEL_CUDA_CORE else 4)))
 
 
 def test_many_tokens_grid():
