@@ -71,14 +71,13 @@ typedef enum smla_status {
  *     NoPE values in E2M1 (dim 2i in the low nibble of byte i), [224, 252)
  *     28 E4M3 block scales (dim d scaled by scale[d / 16]), [252, 380) the 64
  *     RoPE values in BF16, [380, 384) an fp32 scale of every NoPE value.
- * SMLA_PACKED_FP8 rows run the TCGEN05 kernel's BF16 pipeline, whose
- * producers load each selected row and write it dequantised into the BF16
- * tile (its values are exact in BF16); any other tensor-core request plans
- * to TCGEN05, and SMLA_KERNEL_CUDA_CORE runs the CUDA-core kernel.
- * SMLA_NVFP4 rows run the CUDA-core kernel whatever is asked for: their fp32
- * row scale multiplies the NoPE dims only, and folded into BF16 tiles it
- * would round the logits.  The CUDA-core kernel dequantises into fp32
- * shared memory. */
+ * The packed forms run the TCGEN05 kernel's BF16 pipeline, whose producers
+ * load each selected row and write it dequantised into the BF16 tile, exactly
+ * (packed FP8: E4M3 times a power of two; NVFP4: E2M1 times its E4M3 block
+ * scale, the fp32 row scale applied in fp32 to the logits and to P of the
+ * NoPE output dims); any other tensor-core request plans to TCGEN05, and
+ * SMLA_KERNEL_CUDA_CORE runs the CUDA-core kernel, which dequantises into
+ * fp32 shared memory. */
 typedef enum smla_dtype {
   SMLA_BF16 = 0,                   /* bfloat16 query and KV rows */
   SMLA_E4M3 = 1,                   /* per-tensor-scaled FP8 E4M3 ("fn") query and KV rows */

@@ -52,6 +52,7 @@
 // waits for its own copies and MMAs, frees its TMEM and returns.  No role
 // waits on an unbounded hardware barrier inside its loop.
 #include <cuda.h>
+#include <cuda_fp4.h>
 
 #include <algorithm>
 
@@ -110,6 +111,7 @@ struct TcSmall {
   int32_t chunk_off_b[kMaxChunks];
   int32_t only_b_chunk[kMaxChunks];
   int32_t nswa_a, nswa_b, n_a, n_b, only_b_swa, dup;
+  float rscale[kMaxStages][kMaxN];       // NVFP4 rows: each stage row's fp32 NoPE scale
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -213,17 +215,56 @@ __device__ __forceinline__ void packed_fp8_dims64(const unsigned char* row, int 
   }
 }
 
+// NVFP4 rows (kPack = SMLA_NVFP4) take the same path with exact tiles: dims
+// [d, d + 64) as 32 BF16 pairs, the NoPE E2M1 values times the E4M3 scale of
+// their 16-dim block (a product of two 8-bit codes, exact in BF16), or the 64
+// RoPE values.  The row's fp32 scale g multiplies the NoPE dims only, so it
+// stays out of the tile: each CTA applies it to its partial logits in fp32
+// (CTA 1 keeps its NoPE and RoPE dims in separate accumulators) and to the P
+// of its NoPE output dims.
+__device__ __forceinline__ void nvfp4_dims64(const unsigned char* row, int d, uint32_t (&out)[32]) {
+  if (d >= 448) {                                    // RoPE: BF16 as stored, 4-byte aligned
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[i] = __ldg(reinterpret_cast<const uint32_t*>(row + 252) + i);
+    return;
+  }
+  const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(row + 224 + d / 16));   // four block scales
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(row + d / 2) + i);   // 32 dims, low nibble first
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {                    // the two 16-dim blocks of these 32 dims
+      // E2M1 pairs converted by the hardware, times the block scale in fp16:
+      // at most six significant bits and within [2^-10, 2688], so exact
+      const __half2 bs = __float2half2_rn(e4m3_value((sc >> (8 * (2 * i + b))) & 0xFFu));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t byte = (w[2 * b + (k >> 2)] >> (8 * (k & 3))) & 0xFFu;
+        __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)byte, __NV_E2M1);
+        const float2 f = __half22float2(__hmul2(*reinterpret_cast<__half2*>(&hr), bs));
+        out[16 * i + 8 * b + k] = pack_bf16x2(f.x, f.y);
+      }
+    }
+  }
+}
+
 // kPartial: the launch has num_splits > 1 and writes BF16 split partials; its
 // epilogue stages the partial rows in shared memory for contiguous stores (a
 // separate instantiation, so that the single-split code is compiled alone).
 // kPair: H = 64 and a unit is (token pair, split), see Cfg.
-// kPack: 0, or SMLA_PACKED_FP8 (BF16 pipeline: kFp8 false, kPair false).
+// kPack: 0, or SMLA_PACKED_FP8 / SMLA_NVFP4 (BF16 pipeline: kFp8 false, kPair false).
 template <bool kFp8, bool kPartial, bool kPair, int kPack>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ TcParams P) {
-  static_assert(kPack == 0 || (kPack == SMLA_PACKED_FP8 && !kFp8 && !kPair),
-                "packed FP8 rows run the BF16 single-token pipeline");
+  static_assert(kPack == 0 || (!kFp8 && !kPair), "packed rows run the BF16 single-token pipeline");
+  constexpr bool kNv = kPack == SMLA_NVFP4;
   using C = Cfg<kFp8, kPair>;
+  // NVFP4: CTA 1's RoPE logits (three buffers) and the P of the NoPE output
+  // dims (P times each slot's row scale; two buffers) after the P buffers
+  constexpr uint32_t kSRCol = C::kPCol + 2 * C::kPCols;
+  constexpr uint32_t kPGCol = kSRCol + kSBufs * C::kN;
+  static_assert(!kNv || kPGCol + 2 * C::kPCols <= kTmemCols, "tensor memory budget (NVFP4)");
   const DecodeParams& p = P.p;
   constexpr int kN = C::kN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -413,6 +454,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
   if constexpr (!kPair) {
     zero_kv_stages();
     if (H < 128) zero_q_rows(H);
+    if constexpr (kNv) {                 // rows past a tile's count meet P = 0: their scale must be finite
+      float* rs = &sm.rscale[0][0];
+      for (int i = tid; i < kMaxStages * kMaxN; i += kThreads) rs[i] = 0.f;
+    }
     if (tid == 0) {
       init_barriers();
       fence_mbar_init_cluster();
@@ -663,11 +708,15 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           const bool swa = j < tswa;
           const unsigned char* row = reinterpret_cast<const unsigned char*>(swa ? p.swa : p.comp) +
                                      (int64_t)rows[r] * (swa ? p.swa_stride : p.comp_stride);
+          if (kNv && (gi & 1) == 0) sm.rscale[st][r] = __ldg(reinterpret_cast<const float*>(row + 380));
 #pragma unroll 1
           for (int kk = 0; kk < 2; ++kk) {
             const int kb = 2 * (gi & 1) + kk;
             uint32_t v[32];
-            packed_fp8_dims64(row, (int)rank * kHalfDims + 64 * kb, v);
+            if constexpr (kNv)
+              nvfp4_dims64(row, (int)rank * kHalfDims + 64 * kb, v);
+            else
+              packed_fp8_dims64(row, (int)rank * kHalfDims + 64 * kb, v);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               st_shared_v4(stage + kb * C::kRegionKV + sw128_offset(r, c),
@@ -742,7 +791,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         for (int kk = 0; kk < C::kK1; ++kk) {
           const uint64_t a = desc_sw128(q_addr + (kk >> 2) * C::kRegionQ + (kk & 3) * 32, 16, 1024);
           const uint64_t kd = desc_sw128(stage + (kk >> 2) * C::kRegionKV + (kk & 3) * 32, 16, 1024);
-          mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
+          if (kNv && rank == 1 && kk >= C::kK1 - 4)     // CTA 1's dims 448-511: the RoPE logits apart
+            mma<kFp8>(tmem + kSRCol + b * kN, a, kd, idesc_qk, kk > C::kK1 - 4 ? 1u : 0u);
+          else
+            mma<kFp8>(tmem + kSCol + b * kN, a, kd, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(sm.s_full[b]));
         if (k == 0) mma_commit(bar(sm.qk0_done));
@@ -763,8 +815,22 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
         for (int kk = 0; kk < C::kK2; ++kk) {
           const uint64_t v = desc_sw128(stage + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
-          mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + b * C::kPCols + kk * (C::kKStep * C::kElem / 4), v,
-                           idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pk = b * C::kPCols + kk * (C::kKStep * C::kElem / 4);
+          const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
+          if constexpr (kNv) {
+            // NoPE output dims take P times the row scale, CTA 1's RoPE dims (its last 64) P
+            if (rank == 0) {
+              mma_tmem_a<kFp8>(tmem + kOCol, tmem + kPGCol + pk, v, idesc_pv, acc);
+            } else {
+              constexpr uint32_t idesc_nope = idesc(kFp8, 128, kHalfDims - 64, true);
+              constexpr uint32_t idesc_rope = idesc(kFp8, 128, 64, true);
+              const uint64_t vr = desc_sw128(stage + 3 * C::kRegionKV + kk * (C::kKStep / 8) * 1024, C::kRegionKV, 1024);
+              mma_tmem_a<kFp8>(tmem + kOCol, tmem + kPGCol + pk, v, idesc_nope, acc);
+              mma_tmem_a<kFp8>(tmem + kOCol + kHalfDims - 64, tmem + C::kPCol + pk, vr, idesc_rope, acc);
+            }
+          } else {
+            mma_tmem_a<kFp8>(tmem + kOCol, tmem + C::kPCol + pk, v, idesc_pv, acc);
+          }
         }
         mma_commit(bar(sm.p_empty[b]));
         mma_commit(bar(sm.kv_empty[st]));
@@ -802,12 +868,15 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
       for (int i = 0; i < C::kPCols; ++i) zr[i] = 0u;
       tmem_st16(tl + p_cols, zr);
+      if constexpr (kNv) tmem_st16(tl + kPGCol + g * C::kPCols, zr);
       tmem_wait_st();
     }
     // send this CTA's partial S of tile jj (a tile of my warpgroup) to the peer
     auto push = [&](int jj) -> bool {
       const int sb = jj % kSBufs;
       if (!warp_wait(cx, bar(sm.s_full[sb]), (jj / kSBufs) & 1)) return false;
+      // NVFP4: the row scales came with the tile (plain stores before the producers' arrival)
+      if (kNv && !warp_wait(cx, bar(sm.kv_full[jj % C::kStages]), (jj / C::kStages) & 1)) return false;
       tc_fence_after();
       if (jj >= 2 && !warp_wait(cx, bar(sm.xout_free[g]), ((jj >> 1) & 1) ^ 1, true)) return false;
       if (active) {
@@ -817,6 +886,18 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           uint32_t v[16];
           tmem_ld16(tl + kSCol + sb * kN + hb * 16, v);
           tmem_wait_ld();
+          if constexpr (kNv) {
+            // this CTA's share of the logit: g S over its NoPE dims, plus CTA 1's RoPE part
+            const float* rs = sm.rscale[jj % C::kStages] + hb * 16;
+            uint32_t vr[16];
+            if (rank == 1) {
+              tmem_ld16(tl + kSRCol + sb * kN + hb * 16, vr);
+              tmem_wait_ld();
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              v[i] = __float_as_uint(rs[i] * __uint_as_float(v[i]) + (rank == 1 ? __uint_as_float(vr[i]) : 0.f));
+          }
           // 24-bit logits: the low mantissa byte is dropped after rounding;
           // values a, b, c, d travel as [a1 a2 a3 d1] [b1 b2 b3 d2] [c1 c2 c3 d3]
           uint32_t w[12];
@@ -859,6 +940,23 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           tmem_ld32(tl + kSCol + sb * kN + hb * 32, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
+        }
+        if constexpr (kNv) {                      // as pushed: g S (+ CTA 1's RoPE part)
+          tmem_wait_ld();
+          const float* rs = sm.rscale[j % C::kStages];
+          if (rank == 1) {
+#pragma unroll
+            for (int hb = 0; hb < kN / 32; ++hb) {
+              uint32_t r[32];
+              tmem_ld32(tl + kSRCol + sb * kN + hb * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = rs[hb * 32 + i] * sv[hb * 32 + i] + __uint_as_float(r[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kN; ++i) sv[i] *= rs[i];
+          }
         }
       }
       if (!(ok = warp_wait(cx, bar(sm.xin_full[g]), (j >> 1) & 1, true))) break;
@@ -967,6 +1065,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
         }
         tmem_st16(tl + p_cols, pr);
+        if constexpr (kNv) {                      // P of the NoPE output dims: times each slot's row scale
+          const float* rs = sm.rscale[j % C::kStages];
+#pragma unroll
+          for (int i = 0; i < C::kPCols; ++i) pr[i] = pack_bf16x2(sv[2 * i] * rs[2 * i], sv[2 * i + 1] * rs[2 * i + 1]);
+          tmem_st16(tl + kPGCol + g * C::kPCols, pr);
+        }
       }
       // ---- O rescale when the reference moved (O holds tiles < j at m(j-1))
       const bool rescale = active && j > 0 && m_cur != m_prev;
@@ -1118,8 +1222,7 @@ int tc_grid_threads() { return kThreads; }
 
 cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cudaStream_t stream) {
   if (pair && p.H != 64) return cudaErrorInvalidValue;   // two tokens of 64 heads fill the 128 MMA rows
-  if (p.dtype == SMLA_NVFP4) return cudaErrorInvalidValue;   // NVFP4 rows run the CUDA-core kernel
-  const bool packed = p.dtype == SMLA_PACKED_FP8;
+  const bool packed = p.dtype == SMLA_PACKED_FP8 || p.dtype == SMLA_NVFP4;
   if (pair && packed) return cudaErrorInvalidValue;
   TcParams P;
   memset(&P, 0, sizeof(P));
@@ -1133,8 +1236,13 @@ cudaError_t launch_decode_tc_grid(const DecodeParams& p, int grid, bool pair, cu
   };
   const bool partial = p.num_splits > 1;
   if (packed) {                         // no tensor maps: the producers load the rows themselves
-    const cudaError_t e = partial ? launch(decode_tc_kernel<false, true, false, SMLA_PACKED_FP8>)
-                                  : launch(decode_tc_kernel<false, false, false, SMLA_PACKED_FP8>);
+    cudaError_t e;
+    if (p.dtype == SMLA_PACKED_FP8)
+      e = partial ? launch(decode_tc_kernel<false, true, false, SMLA_PACKED_FP8>)
+                  : launch(decode_tc_kernel<false, false, false, SMLA_PACKED_FP8>);
+    else
+      e = partial ? launch(decode_tc_kernel<false, true, false, SMLA_NVFP4>)
+                  : launch(decode_tc_kernel<false, false, false, SMLA_NVFP4>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

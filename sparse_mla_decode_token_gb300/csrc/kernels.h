@@ -15,7 +15,7 @@ smla_status record_error(smla_status st, const char* msg);
 
 // tcgen05 decode kernel, grid schedule (decode_tc_grid.cu): a 2-CTA cluster
 // per (token, split) of at most SMLA_TC_MAX_SPLIT_COLS columns (BF16, E4M3
-// and packed FP8 rows; the last through BF16 tiles); pair = true
+// and the packed forms, the last through BF16 tiles); pair = true
 // (H = 64 only): per (token pair, split), grid = 2 ceil(T / 2) S, the two
 // tokens' heads in one 128-row MMA tile over the union of their rows.
 int tc_grid_smem_bytes(int dtype, bool pair);

@@ -238,14 +238,11 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   if (sms < 1) return fail(SMLA_ERR_INVALID_ARG, "sm_count %d < 1", sms);
   memset(plan, 0, sizeof(*plan));
   const int max_splits = a->max_splits ? a->max_splits : SMLA_DEFAULT_MAX_SPLITS;
-  // Packed FP8 rows run the dims-split tensor-core kernel (its BF16
-  // pipeline behind dequantising producers: the values are exact in BF16), or
-  // the CUDA-core kernel when that is asked for; the E4M3-only and token-pair
-  // forms do not take them.  NVFP4 rows run the CUDA-core kernel: their fp32
-  // row scale multiplies the NoPE dims only, and folded into BF16 tiles it
-  // rounds the logits past the LSE tolerance.
-  const int kernel = a->dtype == SMLA_NVFP4 ? SMLA_KERNEL_CUDA_CORE
-                     : a->dtype == SMLA_PACKED_FP8
+  // The packed KV forms run the dims-split tensor-core kernel (its BF16
+  // pipeline behind dequantising producers, exact tiles), or the CUDA-core
+  // kernel when that is asked for; the E4M3-only and token-pair forms do not
+  // take them.
+  const int kernel = packed_dtype(a->dtype)
                          ? (a->kernel == SMLA_KERNEL_CUDA_CORE ? SMLA_KERNEL_CUDA_CORE : SMLA_KERNEL_TCGEN05)
                      : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a)
                                                      : a->kernel;

@@ -60,11 +60,11 @@ def test_paged_parity(kernel, dtype, H, splits, page_size):
 @pytest.mark.parametrize("splits", [1, 2])
 def test_paged_packed_rows(dtype, page_size, splits):
     """The page-table form with packed KV rows, on the dims-split tensor-core
-    kernel (AUTO for packed FP8) and the CUDA-core kernel."""
+    kernel (AUTO) and the CUDA-core kernel."""
     w = paged_case(700 + page_size + splits, dtype=dtype, H=128, page_size=page_size)
     for kernel in (B.KERNEL_AUTO, B.KERNEL_CUDA_CORE):
         out, lse, plan = run_gpu(w, num_splits=splits, kernel=kernel)
-        want = B.KERNEL_CUDA_CORE if kernel == B.KERNEL_CUDA_CORE or dtype == "nvfp4" else B.KERNEL_TCGEN05
+        want = B.KERNEL_CUDA_CORE if kernel == B.KERNEL_CUDA_CORE else B.KERNEL_TCGEN05
         assert plan["kernel"] == want and plan["num_splits"] == splits
         compare(w, out, lse)
 

@@ -383,9 +383,9 @@ def test_slot_split_many_units(H, splits):
 
 
 def packed_kernel(dtype, asked):
-    """Kernel a packed form plans to: NVFP4 the CUDA-core kernel always,
-    packed FP8 the dims-split kernel unless the CUDA-core kernel is asked for."""
-    return B.KERNEL_CUDA_CORE if dtype == "nvfp4" or asked == B.KERNEL_CUDA_CORE else B.KERNEL_TCGEN05
+    """Kernel a packed form plans to: the dims-split kernel unless the
+    CUDA-core kernel is asked for."""
+    return B.KERNEL_CUDA_CORE if asked == B.KERNEL_CUDA_CORE else B.KERNEL_TCGEN05
 
 
 @pytest.mark.parametrize("dtype", ["packed_fp8", "nvfp4"])
@@ -395,11 +395,10 @@ def packed_kernel(dtype, asked):
                                     B.KERNEL_TCGEN05_TOKEN_PAIRS])
 def test_packed_rows_parity(dtype, H, splits, kernel):
     """Packed KV rows (584-byte packed FP8, 384-byte NVFP4; BF16 query): the
-    dims-split tensor-core kernel's producers dequantise each packed FP8 row
-    into BF16 tiles (AUTO, and the E4M3-only and token-pair requests), the
-    CUDA-core kernel each NVFP4 row (any request) and each row it is asked
-    for into fp32 shared memory; ragged tiles, masked slots, sinks and split
-    partials."""
+    dims-split tensor-core kernel's producers dequantise each row into exact
+    BF16 tiles (AUTO, and the E4M3-only and token-pair requests; NVFP4's row
+    scale applied to the logits and P in fp32), the CUDA-core kernel into fp32
+    shared memory; ragged tiles, masked slots, sinks and split partials."""
     w = small_case(600 + H + splits, dtype=dtype, H=H)
     out, lse, plan = run_gpu(w, kernel=kernel, num_splits=splits)
     assert plan["kernel"] == packed_kernel(dtype, kernel)

@@ -285,23 +285,19 @@ def test_device_plan_equals_the_sm_count_plan():
 
 @pytest.mark.parametrize("dtype", [B.SMLA_PACKED_FP8, B.SMLA_NVFP4])
 def test_packed_rows_plan(dtype):
-    """Packed FP8 rows run the dims-split tensor-core kernel (the BF16 plan:
+    """Packed KV rows run the dims-split tensor-core kernel (the BF16 plan:
     grid schedule, its split rule, smem and workspace), whatever tensor-core
     form or schedule was asked for, and the CUDA-core kernel when that is
-    asked for; NVFP4 rows run the CUDA-core kernel whatever is asked for."""
+    asked for."""
     for T, W_ in [(128, 2176), (4, 16512), (2, 256)]:
         for kernel in (B.KERNEL_AUTO, B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_HEAD_OWNED,
                        B.KERNEL_TCGEN05_SLOT_SPLIT, B.KERNEL_TCGEN05_TOKEN_PAIRS):
             for schedule in (B.SCHEDULE_AUTO, B.SCHEDULE_BALANCED):
                 for H in (64, 128):
                     p = plan(args(T, W_, H=H, dtype=dtype, kernel=kernel, schedule=schedule))
-                    if dtype == B.SMLA_NVFP4:
-                        ref = plan(args(T, W_, H=H, dtype=B.SMLA_BF16, kernel=B.KERNEL_CUDA_CORE))
-                        assert p["kernel"] == B.KERNEL_CUDA_CORE
-                    else:
-                        ref = plan(args(T, W_, H=H, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05,
-                                        schedule=B.SCHEDULE_GRID))
-                        assert p["kernel"] == B.KERNEL_TCGEN05 and p["clusters"] == 0
+                    ref = plan(args(T, W_, H=H, dtype=B.SMLA_BF16, kernel=B.KERNEL_TCGEN05,
+                                    schedule=B.SCHEDULE_GRID))
+                    assert p["kernel"] == B.KERNEL_TCGEN05 and p["clusters"] == 0
                     assert p == ref
         p = plan(args(T, W_, dtype=dtype, kernel=B.KERNEL_CUDA_CORE))
         assert p == plan(args(T, W_, dtype=B.SMLA_BF16, kernel=B.KERNEL_CUDA_CORE))
