@@ -452,7 +452,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     }
   };
   if constexpr (!kPair) {
-    zero_kv_stages();
     if (H < 128) zero_q_rows(H);
     if constexpr (kNv) {                 // rows past a tile's count meet P = 0: their scale must be finite
       float* rs = &sm.rscale[0][0];
@@ -476,6 +475,25 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       if (k < nchunks) {
         const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
         if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+      }
+    }
+    // First use of a stage by a partial tile: the rows past those the
+    // gathers write must be finite (they meet P = 0 in the PV); later uses
+    // find rows an earlier tile wrote there, so the stages are not zeroed whole
+    {
+      const int nsw = sm.nswa, nv = total;
+      const int tsw = (nsw + kN - 1) / kN;
+      const int nt = tsw + (nv - nsw + kN - 1) / kN;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int jz = 0; jz < min(nt, C::kStages); ++jz) {
+        const int start = jz < tsw ? jz * kN : nsw + (jz - tsw) * kN;
+        const int n = min(kN, (jz < tsw ? nsw : nv) - start);
+        const int nw = kPack ? n : (n + 3) & ~3;   // rows the gathers write (gather4: in fours)
+        if (nw >= kN) continue;
+        const int per_region = (kN - nw) * 8;      // 16-byte chunks per 128-byte column block
+        for (int i = tid; i < C::kRegions * per_region; i += kThreads)
+          reinterpret_cast<uint4*>(base + C::kOffKV + jz * C::kStageBytes + (i / per_region) * C::kRegionKV +
+                                   nw * 128)[i % per_region] = z;
       }
     }
   } else {
@@ -1123,7 +1141,12 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + (kPair ? (h & 63) : h)) * kLog2e - lse));
       }
       const int64_t row_th = kPair ? (int64_t)(t + (h >> 6)) * H + (h & 63) : (int64_t)t * H + h;
-      if constexpr (!kPartial) {
+      // The BF16 rows (the output, or a split partial) go through shared
+      // memory (the KV stages are free once every PV is done), so that the
+      // global stores below are whole 256-byte row segments rather than one
+      // 16-byte piece per row per warp instruction.  Warpgroup g stages its
+      // 128 columns; 16-byte chunks are XOR-swizzled by the row to spread banks.
+      unsigned char* row = base + C::kOffKV + g * (128 * 256) + h * 256;
 #pragma unroll 1
       for (int cc = 0; cc < kHalfDims / 64; ++cc) {
         const int col = g * (kHalfDims / 2) + cc * 32;
@@ -1138,53 +1161,22 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        const int d0 = (int)rank * kHalfDims + col;
-        uint4* o = reinterpret_cast<uint4*>(p.out + row_th * kHeadDim + d0);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          o[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+          *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       if (rank == 0 && g == 0) {
-        if (S == 1) {
-          if (p.out_lse) p.out_lse[row_th] = lse;
-        } else {
+        if (kPartial)
           p.part_lse[row_th * S + s] = lse;
-        }
-      }
-      } else {
-        // BF16 partial rows go through shared memory (the KV stages are free
-        // once every PV is done), so that the global stores below are whole
-        // 256-byte row segments rather than one 16-byte piece per row per warp
-        // instruction.  Warpgroup g stages its 128 columns; 16-byte chunks are
-        // XOR-swizzled by the row to spread banks.
-        unsigned char* row = base + C::kOffKV + g * (128 * 256) + h * 256;
-#pragma unroll 1
-        for (int cc = 0; cc < kHalfDims / 64; ++cc) {
-          const int col = g * (kHalfDims / 2) + cc * 32;
-          float v[32];
-          if (have) {
-            uint32_t r[32];
-            tmem_ld32(tl + kOCol + col, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(row + (((cc * 4 + q) ^ (h & 7)) << 4)) =
-                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        }
-        if (rank == 0 && g == 0) p.part_lse[row_th * S + s] = lse;
+        else if (p.out_lse)
+          p.out_lse[row_th] = lse;
       }
     }
-    // copy-out of this warpgroup's staged partial columns, 256 contiguous bytes
-    // per row (half a warp per row)
-    if constexpr (kPartial) {
+    // copy-out of this warpgroup's staged columns, 256 contiguous bytes per
+    // row (half a warp per row): the output row, or the split partial row
+    {
       asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(128) : "memory");
       const unsigned char* stg = base + C::kOffKV + g * (128 * 256);
       const int w4 = (warp - kSoftmaxWarp0) & 3;
@@ -1193,7 +1185,8 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
       for (int r = w4 + 4 * (lane >> 4); r < rows_used; r += 8) {
         const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 256 + ((c ^ (r & 7)) << 4));
         const int64_t row = kPair ? (int64_t)(t + (r >> 6)) * H + (r & 63) : (int64_t)t * H + r;
-        *reinterpret_cast<uint4*>(p.part_o + (row * S + s) * kHeadDim + col0 + c * 8) = x;
+        *reinterpret_cast<uint4*>((kPartial ? p.part_o + (row * S + s) * kHeadDim : p.out + row * kHeadDim) +
+                                  col0 + c * 8) = x;
       }
     }
   }
