@@ -36,11 +36,18 @@
 //                       m(j-1) (handed over by the other warpgroup through
 //                       shared memory), exponentials in base 2 with lazy
 //                       rescaling of O, write P (BF16 or E4M3) into TMEM;
-//                       finally normalise O and store it (BF16 output, or BF16
-//                       split partials staged through shared memory) plus the
-//                       LSE.  Each warpgroup pushes its next tile's partial S
-//                       before its exponentials; one warpgroup's exponentials
-//                       overlap the other's loads and exchange.
+//                       finally normalise O and store it (the BF16 output or
+//                       split partial rows, staged through shared memory for
+//                       256-byte row-segment stores) plus the LSE.  Each
+//                       warpgroup pushes its next tile's partial S before its
+//                       exponentials; one warpgroup's exponentials overlap the
+//                       other's loads and exchange.
+//
+// Two variants of the same pipeline: kPair (H = 64) runs two tokens per unit
+// over the union of their selected rows, their heads in MMA rows 0-63 and
+// 64-127 (see Cfg); kPack (packed FP8 and NVFP4 rows) replaces the TMA
+// gathers by producers that load the packed rows and write them dequantised
+// into the BF16 tiles (see packed_fp8_dims64 / nvfp4_dims64).
 //
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
