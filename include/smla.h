@@ -104,8 +104,14 @@ typedef enum smla_dtype {
  * shared compressed rows) is gathered once, and each head's softmax takes
  * only its own token's slots.  When either token selects some row more than
  * once the unit shares nothing (each slot still counts once per selection).
- * The grid has ceil(T / 2) x S pairs.  AUTO picks TCGEN05_SLOT_SPLIT for E4M3 rows (TCGEN05 when
- * the BALANCED schedule is asked for) and TCGEN05 for BF16 rows. */
+ * The grid has ceil(T / 2) x S pairs.  E4M3 rows run the slot-split kernel's
+ * pair form (the second token's heads fill the 128 rows its P exchange
+ * already carries), which takes at most 1152 columns of each token per split
+ * (the split count rises to meet that); BF16 rows the dims-split kernel's.
+ * AUTO picks TCGEN05_SLOT_SPLIT for E4M3 rows (TCGEN05 when the BALANCED
+ * schedule is asked for; TCGEN05_TOKEN_PAIRS for 64 heads, at most 1152
+ * columns and more tokens than SM pairs: half the units, one wave fewer) and
+ * TCGEN05 for BF16 rows. */
 /* Work hand-out of the TCGEN05 kernel (smla_args.schedule).  GRID: one CTA
  * pair per (token, split), the split count from num_splits / max_splits.
  * BALANCED (with num_splits == 0 and max_splits == 0, W <= 2304 and T <= 14

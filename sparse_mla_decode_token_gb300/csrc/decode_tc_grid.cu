@@ -154,18 +154,20 @@ struct Cfg {
   static constexpr int kOffSmall = kOffMask + (kPair ? 2 * kMaxTiles * 8 : 0);
   static constexpr int kSmemBytes = kOffSmall + (int)sizeof(TcSmall) + 1024;   // + alignment slack
   // token-pair set-up scratch, in the KV stages before the first gather: an
-  // open-addressing hash of the selected rows (keys, then per-key flags:
-  // bit 0 token A selects it, bit 1 token B), each token's compacted list,
-  // and one membership byte per union entry
-  static constexpr int kHashSlots = 8192;                      // > 2 x kMaxCols: probing always ends
-  static constexpr int kScrFlags = kHashSlots * 4;
+  // open-addressing hash of token A's rows (keys, then A's list indices),
+  // each token's compacted list, one membership byte per union entry, and
+  // one "B selects it too" byte per entry of A's list
+  static constexpr int kHashSlots = 4096;                      // > kMaxCols (A's keys): probing always ends
+  static constexpr int kScrVals = kHashSlots * 4;
   static constexpr int kScrListA = 2 * kHashSlots * 4;
   static constexpr int kScrListB = kScrListA + kMaxCols * 4;
   static constexpr int kScrMemb = kScrListB + kMaxCols * 4;
-  static constexpr int kScrEnd = kScrMemb + kIdxCap;
+  static constexpr int kScrShared = kScrMemb + kIdxCap;
+  static constexpr int kScrEnd = kScrShared + kMaxCols;
   static_assert(!kPair || kScrEnd <= kStages * kStageBytes, "token-pair scratch fits in the KV stages");
-  static_assert(kScrFlags % 16 == 0 && kScrListA % 16 == 0, "scratch arrays start on 16-byte boundaries");
-  static_assert(kHashSlots > 2 * kMaxCols && (kHashSlots & (kHashSlots - 1)) == 0, "hash table size");
+  static_assert(kScrVals % 16 == 0 && kScrListA % 16 == 0 && kScrShared % 16 == 0,
+                "scratch arrays start on 16-byte boundaries");
+  static_assert(kHashSlots > kMaxCols && (kHashSlots & (kHashSlots - 1)) == 0, "hash table size");
   static_assert(kStages <= kMaxStages, "barrier arrays");
   static_assert(kStages >= 3, "PV lags QK by two tiles: a third stage keeps the producer going");
   static_assert(kN <= kMaxN, "row lists");
@@ -505,10 +507,10 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     }
   } else {
     // f1, the rows shared by a pair's tokens gathered once.  Each token's
-    // valid slots are compacted as above; a hash of (pool, row) keys marks
-    // which token selects each row; the union list is token A's list with
-    // B's rows that A does not select inserted after A's SWA and compressed
-    // runs, in B's order:
+    // valid slots are compacted as above; token A's rows go into a hash of
+    // (pool, row) keys, which B's rows look up; the union list is token A's
+    // list with B's rows that A does not select inserted after A's SWA and
+    // compressed runs, in B's order:
     //   [A SWA] [B-only SWA] [A compressed] [B-only compressed]
     // A row that either token selects more than once counts once per slot in
     // that token's softmax, which a shared entry cannot express: then the
@@ -516,48 +518,16 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     // The construction is deterministic, so both CTAs of the pair build the
     // same list (the hash slots may differ; the flags read back do not).
     uint32_t* hkeys = reinterpret_cast<uint32_t*>(base + C::kOffKV);
-    uint32_t* hflags = reinterpret_cast<uint32_t*>(base + C::kOffKV + C::kScrFlags);
+    int32_t* hvals = reinterpret_cast<int32_t*>(base + C::kOffKV + C::kScrVals);
     int32_t* list_a = reinterpret_cast<int32_t*>(base + C::kOffKV + C::kScrListA);
     int32_t* list_b = reinterpret_cast<int32_t*>(base + C::kOffKV + C::kScrListB);
     uint8_t* memb = base + C::kOffKV + C::kScrMemb;
-    constexpr uint32_t kEmpty = 0xffffffffu;
-    auto hkey = [](int row, bool comp) { return (uint32_t)row | (comp ? 0x80000000u : 0u); };
-    auto hslot = [](uint32_t key) { return (key * 2654435761u) >> 19; };     // 13 bits: kHashSlots
-    static_assert(C::kHashSlots == 1 << 13, "hash index width");
-    auto insert = [&](uint32_t key, uint32_t flag) {
-      if (key == kEmpty) {                // (comp row 2^31 - 1) would read as empty: share nothing
-        sm.dup = 1;
-        return;
-      }
-      uint32_t h = hslot(key);
-      for (int probe = 0; probe < C::kHashSlots; ++probe) {
-        const uint32_t prev = atomicCAS(hkeys + h, kEmpty, key);
-        if (prev == kEmpty || prev == key) {
-          if (atomicOr(hflags + h, flag) & flag) sm.dup = 1;    // this token selects the row twice
-          return;
-        }
-        h = (h + 1) & (C::kHashSlots - 1);
-      }
-      sm.dup = 1;                          // not reached: the table has more slots than keys
-    };
-    auto flags_of = [&](uint32_t key) -> uint32_t {
-      uint32_t h = hslot(key);
-      for (int probe = 0; probe < C::kHashSlots; ++probe) {
-        const uint32_t k = hkeys[h];
-        if (k == key) return hflags[h];
-        if (k == kEmpty) return 0u;
-        h = (h + 1) & (C::kHashSlots - 1);
-      }
-      return 0u;
-    };
+    uint8_t* shared_a = base + C::kOffKV + C::kScrShared;
+    auto hkey = [](int row, bool comp) { return pair_key(row, comp); };
     {
-      const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), z = make_uint4(0, 0, 0, 0);
-      uint4* kp = reinterpret_cast<uint4*>(hkeys);
-      uint4* fp = reinterpret_cast<uint4*>(hflags);
-      for (int i = tid; i < C::kHashSlots / 4; i += kThreads) {
-        kp[i] = e4;
-        fp[i] = z;
-      }
+      const uint4 e4 = make_uint4(kPairEmpty, kPairEmpty, kPairEmpty, kPairEmpty), z = make_uint4(0, 0, 0, 0);
+      for (int i = tid; i < C::kHashSlots / 4; i += kThreads) reinterpret_cast<uint4*>(hkeys)[i] = e4;
+      for (int i = tid; i < kMaxCols / 16; i += kThreads) reinterpret_cast<uint4*>(shared_a)[i] = z;
       for (int i = tid; i < 2 * C::kMaxTiles; i += kThreads) mask_a[i] = 0ull;
     }
     if (!has_b) zero_q_rows(64);
@@ -583,7 +553,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
           if (rv[q] >= 0) {
             const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
             list_a[e] = rv[q];
-            insert(hkey(rv[q], e >= nswa_a), 1u);
+            pair_insert_a<C::kHashSlots>(hkeys, hvals, &sm.dup, hkey(rv[q], e >= nswa_a), e);
           }
         }
       }
@@ -598,7 +568,6 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
             if (rvb[q] >= 0) {
               const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
               list_b[e] = rvb[q];
-              insert(hkey(rvb[q], e >= nswa_b), 2u);
             }
           }
         }
@@ -607,26 +576,43 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
     }
     __syncthreads();
     const int n_a = sm.n_a, n_b = sm.n_b;
-    const bool dup = sm.dup != 0;
-    // B's entries that A does not select, counted per 32-entry chunk of B's list
+    // B's entries that A does not select (all of them once a repeat is
+    // known), counted per 32-entry chunk of B's list; a B entry that A
+    // selects claims A's entry and marks it shared
     const int nch_b = (n_b + 31) / 32;
     unsigned only_b[kChunksPerWarp];
+    auto count_only_b = [&](bool all) {
 #pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int k = warp + q * kWarps;
-      only_b[q] = 0u;
-      if (k < nch_b) {
-        const int i = k * 32 + lane;
-        const bool ob = i < n_b && (dup || !(flags_of(hkey(list_b[i], i >= nswa_b)) & 1u));
-        only_b[q] = __ballot_sync(0xffffffffu, ob);
-        const unsigned ob_swa = __ballot_sync(0xffffffffu, ob && i < nswa_b);
-        if (lane == 0) {
-          sm.only_b_chunk[k] = __popc(only_b[q]);
-          if (ob_swa) atomicAdd(&sm.only_b_swa, __popc(ob_swa));
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int k = warp + q * kWarps;
+        only_b[q] = 0u;
+        if (k < nch_b) {
+          const int i = k * 32 + lane;
+          bool ob = i < n_b;
+          if (ob && !all) {
+            const int ia = pair_claim_a<C::kHashSlots>(hkeys, hvals, &sm.dup, hkey(list_b[i], i >= nswa_b));
+            if (ia >= 0) shared_a[ia] = 1;
+            ob = ia < 0;
+          }
+          only_b[q] = __ballot_sync(0xffffffffu, ob);
+          const unsigned ob_swa = __ballot_sync(0xffffffffu, ob && i < nswa_b);
+          if (lane == 0) {
+            sm.only_b_chunk[k] = __popc(only_b[q]);
+            if (ob_swa) atomicAdd(&sm.only_b_swa, __popc(ob_swa));
+          }
         }
       }
-    }
+    };
+    const bool dup_a = sm.dup != 0;
+    count_only_b(dup_a);
     __syncthreads();
+    const bool dup = sm.dup != 0;
+    if (dup && !dup_a) {                   // B repeats a shared row: share nothing after all
+      if (tid == 0) sm.only_b_swa = 0;
+      __syncthreads();
+      count_only_b(true);
+      __syncthreads();
+    }
     const int bs = sm.only_b_swa;          // B-only SWA entries (they come first in B's order)
     const int nswa_u = nswa_a + bs;
     {
@@ -651,7 +637,7 @@ decode_tc_kernel(const __grid_constant__ TcParams P) {
         const bool comp = i >= nswa_a;
         const int e = comp ? nswa_u + (i - nswa_a) : i;
         idx_s[e] = row;
-        memb[e] = (uint8_t)(1u | ((!dup && (flags_of(hkey(row, comp)) & 2u)) ? 2u : 0u));
+        memb[e] = (uint8_t)(1u | ((!dup && shared_a[i]) ? 2u : 0u));
       }
     }
     __syncthreads();

@@ -117,6 +117,22 @@ constexpr int kQStageBytes = 128 * 512;          // Q rows staged in the R ring 
 static_assert(kNR * kEntry >= kQStageBytes, "Q staging fits in the R ring");
 constexpr int kOffIdx = kOffP + 2 * kPBytes;
 constexpr int kOffSmall = kOffIdx + kMaxCols * 4;
+// Token pairs (H = 64): a unit holds two tokens (heads in MMA rows 0-63 and
+// 64-127) over the union of their selected rows, each token at most
+// kPairCols columns per split so that the union fits the kMaxCols list.  The
+// union is built in the set-up with scratch in the V and K rings: a hash of
+// token A's rows (keys, A's list indices), each token's compacted list, one
+// membership byte per union entry, and one "B selects it too" byte per entry
+// of A's list.
+constexpr int kPairCols = kMaxCols / 2;
+constexpr int kPairTiles = kMaxCols / kNT + 2;   // the SWA and compressed runs may each end in a partial tile
+constexpr int kPairHash = 4096;                  // > kMaxCols: probing always ends
+constexpr int kScrVals = kPairHash * 4;
+constexpr int kScrListA = 2 * kPairHash * 4;
+constexpr int kScrListB = kScrListA + kPairCols * 4;
+constexpr int kScrMemb = kScrListB + kPairCols * 4;
+constexpr int kScrShared = kScrMemb + kMaxCols;
+static_assert(kScrShared + kPairCols <= kOffR - kOffV, "token-pair scratch fits in the V and K rings");
 constexpr uint32_t kBarStride = (uint32_t)sizeof(uint64_t);
 
 struct TcSmall {
@@ -139,6 +155,8 @@ struct TcSmall {
   uint64_t o_full;
   uint64_t qk0_done;
   uint64_t qk_done;
+  uint64_t mask_a[kPairTiles];           // token pairs: this CTA's own entries of tile j that token A selects
+  uint64_t mask_b[kPairTiles];           //              ... and token B
   float mx[2][2][128];
   float lpeer[128];
   float m_end[2][128];
@@ -147,6 +165,11 @@ struct TcSmall {
   int32_t chunk_off[kMaxChunks];
   int32_t nswa;
   int32_t nvalid;
+  // token pairs: token B's chunk counts, the chunk counts of B's rows that
+  // token A does not select, and the per-token list sizes
+  int32_t chunk_off_b[kMaxChunks];
+  int32_t only_b_chunk[kMaxChunks];
+  int32_t nswa_a, nswa_b, n_a, n_b, only_b_swa, dup;
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -168,7 +191,9 @@ struct SlotParams {
   DecodeParams p;
 };
 
-template <bool kPartial>
+// kPartial: split partials (num_splits > 1).  kPair: H = 64 and a unit is
+// (token pair, split), see kPairCols.
+template <bool kPartial, bool kPair>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
   const DecodeParams& p = P.p;
@@ -189,16 +214,18 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
   const int S = p.num_splits;
   const int unit = blockIdx.x >> 1;
   const int s = unit % S;
-  const int t = unit / S;
+  const int t = kPair ? 2 * (unit / S) : unit / S;   // the token (a pair: token A; token B is t + 1)
+  const bool has_b = kPair && t + 1 < p.sum_q;       // an odd token count leaves the last pair one token
   const int H = p.H;
+  const int rows_used = kPair ? (has_b ? 128 : 64) : H;   // MMA rows that carry a head
   // column range of this split (the grid kernel's rule)
   int per_split = (p.W + S - 1) / S;
   if (p.bt) per_split = (per_split + kNH - 1) / kNH * kNH;
   const int c0 = min(p.W, s * per_split);
   int c1 = min(p.W, c0 + per_split);
-  if (c1 - c0 > kMaxCols) {
+  if (c1 - c0 > (kPair ? kPairCols : kMaxCols)) {   // the planner prevents this
     if (p.err && tid == 0) atomicOr(p.err, SMLA_DEVERR_INTERNAL);
-    c1 = c0 + kMaxCols;
+    c1 = c0 + (kPair ? kPairCols : kMaxCols);
   }
 
   auto bar = [&](const uint64_t& b) { return smem_addr(&b); };
@@ -209,32 +236,46 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
   // the split's index columns first: they lead to the first gathers, while Q
   // is needed only by the first QK
   const int nchunks = (c1 - c0 + 31) / 32;
-  const int32_t* irow = p.ind + (int64_t)t * p.ind_stride;
+  auto load_cols = [&](int tok, int32_t (&r)[kChunksPerWarp]) {
+    const int32_t* irow = p.ind + (int64_t)tok * p.ind_stride;
+    if (p.bt == nullptr) {
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int col = c0 + (warp + q * kWarps) * 32 + lane;
+        r[q] = (col < c1) ? __ldg(irow + col) : -1;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int col = c0 + (warp + q * kWarps) * 32 + lane;
+        r[q] = -1;
+        if (col < c1) r[q] = col >= kSwaCols ? paged_row(p, tok, col - kSwaCols) : __ldg(irow + col);
+      }
+    }
+  };
   int32_t rv[kChunksPerWarp];
-  if (p.bt == nullptr) {
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = (col < c1) ? __ldg(irow + col) : -1;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int col = c0 + (warp + q * kWarps) * 32 + lane;
-      rv[q] = -1;
-      if (col < c1) rv[q] = col >= kSwaCols ? paged_row(p, t, col - kSwaCols) : __ldg(irow + col);
-    }
-  }
+  int32_t rvb[kChunksPerWarp];         // token pairs: token B's columns (unused otherwise)
+  load_cols(t, rv);
+  if (has_b) load_cols(t + 1, rvb);
   // Q rows staged in the R ring (free until the set-up's cluster barrier):
   // row h at 512 h, its 16-byte chunk c at chunk position c ^ (h % 32) so
-  // that the per-head reads below spread over the banks
-  const unsigned char* qrow = reinterpret_cast<const unsigned char*>(p.q) + (int64_t)t * p.q_stride_token;
-  for (int c = tid; c < H * 32; c += kThreads) {
+  // that the per-head reads below spread over the banks (a token pair: MMA
+  // row h is head h & 63 of token t + (h >> 6))
+  for (int c = tid; c < rows_used * 32; c += kThreads) {
     const int h = c >> 5, cc = c & 31;
-    cp_async_16(r_addr + h * 512 + ((cc ^ (h & 31)) << 4), qrow + (int64_t)h * kHeadDim + cc * 16);
+    const unsigned char* qrow = reinterpret_cast<const unsigned char*>(p.q) +
+                                (int64_t)(kPair ? t + (h >> 6) : t) * p.q_stride_token;
+    cp_async_16(r_addr + h * 512 + ((cc ^ (h & 31)) << 4), qrow + (int64_t)(kPair ? h & 63 : h) * kHeadDim + cc * 16);
   }
   const TokenInfo ti = token_info(p, t);
+  const int c1b_full = c1;
   c1 = min(c1, max(c0, ti.n_lim));
+  int c1b = c0, w_swa_b = 0;
+  if (has_b) {
+    const TokenInfo tib = token_info(p, t + 1);
+    c1b = min(c1b_full, max(c0, tib.n_lim));
+    w_swa_b = tib.w_swa;
+  }
   {
     // P rows of absent heads must read 0 (the softmax writes only the rows
     // of present heads).  The V and K rings are not zeroed whole: rows past
@@ -242,10 +283,22 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     // written is, so only those rows of an entry's first use are zeroed,
     // once the tiles are known (below; the R ring's entries are copies of
     // the peer's K entries)
-    if (H < 128) {
+    if (rows_used < 128) {
       const uint4 z = make_uint4(0, 0, 0, 0);
       uint4* zp = reinterpret_cast<uint4*>(base + kOffP);
       for (int i = tid; i < 2 * kPBytes / 16; i += kThreads) zp[i] = z;
+    }
+    uint32_t* hkeys = reinterpret_cast<uint32_t*>(base + kOffV);              // token pairs: set-up scratch
+    int32_t* hvals = reinterpret_cast<int32_t*>(base + kOffV + kScrVals);
+    int32_t* list_a = reinterpret_cast<int32_t*>(base + kOffV + kScrListA);
+    int32_t* list_b = reinterpret_cast<int32_t*>(base + kOffV + kScrListB);
+    uint8_t* memb = base + kOffV + kScrMemb;
+    uint8_t* shared_a = base + kOffV + kScrShared;
+    if constexpr (kPair) {
+      const uint4 e4 = make_uint4(kPairEmpty, kPairEmpty, kPairEmpty, kPairEmpty), z = make_uint4(0, 0, 0, 0);
+      for (int i = tid; i < kPairHash / 4; i += kThreads) reinterpret_cast<uint4*>(hkeys)[i] = e4;
+      for (int i = tid; i < kPairCols / 16; i += kThreads) reinterpret_cast<uint4*>(shared_a)[i] = z;
+      for (int i = tid; i < 2 * kPairTiles; i += kThreads) sm.mask_a[i] = 0ull;   // mask_b follows mask_a
     }
     if (tid == 0) {
       for (int i = 0; i < kNV; ++i) {
@@ -279,6 +332,7 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       mbar_init(bar(sm.qk_done), kQkWarps);
       sm.abort_flag = 0;
       sm.nswa = 0;
+      sm.nswa_a = sm.nswa_b = sm.only_b_swa = sm.dup = 0;
       fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) {
@@ -287,46 +341,48 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     }
     __syncthreads();
     tc_fence_after();
-    // compaction of the split's columns [c0, c1) into idx_s: valid SWA slots
-    // first, then valid compressed slots, each in column order
+    // a2 for one loaded column: the row, or -1 when the slot is masked (an
+    // index < -1 or past the pool is masked and flagged)
+    auto check_slot = [&](int idx, int col, int c1t, int w_swa) -> int {
+      if (col >= c1t) return -1;
+      const bool swa = col < kSwaCols;
+      if (idx == -1 || (swa && col >= w_swa)) return -1;
+      const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
+      if (idx < 0 || (int64_t)idx >= nrows) {
+        if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
+        return -1;
+      }
+      return idx;
+    };
+    // per-chunk valid counts of this warp's chunks (k = warp + q * kWarps)
+    // and the valid SWA slots, for one token's loaded columns (valid rows
+    // stay in r)
+    auto count_chunks = [&](int32_t (&r)[kChunksPerWarp], int c1t, int w_swa, int32_t* cnt, int32_t* nswa_out) {
 #pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int k = warp + q * kWarps;
-      if (k < nchunks) {
-        const int col = c0 + k * 32 + lane;
-        const int idx = rv[q];
-        rv[q] = -1;
-        if (col < c1) {
-          const bool swa = col < kSwaCols;
-          bool ok = idx != -1 && (!swa || col < ti.w_swa);
-          if (ok) {
-            const int64_t nrows = swa ? p.swa_rows : p.comp_rows;
-            if (idx < 0 || (int64_t)idx >= nrows) {
-              ok = false;
-              if (p.err && rank == 0) atomicOr(p.err, SMLA_DEVERR_INDEX_OUT_OF_RANGE);
-            }
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int k = warp + q * kWarps;
+        if (k < nchunks) {
+          const int col = c0 + k * 32 + lane;
+          r[q] = check_slot(r[q], col, c1t, w_swa);
+          const unsigned ball = __ballot_sync(0xffffffffu, r[q] >= 0);
+          const unsigned ball_swa = __ballot_sync(0xffffffffu, r[q] >= 0 && col < kSwaCols);
+          if (lane == 0) {
+            cnt[k] = __popc(ball);
+            if (ball_swa) atomicAdd(nswa_out, __popc(ball_swa));
           }
-          if (ok) rv[q] = idx;
-        }
-        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        const unsigned ball_swa = __ballot_sync(0xffffffffu, rv[q] >= 0 && col < kSwaCols);
-        if (lane == 0) {
-          sm.chunk_off[k] = __popc(ball);
-          if (ball_swa) atomicAdd(&sm.nswa, __popc(ball_swa));
         }
       }
-    }
-    __syncthreads();
+    };
     // every warp scans the chunk counts itself: lane L sums chunks 3L .. 3L + 2
     // (3 x 32 >= kMaxChunks), one shuffle ladder over the lanes, and each of
-    // the warp's chunks reads its base from the lane that holds it
+    // the warp's chunks reads its base from the lane that holds it; returns
+    // the total
     static_assert(3 * 32 >= kMaxChunks, "three chunks per lane");
-    int chunk_base[kChunksPerWarp];
-    {
+    auto scan_chunks = [&](const int32_t* cnt, int nch, int (&chunk_base)[kChunksPerWarp]) -> int {
       const int k3 = 3 * lane;
-      const int e0 = k3 < nchunks ? sm.chunk_off[k3] : 0;
-      const int e1 = k3 + 1 < nchunks ? sm.chunk_off[k3 + 1] : 0;
-      const int e2 = k3 + 2 < nchunks ? sm.chunk_off[k3 + 2] : 0;
+      const int e0 = k3 < nch ? cnt[k3] : 0;
+      const int e1 = k3 + 1 < nch ? cnt[k3 + 1] : 0;
+      const int e2 = k3 + 2 < nch ? cnt[k3 + 2] : 0;
       const int own = e0 + e1 + e2;
       int incl = own;
 #pragma unroll
@@ -343,15 +399,157 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
         const int a1 = __shfl_sync(0xffffffffu, e1, src);
         chunk_base[q] = ex + (r >= 1 ? a0 : 0) + (r >= 2 ? a1 : 0);
       }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      return __shfl_sync(0xffffffffu, incl, 31);
+    };
+    if constexpr (!kPair) {
+      // compaction of the split's columns [c0, c1) into idx_s: valid SWA
+      // slots first, then valid compressed slots, each in column order
+      count_chunks(rv, c1, ti.w_swa, sm.chunk_off, &sm.nswa);
+      __syncthreads();
+      int chunk_base[kChunksPerWarp];
+      const int total = scan_chunks(sm.chunk_off, nchunks, chunk_base);
       if (warp == 0 && lane == 0) sm.nvalid = total;
-    }
 #pragma unroll
-    for (int q = 0; q < kChunksPerWarp; ++q) {
-      const int k = warp + q * kWarps;
-      if (k < nchunks) {
-        const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
-        if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+      for (int q = 0; q < kChunksPerWarp; ++q) {
+        const int k = warp + q * kWarps;
+        if (k < nchunks) {
+          const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+          if (rv[q] >= 0) idx_s[chunk_base[q] + __popc(ball & ((1u << lane) - 1u))] = rv[q];
+        }
+      }
+    } else {
+      // f1, the rows shared by a pair's tokens gathered once (as in the
+      // token-pair form of the dims-split kernel): both tokens compacted,
+      // every valid (pool, row) hashed with a flag per token, and the union
+      //   [A SWA] [B-only SWA] [A compressed] [B-only compressed]
+      // built in B's order by ballot scans, so both CTAs build the same list;
+      // a token that selects a row twice makes the unit share nothing.
+      count_chunks(rv, c1, ti.w_swa, sm.chunk_off, &sm.nswa_a);
+      if (has_b) count_chunks(rvb, c1b, w_swa_b, sm.chunk_off_b, &sm.nswa_b);
+      __syncthreads();
+      const int nswa_a = sm.nswa_a, nswa_b = sm.nswa_b;
+      {
+        int chunk_base[kChunksPerWarp];
+        const int n_a = scan_chunks(sm.chunk_off, nchunks, chunk_base);
+        if (warp == 0 && lane == 0) sm.n_a = n_a;
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int k = warp + q * kWarps;
+          if (k < nchunks) {
+            const unsigned ball = __ballot_sync(0xffffffffu, rv[q] >= 0);
+            if (rv[q] >= 0) {
+              const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
+              list_a[e] = rv[q];
+              pair_insert_a<kPairHash>(hkeys, hvals, &sm.dup, pair_key(rv[q], e >= nswa_a), e);
+            }
+          }
+        }
+        int n_b = 0;
+        if (has_b) {
+          n_b = scan_chunks(sm.chunk_off_b, nchunks, chunk_base);
+#pragma unroll
+          for (int q = 0; q < kChunksPerWarp; ++q) {
+            const int k = warp + q * kWarps;
+            if (k < nchunks) {
+              const unsigned ball = __ballot_sync(0xffffffffu, rvb[q] >= 0);
+              if (rvb[q] >= 0) {
+                const int e = chunk_base[q] + __popc(ball & ((1u << lane) - 1u));
+                list_b[e] = rvb[q];
+              }
+            }
+          }
+        }
+        if (warp == 0 && lane == 0) sm.n_b = n_b;
+      }
+      __syncthreads();
+      const int n_a = sm.n_a, n_b = sm.n_b;
+      // B's entries that A does not select (all of them once a repeat is
+      // known), counted per 32-entry chunk of B's list; a B entry that A
+      // selects claims A's entry and marks it shared
+      const int nch_b = (n_b + 31) / 32;
+      unsigned only_b[kChunksPerWarp];
+      auto count_only_b = [&](bool all) {
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int k = warp + q * kWarps;
+          only_b[q] = 0u;
+          if (k < nch_b) {
+            const int i = k * 32 + lane;
+            bool ob = i < n_b;
+            if (ob && !all) {
+              const int ia = pair_claim_a<kPairHash>(hkeys, hvals, &sm.dup, pair_key(list_b[i], i >= nswa_b));
+              if (ia >= 0) shared_a[ia] = 1;
+              ob = ia < 0;
+            }
+            only_b[q] = __ballot_sync(0xffffffffu, ob);
+            const unsigned ob_swa = __ballot_sync(0xffffffffu, ob && i < nswa_b);
+            if (lane == 0) {
+              sm.only_b_chunk[k] = __popc(only_b[q]);
+              if (ob_swa) atomicAdd(&sm.only_b_swa, __popc(ob_swa));
+            }
+          }
+        }
+      };
+      const bool dup_a = sm.dup != 0;
+      count_only_b(dup_a);
+      __syncthreads();
+      const bool dup = sm.dup != 0;
+      if (dup && !dup_a) {                 // B repeats a shared row: share nothing after all
+        if (tid == 0) sm.only_b_swa = 0;
+        __syncthreads();
+        count_only_b(true);
+        __syncthreads();
+      }
+      const int bs = sm.only_b_swa;        // B-only SWA entries (they come first in B's order)
+      const int nswa_u = nswa_a + bs;
+      {
+        int chunk_base[kChunksPerWarp];
+        const int n_only = scan_chunks(sm.only_b_chunk, nch_b, chunk_base);
+        if (warp == 0 && lane == 0) {
+          sm.nswa = nswa_u;
+          sm.nvalid = n_a + n_only;
+        }
+#pragma unroll
+        for (int q = 0; q < kChunksPerWarp; ++q) {
+          const int k = warp + q * kWarps;
+          if (k < nch_b && ((only_b[q] >> lane) & 1u)) {
+            const int r = chunk_base[q] + __popc(only_b[q] & ((1u << lane) - 1u));
+            const int e = r < bs ? nswa_a + r : nswa_u + (n_a - nswa_a) + (r - bs);
+            idx_s[e] = list_b[k * 32 + lane];
+            memb[e] = 2;
+          }
+        }
+        for (int i = tid; i < n_a; i += kThreads) {
+          const int row = list_a[i];
+          const bool comp = i >= nswa_a;
+          const int e = comp ? nswa_u + (i - nswa_a) : i;
+          idx_s[e] = row;
+          memb[e] = (uint8_t)(1u | ((!dup && shared_a[i]) ? 2u : 0u));
+        }
+      }
+      __syncthreads();
+      {
+        // this CTA's own entries of every 128-entry tile: bit i of mask_x[j]
+        // is own entry i (list entry tile_start(j) + 64 rank + i)
+        const int nsw = sm.nswa, nva = sm.nvalid;
+        const int tsw = (nsw + kNT - 1) / kNT;
+        const int nt = tsw + (nva - nsw + kNT - 1) / kNT;
+        for (int j = warp; j < nt; j += kWarps) {
+          const int start = (j < tsw ? j * kNT : nsw + (j - tsw) * kNT) + kNH * (int)rank;
+          const int n = max(0, min(kNH, (j < tsw ? nsw : nva) - start));
+          uint64_t ma = 0ull, mb = 0ull;
+#pragma unroll
+          for (int hb = 0; hb < kNH / 32; ++hb) {
+            const int i = hb * 32 + lane;
+            const uint32_t m = i < n ? memb[start + i] : 0u;
+            ma |= (uint64_t)__ballot_sync(0xffffffffu, (m & 1u) != 0u) << (32 * hb);
+            mb |= (uint64_t)__ballot_sync(0xffffffffu, (m & 2u) != 0u) << (32 * hb);
+          }
+          if (lane == 0) {
+            sm.mask_a[j] = ma;
+            sm.mask_b[j] = mb;
+          }
+        }
       }
     }
     // Q into tensor memory: softmax warp (g, quadrant) writes dims
@@ -391,7 +589,7 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int cc = g_sm * 16 + half * 8 + i;
-          const uint4 x = h < H ? *reinterpret_cast<const uint4*>(qs + ((cc ^ (h & 31)) << 4)) : make_uint4(0, 0, 0, 0);
+          const uint4 x = h < rows_used ? *reinterpret_cast<const uint4*>(qs + ((cc ^ (h & 31)) << 4)) : make_uint4(0, 0, 0, 0);
           r[4 * i] = x.x;
           r[4 * i + 1] = x.y;
           r[4 * i + 2] = x.z;
@@ -576,15 +774,16 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     regs_increase<kRegsSoftmax>();
     const int g = (warp - kSoftmaxWarp0) >> 2;        // warpgroup: tiles j with j % 2 == g
     const int q4 = warp & 3;                           // TMEM lane quadrant of this warp
-    const int h = q4 * 32 + lane;
-    const bool active = q4 * 32 < H;                   // warp-uniform
+    const int h = q4 * 32 + lane;                      // MMA row (a token pair: head h & 63 of token t + (h >> 6))
+    const bool active = q4 * 32 < rows_used;           // warp-uniform
+    const uint64_t* my_mask = (h < 64) ? sm.mask_a : sm.mask_b;   // token pairs: this row's own entries
     const bool leader = (warp - kSoftmaxWarp0) % 4 == 0 && lane == 0;   // one thread per warpgroup (quadrant 0: active)
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     // BF16 partial staging: warpgroup g's 128 rows of 256 bytes in half of
     // the V ring (read by nothing but this CTA's QK and PV, done by then)
     auto stage_row = [&](int sg, int r) -> unsigned char* { return base + kOffV + sg * (128 * 256) + r * 256; };
     const float c = load_scale(p.bmm1, p.bmm1_dev) * kLog2e;
-    const uint32_t mx_bytes = (uint32_t)(H * 4);
+    const uint32_t mx_bytes = (uint32_t)(rows_used * 4);
     // the peer's copy of a TcSmall field: one mapped base plus the field's offset
     const uint32_t small_local = smem_addr(&sm);
     const uint32_t small_peer = map_to_rank(small_local, peer);
@@ -602,7 +801,9 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     float m_last = -INFINITY, l_run = 0.f;
     // E4M3 P keeps 3 mantissa bits: short splits move the reference on every
     // new maximum (the same choice in both CTAs: nvalid is the pair's)
-    const float thr = nvalid <= kExactRefSlots ? 0.f : kRescaleThreshold;
+    // (a token pair: by the slot count of the row's own token)
+    const int n_row = kPair ? (h < 64 ? sm.n_a : sm.n_b) : nvalid;
+    const float thr = n_row <= kExactRefSlots ? 0.f : kRescaleThreshold;
     bool ok = true;
     int j = g;
     const uint64_t c2 = f2_pack(c, c);
@@ -631,7 +832,13 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
 #pragma unroll
         for (int i = 0; i < kNH; i += 2) f2_unpack(f2_mul(f2_pack(sv[i], sv[i + 1]), c2), sv[i], sv[i + 1]);
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (n_own >= kNH) {
+        if constexpr (kPair) {
+          // only the entries of this row's token (the tile's other entries are the other token's)
+          const uint64_t mrow = my_mask[j];
+#pragma unroll
+          for (int i = 0; i < kNH; ++i)
+            if ((mrow >> i) & 1ull) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
+        } else if (n_own >= kNH) {
 #pragma unroll
           for (int i = 0; i < kNH; ++i) m4[i & 3] = fmaxf(m4[i & 3], sv[i]);
         } else {
@@ -675,7 +882,12 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
           sv[i] = fast_exp2(x0);
           sv[i + 1] = fast_exp2(x1);
         }
-        if (n_own < kNH) {
+        if constexpr (kPair) {
+          const uint64_t mrow = my_mask[j];
+#pragma unroll
+          for (int i = 0; i < kNH; ++i)
+            if (!((mrow >> i) & 1ull)) sv[i] = 0.f;
+        } else if (n_own < kNH) {
 #pragma unroll
           for (int i = 0; i < kNH; ++i)
             if (i >= n_own) sv[i] = 0.f;
@@ -764,9 +976,9 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       float f = have ? 1.f / l_tot : 0.f;
       if (S == 1) {
         f *= load_scale(p.bmm2, p.bmm2_dev);
-        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + h) * kLog2e - lse));
+        if (p.sinks != nullptr && have) f *= 1.f / (1.f + fast_exp2(__ldg(p.sinks + (kPair ? (h & 63) : h)) * kLog2e - lse));
       }
-      const int64_t row_th = (int64_t)t * H + h;
+      const int64_t row_th = kPair ? (int64_t)(t + (h >> 6)) * H + (h & 63) : (int64_t)t * H + h;
       // The normalised BF16 rows go through shared memory, so that the
       // global stores below are whole 256-byte row segments rather than one
       // 16-byte piece per row per warp instruction: warpgroup g stages its
@@ -808,9 +1020,10 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       const int w4 = (warp - kSoftmaxWarp0) & 3;
       const int col0 = (int)rank * kHalfDims + g * (kHalfDims / 2);
       const int cidx = lane & 15;
-      for (int r = w4 + 4 * (lane >> 4); r < H; r += 8) {
+      for (int r = w4 + 4 * (lane >> 4); r < rows_used; r += 8) {
         const uint4 x = *reinterpret_cast<const uint4*>(stage_row(g, r) + ((cidx ^ (r & 7)) << 4));
-        const int64_t orow = kPartial ? ((int64_t)t * H + r) * S + s : (int64_t)t * H + r;
+        const int64_t row = kPair ? (int64_t)(t + (r >> 6)) * H + (r & 63) : (int64_t)t * H + r;
+        const int64_t orow = kPartial ? row * S + s : row;
         *reinterpret_cast<uint4*>((kPartial ? p.part_o : p.out) + orow * kHeadDim + col0 + cidx * 8) = x;
       }
     }
@@ -833,8 +1046,9 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
 int tc_slot_smem_bytes() { return kSmemBytes; }
 int tc_slot_threads() { return kThreads; }
 
-cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, bool pair, cudaStream_t stream) {
   if (p.dtype != SMLA_E4M3) return cudaErrorInvalidValue;
+  if (pair && p.H != 64) return cudaErrorInvalidValue;   // two tokens of 64 heads fill the 128 MMA rows
   SlotParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
@@ -849,8 +1063,8 @@ cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, cudaStream_t 
   auto launch = [&](auto kernel) -> cudaError_t {
     // the register split waits until the launch holds the registers it hands
     // out: refuse a build whose per-thread count is below the one it was sized for
-    static std::atomic<int> launch_regs[2];            // per kernel (single split, split partials)
-    std::atomic<int>& cached = launch_regs[p.num_splits > 1 ? 1 : 0];
+    static std::atomic<int> launch_regs[4];            // per kernel (single split, split partials; x token pairs)
+    std::atomic<int>& cached = launch_regs[(p.num_splits > 1 ? 1 : 0) + (pair ? 2 : 0)];
     int regs = cached.load(std::memory_order_relaxed);
     if (regs == 0) {
       cudaFuncAttributes fa;
@@ -865,7 +1079,10 @@ cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, cudaStream_t 
     kernel<<<grid, kThreads, kSmemBytes, stream>>>(P);
     return cudaSuccess;
   };
-  e = p.num_splits > 1 ? launch(decode_tc_slot_kernel<true>) : launch(decode_tc_slot_kernel<false>);
+  if (pair)
+    e = p.num_splits > 1 ? launch(decode_tc_slot_kernel<true, true>) : launch(decode_tc_slot_kernel<false, true>);
+  else
+    e = p.num_splits > 1 ? launch(decode_tc_slot_kernel<true, false>) : launch(decode_tc_slot_kernel<false, false>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

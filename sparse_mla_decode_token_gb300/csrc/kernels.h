@@ -45,9 +45,12 @@ cudaError_t launch_decode_tc_head_owned(const DecodeParams& p, int grid, cudaStr
 // tcgen05 decode kernel for E4M3 rows with the slot-split pair
 // (decode_tc_slot.cu): a 2-CTA cluster per (token, split), same column limit;
 // each CTA computes the full logits of its half of every 128-slot tile.
+// pair = true (H = 64 only): per (token pair, split) over the union of the two
+// tokens' rows, at most SMLA_TC_MAX_SPLIT_COLS / 2 columns of each token per
+// split; grid = 2 ceil(T / 2) S.
 int tc_slot_smem_bytes();
 int tc_slot_threads();
-cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc_slot(const DecodeParams& p, int grid, bool pair, cudaStream_t stream);
 
 // Split-K log-sum-exp combine (combine.cu)
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);

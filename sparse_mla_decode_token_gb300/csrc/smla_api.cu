@@ -211,11 +211,18 @@ smla_status validate_host(const smla_args* a) {
 // Kernel and schedule that SMLA_KERNEL_AUTO / SMLA_SCHEDULE_AUTO select: the
 // slot-split kernel for E4M3 rows (unless the balanced schedule is asked
 // for, which only the dims-split kernel runs), the dims-split kernel for BF16.
+// E4M3 rows with 64 heads, at most SMLA_TC_MAX_SPLIT_COLS / 2 columns and
+// more tokens than SM pairs take the slot-split kernel's token-pair form:
+// half the units, so one wave fewer (measured 8-10 % faster at 128 and 300
+// tokens of 640 columns, even at 152 tokens of 1152; slower when one wave
+// holds every token anyway).
 constexpr int kAutoSchedule = SMLA_SCHEDULE_GRID;
-int auto_kernel(const smla_args* a) {
+int auto_kernel(const smla_args* a, int sms) {
   const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
-  return a->dtype == SMLA_E4M3 && schedule != SMLA_SCHEDULE_BALANCED ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
-                                                                     : SMLA_KERNEL_TCGEN05;
+  if (a->dtype != SMLA_E4M3 || schedule == SMLA_SCHEDULE_BALANCED) return SMLA_KERNEL_TCGEN05;
+  if (a->num_heads == 64 && a->width <= SMLA_TC_MAX_SPLIT_COLS / 2 && a->sum_q > sms / 2)
+    return SMLA_KERNEL_TCGEN05_TOKEN_PAIRS;
+  return SMLA_KERNEL_TCGEN05_SLOT_SPLIT;
 }
 
 std::atomic<int> g_sm_count[64];   // per device; 0 = not queried yet (callers may be on several threads)
@@ -244,7 +251,7 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
   // take them.
   const int kernel = packed_dtype(a->dtype)
                          ? (a->kernel == SMLA_KERNEL_CUDA_CORE ? SMLA_KERNEL_CUDA_CORE : SMLA_KERNEL_TCGEN05)
-                     : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a)
+                     : a->kernel == SMLA_KERNEL_AUTO ? auto_kernel(a, sms)
                                                      : a->kernel;
   int S = a->num_splits;
   // token units of the grid: tokens, or token pairs for the token-pair kernel
@@ -258,22 +265,27 @@ smla_status plan_checked(const smla_args* a, int sms, smla_plan* plan) {
     const bool head_owned = kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED && a->dtype == SMLA_E4M3;
     const bool slot_split = kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT && a->dtype == SMLA_E4M3;
     const bool pairs_of_tokens = kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS && a->num_heads == 64;
+    // E4M3 token pairs run the slot-split kernel's pair form, whose union list
+    // holds at most SMLA_TC_MAX_SPLIT_COLS entries: half of that per token
+    const bool slot_pairs = pairs_of_tokens && a->dtype == SMLA_E4M3;
+    const int col_cap = slot_pairs ? SMLA_TC_MAX_SPLIT_COLS / 2 : SMLA_TC_MAX_SPLIT_COLS;
     plan->kernel = head_owned        ? SMLA_KERNEL_TCGEN05_HEAD_OWNED
                    : slot_split      ? SMLA_KERNEL_TCGEN05_SLOT_SPLIT
                    : pairs_of_tokens ? SMLA_KERNEL_TCGEN05_TOKEN_PAIRS
                                      : SMLA_KERNEL_TCGEN05;
     if (pairs_of_tokens) units = (a->sum_q + 1) / 2;
     plan->ctas_per_split = 2;
-    plan->threads = head_owned ? tc_head_owned_threads() : slot_split ? tc_slot_threads() : tc_grid_threads();
-    plan->smem_bytes = head_owned   ? tc_head_owned_smem_bytes()
-                       : slot_split ? tc_slot_smem_bytes()
-                                    : tc_grid_smem_bytes(a->dtype, pairs_of_tokens);
-    const int s_min = (a->width + SMLA_TC_MAX_SPLIT_COLS - 1) / SMLA_TC_MAX_SPLIT_COLS;
+    plan->threads = head_owned ? tc_head_owned_threads()
+                    : (slot_split || slot_pairs) ? tc_slot_threads() : tc_grid_threads();
+    plan->smem_bytes = head_owned                   ? tc_head_owned_smem_bytes()
+                       : (slot_split || slot_pairs) ? tc_slot_smem_bytes()
+                                                    : tc_grid_smem_bytes(a->dtype, pairs_of_tokens);
+    const int s_min = (a->width + col_cap - 1) / col_cap;
     if (s_min > SMLA_MAX_SPLITS)
       return fail(SMLA_ERR_UNSUPPORTED, "width %d needs more than %d splits", a->width, SMLA_MAX_SPLITS);
     if (S != 0 && S < s_min)
       return fail(SMLA_ERR_INVALID_ARG, "num_splits %d < %d: the tcgen05 kernel takes at most %d columns per split",
-                  S, s_min, SMLA_TC_MAX_SPLIT_COLS);
+                  S, s_min, col_cap);
     const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
     const int schedule = a->schedule == SMLA_SCHEDULE_AUTO ? kAutoSchedule : a->schedule;
     if (schedule == SMLA_SCHEDULE_BALANCED && S == 0 && a->max_splits == 0 && !head_owned && !slot_split &&
@@ -479,7 +491,9 @@ smla_status smla_decode(const smla_args* a, void* stream_ptr) {
   if (plan.kernel == SMLA_KERNEL_TCGEN05_HEAD_OWNED)
     ce = launch_decode_tc_head_owned(p, plan.grid, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05_SLOT_SPLIT)
-    ce = launch_decode_tc_slot(p, plan.grid, stream);
+    ce = launch_decode_tc_slot(p, plan.grid, false, stream);
+  else if (plan.kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS && a->dtype == SMLA_E4M3)
+    ce = launch_decode_tc_slot(p, plan.grid, true, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05 && plan.clusters > 0)
     ce = launch_decode_tc(p, plan.grid, plan.clusters, piece_o, piece_lse, piece_cnt, stream);
   else if (plan.kernel == SMLA_KERNEL_TCGEN05 || plan.kernel == SMLA_KERNEL_TCGEN05_TOKEN_PAIRS)

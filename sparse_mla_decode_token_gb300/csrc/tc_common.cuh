@@ -72,5 +72,70 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ---------------------------------------------------------------- token pairs
+// The union of two tokens' selected rows (the token-pair forms of the
+// tcgen05 kernels).  Token A's rows go into an open-addressing hash in shared
+// memory, keyed by (pool, row), each key with A's list index; token B's rows
+// look themselves up.  A B row found in A claims A's entry (the sign bit of
+// the index): a second claim means B selects a row A selects twice over, and
+// a key already present when A inserts means A selects a row twice; either
+// sets *dup, and the unit then shares nothing (a shared entry cannot count
+// one token's row twice).  B rows that A does not select stay B's own
+// entries, repeats included.  kHashSlots is a power of two larger than the
+// keys, so probing always ends.
+// (Out of line: the set-up code of a unit runs once, cold in the instruction
+// cache, so its size is what it costs.)
+constexpr uint32_t kPairEmpty = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t pair_key(int row, bool comp) {
+  return (uint32_t)row | (comp ? 0x80000000u : 0u);
+}
+
+template <int kHashSlots>
+__device__ __forceinline__ uint32_t pair_slot(uint32_t key) {
+  static_assert((kHashSlots & (kHashSlots - 1)) == 0, "power of two");
+  return (key * 2654435761u) >> (32 - __builtin_ctz(kHashSlots));
+}
+
+// token A's row (list index a): one slot per key
+template <int kHashSlots>
+__device__ __noinline__ void pair_insert_a(uint32_t* keys, int32_t* vals, int32_t* dup, uint32_t key, int a) {
+  if (key == kPairEmpty) {                                    // would read as empty
+    *dup = 1;
+    return;
+  }
+  uint32_t h = pair_slot<kHashSlots>(key);
+  for (int probe = 0; probe < kHashSlots; ++probe) {
+    const uint32_t prev = atomicCAS(keys + h, kPairEmpty, key);
+    if (prev == kPairEmpty) {
+      vals[h] = a;
+      return;
+    }
+    if (prev == key) {                                        // token A selects the row twice
+      *dup = 1;
+      return;
+    }
+    h = (h + 1) & (kHashSlots - 1);
+  }
+  *dup = 1;                                                   // not reached: more slots than keys
+}
+
+// token B's row: A's list index of the same row (claimed for B), or -1
+template <int kHashSlots>
+__device__ __noinline__ int pair_claim_a(const uint32_t* keys, int32_t* vals, int32_t* dup, uint32_t key) {
+  uint32_t h = pair_slot<kHashSlots>(key);
+  for (int probe = 0; probe < kHashSlots; ++probe) {
+    const uint32_t k = keys[h];
+    if (k == key) {
+      const int32_t old = atomicOr(vals + h, (int32_t)0x80000000);
+      if (old < 0) *dup = 1;                                  // B's second entry of a row A selects
+      return old & 0x7fffffff;
+    }
+    if (k == kPairEmpty) return -1;
+    h = (h + 1) & (kHashSlots - 1);
+  }
+  return -1;
+}
+
 }  // namespace tc
 }  // namespace smla

@@ -168,12 +168,34 @@ def test_token_pair_plan_rule(T, W_, dtype):
         assert p["kernel"] == B.KERNEL_TCGEN05_TOKEN_PAIRS and p["clusters"] == 0
         S = p["num_splits"]
         # as many splits as keep one wave of units, at least 64 union columns
-        # (up to 2W) per split, and at most 2304 columns of each token
+        # (up to 2W) per split, and at most 2304 columns of each token (1152
+        # for E4M3, whose pairs run the slot-split kernel's pair form)
+        cap = 1152 if dtype == B.SMLA_E4M3 else 2304
         want = min(GB300_SMS // 2 // U, math.ceil(2 * W_ / 64), 32)
-        assert S == max(want, math.ceil(W_ / 2304), 1)
+        assert S == max(want, math.ceil(W_ / cap), 1)
+        slot = plan(args(T, W_, dtype=B.SMLA_E4M3, kernel=B.KERNEL_TCGEN05_SLOT_SPLIT))
+        if dtype == B.SMLA_E4M3:
+            assert p["smem_bytes"] == slot["smem_bytes"]
         assert p["grid"] == 2 * U * S and p["ctas_per_split"] == 2
         assert p["workspace_bytes"] == (0 if S == 1 else workspace(T * 64 * S))
         assert p["threads"] == 512 and p["smem_bytes"] <= 232448
+
+
+def test_auto_takes_token_pairs_for_e4m3_64_heads_past_a_wave():
+    """AUTO: E4M3 rows with 64 heads, at most 1152 columns and more tokens
+    than SM pairs run the slot-split kernel's token-pair form; otherwise the
+    slot-split kernel (and BF16 rows the dims-split kernel)."""
+    pairs = GB300_SMS // 2
+    for T, W_, want in [(pairs + 1, 640, B.KERNEL_TCGEN05_TOKEN_PAIRS), (300, 1152, B.KERNEL_TCGEN05_TOKEN_PAIRS),
+                        (pairs, 640, B.KERNEL_TCGEN05_SLOT_SPLIT), (300, 1153, B.KERNEL_TCGEN05_SLOT_SPLIT),
+                        (300, 2176, B.KERNEL_TCGEN05_SLOT_SPLIT)]:
+        p = plan(args(T, W_, H=64))
+        assert p["kernel"] == want, (T, W_, p)
+        if want == B.KERNEL_TCGEN05_TOKEN_PAIRS:
+            assert p["grid"] == 2 * ((T + 1) // 2) * p["num_splits"]
+    assert plan(args(300, 640, H=128))["kernel"] == B.KERNEL_TCGEN05_SLOT_SPLIT
+    assert plan(args(300, 640, H=64, dtype=B.SMLA_BF16))["kernel"] == B.KERNEL_TCGEN05
+    assert plan(args(300, 640, H=64, schedule=B.SCHEDULE_BALANCED))["kernel"] == B.KERNEL_TCGEN05
 
 
 def test_token_pair_form_needs_64_heads():

@@ -57,6 +57,29 @@ def pair_case(seed, *, dtype="bf16", q_lens=(2, 3, 1, 2), width=128 + 300, overl
     return w
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("overlap", ["none", "shuffle"])
+def test_wide_tables(dtype, overlap):
+    """128 + 2048 columns: the E4M3 pair form takes at most 1152 columns of
+    each token per split (two splits at least), the BF16 one up to 2304."""
+    w = pair_case(780, dtype=dtype, q_lens=(2, 2, 1), width=128 + 2048, overlap=overlap, comp_rows=65536)
+    out, lse, plan = run_gpu(w, kernel=PAIRS)
+    check_plan(plan, w.sum_q)
+    assert plan["num_splits"] >= (2 if dtype == "e4m3" else 1)
+    compare(w, out, lse)
+
+
+def test_auto_takes_pairs_past_a_wave():
+    """AUTO runs the slot-split kernel's token-pair form for E4M3 rows with
+    64 heads, at most 1152 columns and more tokens than SM pairs (here 160
+    tokens of 128 + 512 columns, requests of two tokens): every token against
+    the oracle."""
+    w = pair_case(790, dtype="e4m3", q_lens=[2] * 80, width=128 + 512, overlap="half")
+    out, lse, plan = run_gpu(w)
+    check_plan(plan, w.sum_q)
+    compare(w, out, lse)
+
+
 def check_plan(plan, T, splits=None):
     assert plan["kernel"] == PAIRS
     S = plan["num_splits"]
@@ -103,13 +126,14 @@ def test_same_row_number_in_other_pool_is_not_shared(dtype):
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("splits", [1, 2])
-def test_odd_tokens_empty_tokens_and_many_units(splits):
+def test_odd_tokens_empty_tokens_and_many_units(dtype, splits):
     """301 tokens (151 units: more than the SM pairs, and a last unit of one
     token), every fifth token with no active slot, every seventh with only
     SWA slots."""
     T = 301
-    w = pair_case(740 + splits, dtype="bf16", q_lens=[2] * 150 + [1], width=128 + 200, overlap="shuffle")
+    w = pair_case(740 + splits, dtype=dtype, q_lens=[2] * 150 + [1], width=128 + 200, overlap="shuffle")
     w.indices[::5, :] = -1
     w.topk_lens = np.asarray(w.topk_lens).copy()
     w.topk_lens[::7] = 128
@@ -118,10 +142,11 @@ def test_odd_tokens_empty_tokens_and_many_units(splits):
     compare(w, out, lse)
 
 
-def test_pairs_page_table_form():
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_pairs_page_table_form(dtype):
     """Compressed segment from per-token page tables (consecutive tokens of a
     request share their request's pages), per-row window lengths."""
-    w = W.make_paged_workload(seed=750, dtype="bf16", batch=3, q_lens=[2, 3, 2], num_heads=64,
+    w = W.make_paged_workload(seed=750, dtype=dtype, batch=3, q_lens=[2, 3, 2], num_heads=64,
                               swa_rows=3 * 130 + 10, comp_pages=64, page_size=64, max_pages=5,
                               hca_seq_lens=[128 + 300, 128 + 64, 200], seq_lens=[5000, 900, 3000],
                               ring_len=130, topk_lens=np.full(7, 128 + 320), swa_topk_lens=[128, 17, 0, 64, 128, 90, 128],
