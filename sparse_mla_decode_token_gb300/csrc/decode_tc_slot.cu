@@ -41,6 +41,12 @@
 // maxima to its peer, against 48 KB of 24-bit partial logits in the dims-split
 // kernel, and runs the exponentials of its own 64 slots only.
 //
+// kPair (64 heads): a unit holds two tokens, their heads in MMA rows 0-63 and
+// 64-127, over the union of their selected rows (built in the set-up, see
+// kPairCols); each softmax row masks the other token's entries.  The P halves
+// and maxima already carry 128 rows, so the second token's heads travel free
+// and the per-unit fixed cost is paid once per two tokens.
+//
 // The operation follows the FlashInfer trtllm_batch_decode_sparse_mla_dsv4 page
 // (description, SM100/SM103 paragraph; Parameters); the base-2 LSE, the sink in
 // the normaliser and the split partials follow the cake_sparse_mla_sm120 page
