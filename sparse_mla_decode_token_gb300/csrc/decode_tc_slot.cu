@@ -16,12 +16,13 @@
 //                       K ring (rings below); the tile's 64 requests spread
 //                       over the four warps; 64 consecutive rows are one box
 //                       copy per column block
-//   QK warps 4-5        first copy the peer's output half of the landed own
-//                       rows (16 KB) into the peer's stage with one DSMEM bulk
-//                       copy, then S_r = Q K_own^T (M = 128 heads, N = 64 own
-//                       slots, K = 512 dims; Q is read from tensor memory)
-//                       into one of two TMEM S buffers, warp 4 + b issuing
-//                       the tiles of buffer b
+//   QK warps 4-5        warp 4 first copies the peer's output half of the
+//                       landed own rows (16 KB) into the peer's stage with one
+//                       DSMEM bulk copy, then S_r = Q K_own^T (M = 128 heads, N = 64 own
+//                       slots, K = 512 dims; Q is read from tensor memory):
+//                       warp 4 + q issues the eight MMAs of dims
+//                       [256 q, 256 q + 256) into half q of the TMEM S area,
+//                       so a tile's QK runs as two chains that the softmax adds
 //   PV warp 7           O_r += P V_r (M = 128 heads, N = 256 output dims, K =
 //                       128 slots): P from shared memory (this CTA's half
 //                       written by its softmax, the peer's half copied in), V
@@ -77,7 +78,7 @@ constexpr int kNT = 2 * kNH;                     // slots per tile (the pair's)
 constexpr int kHalfDims = 256;                   // output dims per CTA
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = kProducerWarps;         // first QK issuer; allocates and frees TMEM
-constexpr int kQkWarps = 2;                      // one per S buffer; warp 6 has no role
+constexpr int kQkWarps = 2;                      // one per half of the QK (K steps 0-7, 8-15); warp 6 has no role
 constexpr int kPvWarp = 7;
 constexpr int kSoftmaxWarp0 = 8;
 constexpr int kSoftmaxWarps = 8;
@@ -99,9 +100,9 @@ constexpr int kChunksPerWarp = (kMaxChunks + kWarps - 1) / kWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;                    // O: 256 fp32 columns
 constexpr uint32_t kQCol = 256;                  // Q: 128 columns of four E4M3 values (dims 4c .. 4c + 3)
-constexpr uint32_t kSCol = 384;                  // S: two buffers of 64 fp32 columns
-constexpr int kSBufs = 2;
-static_assert(kQkWarps == kSBufs, "one QK issuer per S buffer");
+constexpr uint32_t kSCol = 384;                  // S: a tile's two partial logits (64 fp32 columns each)
+constexpr int kSBufs = 2;                        // s_full / s_empty barrier sets, one per softmax warpgroup
+static_assert(kQkWarps == 2, "one QK issuer per half of the S area");
 static_assert(kSCol + kSBufs * kNH == kTmemCols, "tensor memory budget");
 constexpr float kRescaleThreshold = 8.f;         // log2 units: P stays <= 2^8
 constexpr int kExactRefSlots = 512;              // E4M3 P: splits of at most this many slots follow the exact maximum
@@ -311,7 +312,7 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
         mbar_init(bar(sm.kv_full[i]), 1);
         mbar_init(bar(sm.v_empty[i]), 1);
       }
-      for (int i = 0; i < kNK; ++i) mbar_init(bar(sm.k_empty[i]), 2);
+      for (int i = 0; i < kNK; ++i) mbar_init(bar(sm.k_empty[i]), 3);   // two QK halves + the peer's acknowledgement
       for (int i = 0; i < kNR; ++i) {
         mbar_init(bar(sm.r_full[i]), 1);
         mbar_init(bar(sm.r_empty[i]), 1);
@@ -319,7 +320,7 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
         mbar_init(bar(sm.r_seen[i]), 1);
       }
       for (int b = 0; b < kSBufs; ++b) {
-        mbar_init(bar(sm.s_full[b]), 1);
+        mbar_init(bar(sm.s_full[b]), kQkWarps);   // one commit per QK half
         mbar_init(bar(sm.s_empty[b]), kSoftmaxWarps / 2);
       }
       for (int b = 0; b < 2; ++b) {
@@ -689,48 +690,59 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
     regs_decrease<kRegsMma>();
     if (warp < kMmaWarp + kQkWarps) {
     // ============================================================ QK issue
+    // Both QK warps take every tile: warp 4 + qi issues the K steps
+    // 8 qi .. 8 qi + 7 (dims 256 qi .. 256 qi + 255) into half qi of the S
+    // area, so a tile's 16 dependent MMAs run as two chains of eight that the
+    // softmax adds.  Warp 4 also copies the tile's K entry to the peer and
+    // acknowledges the peer's copy of the tile.
     constexpr uint32_t idesc_qk = idesc(true, 128, kNH, false);
     const int qi = warp - kMmaWarp;
     const uint32_t r_dst0 = map_to_rank(r_addr, peer);
     const uint32_t r_full_peer = map_to_rank(bar(sm.r_full[0]), peer);
     const uint32_t k_empty_peer = map_to_rank(bar(sm.k_empty[0]), peer);
-    for (int k = qi; k < ntiles; k += kQkWarps) {
+    for (int k = 0; k < ntiles; ++k) {
       const int iv = k % kNV, ik = k % kNK, ir = k % kNR;
       if (!warp_wait(cx, bar(sm.kv_full[iv]), (k / kNV) & 1)) break;
-      // the peer's output half of the own rows (the K entry) into the peer's
-      // R entry, once the peer has released it
-      if (!warp_wait(cx, bar(sm.r_free[ir]), (k / kNR) & 1, true)) break;
-      if (lane == 0)
-        bulk_copy_to_cluster(r_dst0 + ir * kEntry, k_addr + ik * kEntry, (uint32_t)kEntry,
-                             r_full_peer + (uint32_t)ir * kBarStride);
-      // the other issuer starts its MMAs once the CTA's first QK has
+      if (qi == 0) {
+        // the peer's output half of the own rows (the K entry) into the
+        // peer's R entry, once the peer has released it
+        if (!warp_wait(cx, bar(sm.r_free[ir]), (k / kNR) & 1, true)) break;
+        if (lane == 0)
+          bulk_copy_to_cluster(r_dst0 + ir * kEntry, k_addr + ik * kEntry, (uint32_t)kEntry,
+                               r_full_peer + (uint32_t)ir * kBarStride);
+      }
+      // the second issuer starts its MMAs once the CTA's first QK half has
       // completed (as in the grid kernel)
-      if (k == qi && qi > 0 && !warp_wait(cx, bar(sm.qk0_done), 0)) break;
-      const int b = k % kSBufs;
-      if (!warp_wait(cx, bar(sm.s_empty[b]), ((k / kSBufs) & 1) ^ 1)) break;
+      if (k == 0 && qi > 0 && !warp_wait(cx, bar(sm.qk0_done), 0)) break;
+      // the S area is free once the softmax of tile k - 1 (the other
+      // warpgroup's) has read it
+      if (k > 0 && !warp_wait(cx, bar(sm.s_empty[(k - 1) & 1]), ((k - 1) >> 1) & 1)) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t d = tmem + kSCol + b * kNH;
+        const uint32_t d = tmem + kSCol + qi * kNH;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
+        for (int h8 = 0; h8 < 8; ++h8) {
+          const int kk = 8 * qi + h8;
           const int kb = kk >> 2;            // column block of the own rows
           const uint32_t blk = (kb >> 1) == (int)rank ? v_addr + iv * kEntry + (kb & 1) * kRegion
                                                       : k_addr + ik * kEntry + (kb & 1) * kRegion;
           const uint64_t kd = desc_sw128(blk + (kk & 3) * 32, 16, 1024);
-          mma_tmem_a<true>(d, tmem + kQCol + kk * 8, kd, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_tmem_a<true>(d, tmem + kQCol + kk * 8, kd, idesc_qk, h8 > 0 ? 1u : 0u);
         }
-        mma_commit(bar(sm.s_full[b]));
-        mma_commit(bar(sm.k_empty[ik]));     // this CTA's read of the K entry
-        if (k == 0) mma_commit(bar(sm.qk0_done));
+        mma_commit(bar(sm.s_full[k & 1]));   // (two commits per tile)
+        mma_commit(bar(sm.k_empty[ik]));     // this CTA's reads of the K entry
+        if (k == 0 && qi == 0) mma_commit(bar(sm.qk0_done));
       }
       __syncwarp();
-      // the peer's copy of tile k has landed here: tell the peer (its K
-      // entry's other reader), then the PV warp (which waits for this, so
-      // that the entry's next phase cannot complete before this wait)
-      if (!warp_wait(cx, bar(sm.r_full[ir]), (k / kNR) & 1, true)) break;
-      if (lane == 0) {
-        mbar_arrive_cluster_relaxed(k_empty_peer + (uint32_t)ik * kBarStride);
-        mbar_arrive(bar(sm.r_seen[ir]));
+      if (qi == 0) {
+        // the peer's copy of tile k has landed here: tell the peer (its K
+        // entry's other reader), then the PV warp (which waits for this, so
+        // that the entry's next phase cannot complete before this wait)
+        if (!warp_wait(cx, bar(sm.r_full[ir]), (k / kNR) & 1, true)) break;
+        if (lane == 0) {
+          mbar_arrive_cluster_relaxed(k_empty_peer + (uint32_t)ik * kBarStride);
+          mbar_arrive(bar(sm.r_seen[ir]));
+        }
       }
     }
     if (lane == 0) mma_commit(bar(sm.qk_done));
@@ -820,18 +832,27 @@ decode_tc_slot_kernel(const __grid_constant__ SlotParams P) {
       tc_fence_after();
       float sv[kNH];
       if (active) {
+        // the two QK halves' partial logits (dims 0-255 and 256-511)
 #pragma unroll
         for (int hb = 0; hb < kNH / 32; ++hb) {
           uint32_t r[32];
-          tmem_ld32(tl + kSCol + sb * kNH + hb * 32, r);
+          tmem_ld32(tl + kSCol + hb * 32, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) sv[hb * 32 + i] = __uint_as_float(r[i]);
         }
         tmem_wait_ld();
+#pragma unroll
+        for (int hb = 0; hb < kNH / 32; ++hb) {
+          uint32_t r[32];
+          tmem_ld32(tl + kSCol + kNH + hb * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sv[hb * 32 + i] += __uint_as_float(r[i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(sm.s_empty[sb]));     // S buffer sb may be overwritten
+      if (lane == 0) mbar_arrive(bar(sm.s_empty[sb]));     // the S area may be overwritten (by tile j + 1)
       // ---- this CTA's tile maximum to the peer, the peer's back
       float mt = -INFINITY;
       if (active) {
