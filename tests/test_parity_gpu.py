@@ -155,6 +155,22 @@ def test_mixed_prefill_and_decode_batch(kernel, dtype, H, q_lens, width):
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("kernel", [B.KERNEL_TCGEN05, B.KERNEL_TCGEN05_SLOT_SPLIT])
+def test_e4m3_exact_maximum_boundary(kernel):
+    """E4M3 P: a split of at most 512 valid slots follows the exact running
+    maximum, a longer one the lazy reference (threshold 2^8).  Tokens of 511,
+    512 and 513 valid slots in one unsplit call, on both tensor-core kernels."""
+    w = small_case(31, dtype="e4m3", H=128, width=128 + 400, batch=3, holes=False,
+                   topk=np.array([511, 512, 513]))
+    counts = [len(oracle.valid_slots(t, indices=w.indices, topk_lens=w.topk_lens, seq_lens=w.seq_lens,
+                                     cum_seq_lens_q=None, batch=w.batch, swa_rows=w.swa_kv.shape[0],
+                                     comp_rows=w.comp_kv.shape[0])) for t in range(w.sum_q)]
+    assert counts == [511, 512, 513]
+    out, lse, plan = run_gpu(w, kernel=kernel, num_splits=1)
+    assert plan["num_splits"] == 1
+    compare(w, out, lse)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_swa_only_width_128(kernel):
     w = small_case(8, dtype="e4m3", H=128, width=128, holes=False, topk="none")
